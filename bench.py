@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark: chunked causal linear attention, forward + backward, on GB300.
+
+One step = the whole hot path over one batch: la_chunked_fwd then la_chunked_bwd on
+the Fractus-1B block shape (B=4, levels=2, heads=20 -> G=160 groups, C=128 tokens,
+head size D=64, block=64, bf16 inputs, fp32 carry, carry active), synthetic seeded
+inputs.  Metric: G*C tokens per second (groups x tokens processed per second).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timed region: W eager warm-up steps, then EXACTLY K steps replayed from CUDA graphs,
+bracketed by a barrier and cudaDeviceSynchronize, timed with CUDA events on the
+launching stream, max over ranks.  The steps cycle through enough input/output buffer
+sets that the working set is over 4x the L2 size, so every step reads HBM.
+One JSON line is printed by rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(G=160, C=128, D=64, block=64, dtype="bf16", eps=1e-6)
+WORKLOAD_NAME = "fractus1b_block: G=160 (B=4 x 2 levels x 20 heads), C=128, D=64, block=64, bf16, fwd+bwd"
+METRIC = "linear-attn tokens·groups/s (G·C/s) fwd and fwd+bwd; % of binding roofline"
+UNIT = "G·C tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(G, C, D, esz):
+    """Bytes a launch must move at minimum (each input read once, each output written once)."""
+    state = (D * D + D) * 4
+    fwd = G * (3 * C * D * esz + C * D * esz + 2 * state)            # q,k,v in; o out; carry in + out
+    bwd = G * (4 * C * D * esz + 2 * state + 3 * C * D * esz + state)  # q,k,v,dO,S0,z0,dS,dz in; dq,dk,dv,dS0,dz0 out
+    return fwd, bwd
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        if not rows:
+            return None
+        t0, t1 = self.window or (rows[0][0], rows[-1][0])
+        inside = [p for t, p in rows if t0 - 0.1 <= t <= t1 + 0.1] or [rows[-1][1]]
+        sm = [float(p[1]) for p in inside if p[1].replace(".", "", 1).isdigit()]
+        smax = [float(p[2]) for p in inside if p[2].replace(".", "", 1).isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in inside for n, val in zip(names, p[5:9]) if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- our arm (GPU)
+class StepBuffers:
+    """Device inputs and outputs of one step."""
+
+    def __init__(self, src, G, C, D):
+        import torch
+        self.x = src
+        self.o = torch.empty_like(src.q)
+        self.S_out = torch.empty(G, D, D, device=src.q.device, dtype=torch.float32)
+        self.z_out = torch.empty(G, D, device=src.q.device, dtype=torch.float32)
+        self.grads = (torch.empty_like(src.q), torch.empty_like(src.q), torch.empty_like(src.q),
+                      torch.empty(G, D, D, device=src.q.device, dtype=torch.float32),
+                      torch.empty(G, D, device=src.q.device, dtype=torch.float32))
+
+    def nbytes(self):
+        ts = list(self.x.tensors().values()) + [self.o, self.S_out, self.z_out, *self.grads]
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import causal_linear_attention_gb300 as la
+    from causal_linear_attention_gb300.inputs import Inputs, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    la.build()
+    G, C, D, block, eps = (WORKLOAD[k] for k in ("G", "C", "D", "block", "eps"))
+    esz = 2
+    fwd_bytes, bwd_bytes = algorithmic_bytes(G, C, D, esz)
+
+    # one seeded set of inputs (each rank draws its own groups), replicated into enough
+    # buffer sets that the rotation touches > 4x L2 between two uses of a set
+    host = make_inputs(G, C, D, dtype="bf16", seed=1000 + rank, grads=True)
+    base = host.to(dev)
+    one = StepBuffers(base, G, C, D)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, -(-4 * l2 // one.nbytes()))
+    sets = [one] + [StepBuffers(Inputs(**{k: (None if t is None else t.clone()) for k, t in base.__dict__.items()}),
+                                G, C, D) for _ in range(nsets - 1)]
+
+    def fwd(b):
+        la.chunked_fwd(b.x.q, b.x.k, b.x.v, b.x.S0, b.x.z0, block=block, eps=eps, o=b.o, S_out=b.S_out,
+                       z_out=b.z_out)
+
+    def bwd(b):
+        la.chunked_bwd(b.x.q, b.x.k, b.x.v, b.x.S0, b.x.z0, b.x.dO, b.x.dS_out, b.x.dz_out, block=block, eps=eps,
+                       out=b.grads)
+
+    def step(b):
+        fwd(b)
+        bwd(b)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(sets[i % nsets])
+    torch.cuda.synchronize()
+
+    def capture(fn, n, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(sets[(offset + i) % nsets])
+        return g
+
+    chunk = min(args.steps, 512)
+
+    def timed(fn, steps):
+        """Replay `steps` calls of fn from CUDA graphs; returns device seconds (this rank)."""
+        full, rest = divmod(steps, chunk)
+        g_full = capture(fn, chunk) if full else None
+        g_rest = capture(fn, rest, offset=full * chunk) if rest else None
+        if g_full is not None:  # one untimed replay: graph upload / first-launch costs
+            g_full.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(full):
+                g_full.replay()
+            if g_rest is not None:
+                g_rest.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1) / 1e3
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall0 = time.time()
+    secs = max_over_ranks(timed(step, args.steps))
+    clocks.mark(t_wall0, time.time())
+    clock_info = clocks.stop()
+
+    # per-kernel average launch durations (same rotation, same stream)
+    n_k = max(args.steps, 64)
+    fwd_secs = max_over_ranks(timed(fwd, n_k)) / n_k
+    bwd_secs = max_over_ranks(timed(bwd, n_k)) / n_k
+
+    # end to end through the public API: pinned host inputs -> device -> fwd + bwd -> host outputs
+    e2e = run_e2e(args, host, one, fwd, bwd, stream, barrier, max_over_ranks, G, C)
+
+    tokens = G * C
+    value = world * tokens * args.steps / secs
+    hbm, peak_src = measured_peaks()
+    kernels = {
+        "la_fwd": {"avg_us": fwd_secs * 1e6, "alg_bytes": fwd_bytes, "gbs": fwd_bytes / fwd_secs / 1e9},
+        "la_bwd": {"avg_us": bwd_secs * 1e6, "alg_bytes": bwd_bytes, "gbs": bwd_bytes / bwd_secs / 1e9},
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["avg_us"])
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(kernels[dom]["gbs"], 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / hbm, 4), "peak_source": peak_src,
+            "traffic": None}
+    for k in kernels:
+        kernels[k]["frac"] = round(kernels[k]["gbs"] / hbm, 4)
+        kernels[k]["avg_us"] = round(kernels[k]["avg_us"], 3)
+        kernels[k]["gbs"] = round(kernels[k]["gbs"], 1)
+    fwd_only = world * tokens / fwd_secs
+
+    out = None
+    if rank == 0:
+        cpu = cpu_baseline(host, G, C, D, eps)
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "G_per_gpu": G, "C": C, "D": D, "block": block, "eps": eps,
+                       "step": "la_chunked_fwd + la_chunked_bwd", "parallelism": f"groups sharded, {world} rank(s)",
+                       "l2": f"rotating {nsets} buffer sets ({nsets * one.nbytes() / 2**20:.0f} MiB > 4x L2 "
+                             f"{l2 / 2**20:.0f} MiB)", "timing": "CUDA graphs, CUDA events, max over ranks"},
+            "fwd_only": {"value": fwd_only, "unit": UNIT, "us_per_launch": kernels["la_fwd"]["avg_us"]},
+            "roofline": roof, "kernels": kernels, "e2e": e2e, "gpu_launches": 2 * args.steps,
+            "clocks": clock_info, "cpu_baseline": cpu,
+        }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
+
+
+def run_e2e(args, host, one, fwd, bwd, stream, barrier, max_over_ranks, G, C):
+    import torch
+    pinned_in = {k: t.pin_memory() for k, t in host.tensors().items()}
+    outs = [one.o, one.S_out, one.z_out, *one.grads]
+    pinned_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+    dev_in = one.x.tensors()
+
+    def e2e_step():
+        for k, t in pinned_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        fwd(one)
+        bwd(one)
+        for d, h in zip(outs, pinned_out):
+            h.copy_(d, non_blocking=True)
+
+    n = min(args.steps, 1000)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            e2e_step()
+    torch.cuda.synchronize()
+    secs = max_over_ranks(time.perf_counter() - t0)
+    barrier()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * G * C * n / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "api": "causal_linear_attention_gb300.chunked_fwd/chunked_bwd, pinned host buffers"}
+
+
+# ---------------------------------------------------------------- the oracle on the host cores
+def oracle_step(x, eps):
+    import oracle
+    oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=eps)
+    oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=eps)
+
+
+def cpu_baseline(host, G, C, D, eps, budget_s=10.0):
+    """The fp64 oracle (as it stands) on this host's cores: full fwd+bwd of the same
+    workload, repeated until `budget_s` seconds of work have run."""
+    import oracle
+    oracle.build()
+    oracle_step(host, eps)  # warm (page-in, thread pool)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(host, eps)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": G * C * reps / el, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"{reps} x full fwd+bwd of the workload (G={G}, C={C}, D={D}) in fp64, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 oracle on the host cores, same workload/metric/unit.
+    Under torchrun only rank 0 runs it."""
+    if rank != 0:
+        return None
+    import oracle
+    from causal_linear_attention_gb300.inputs import make_inputs
+    G, C, D, eps = (WORKLOAD[k] for k in ("G", "C", "D", "eps"))
+    oracle.build()
+    host = make_inputs(G, C, D, dtype="bf16", seed=1000, grads=True)
+    # each step: a bounded sample of the workload sized so the whole run takes a few minutes
+    t0 = time.perf_counter()
+    oracle_step(host, eps)
+    one = time.perf_counter() - t0
+    budget_per_step = 120.0 / max(1, args.steps + args.warmup)
+    g_sample = max(1, min(G, int(G * budget_per_step / max(one, 1e-9))))
+    sample = make_inputs(g_sample, C, D, dtype="bf16", seed=1000, grads=True)
+    for _ in range(args.warmup):
+        oracle_step(sample, eps)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sample, eps)
+    secs = time.perf_counter() - t0
+    value = g_sample * C * args.steps / secs
+    desc = f"{g_sample} of {G} groups per step (C={C}, D={D}), fp64 fwd+bwd"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "G_per_step": g_sample, "C": C, "D": D, "block": WORKLOAD["block"],
+                   "eps": eps, "step": "oracle fwd + bwd (per-token fp64 loop, OpenMP over groups)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "cpu": cpu_model(), "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    rank, world, local = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

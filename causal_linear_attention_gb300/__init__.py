@@ -1,0 +1,91 @@
+"""Chunked causal linear attention with a carried running state, for GB300 (sm_103a).
+
+Per group g (G = B * levels * heads independent problems) and token t, with
+S_t = S0 + sum_{j<=t} k_j v_j^T and z_t = z0 + sum_{j<=t} k_j (inclusive of t):
+
+    o_t = (q_t^T S_t) / (q_t . z_t + eps),    final carry (S_{C-1}, z_{C-1})
+
+("Fractus-1B training optimization -- 2026-08-22", section 2 "Opt 2": a masked
+block x block score matrix inside a block plus the running state across blocks;
+backward = the reverse cumsum of section 1.)  The kernels live in libla.so behind
+the C ABI of include/la.h; this package only marshals arguments.
+
+    import causal_linear_attention_gb300 as la
+    o, S, z = la.chunked_fwd(q, k, v, S0, z0, block=64)          # q, k, v: [G, C, D] cuda
+    dq, dk, dv, dS0, dz0 = la.chunked_bwd(q, k, v, S0, z0, dO, dS, dz, block=64)
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+from . import _lib
+from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
+                   la_status_string, la_version, lib)
+
+__all__ = ["chunked_fwd", "chunked_bwd", "la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c",
+           "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    if t.dtype == torch.float32:
+        return LA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    if t.shape != shape or t.dtype != dtype or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {tuple(shape)} {dtype} on {device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+def chunked_fwd(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float = 1e-6,
+                o=None, S_out=None, z_out=None, stream=None):
+    """Forward of one chunk.  q, k, v: contiguous [G, C, D] bf16 or fp32 CUDA tensors;
+    S0 [G, D, D], z0 [G, D] fp32 or None (zero carry).  Returns (o, S_out, z_out);
+    pass S_out=S0, z_out=z0 to thread the carry in place."""
+    import torch
+    G, C, D = q.shape
+    dt = q.dtype
+    for n, t in (("k", k), ("v", v)):
+        _check_tensor(n, t, q.shape, dt, q.device)
+    _check_tensor("q", q, q.shape, dt, q.device)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, q.device)
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(G, D, D, device=q.device, dtype=torch.float32) if S_out is None else S_out
+    z_out = torch.empty(G, D, device=q.device, dtype=torch.float32) if z_out is None else z_out
+    la_chunked_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, _dtype_code(q), eps, _stream(stream))
+    return o, S_out, z_out
+
+
+def chunked_bwd(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 64, eps: float = 1e-6,
+                out: Optional[tuple] = None, stream=None):
+    """Backward of chunked_fwd, recomputed from its inputs.  Returns (dq, dk, dv, dS0, dz0)."""
+    import torch
+    G, C, D = q.shape
+    dt = q.dtype
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _check_tensor(n, t, q.shape, dt, q.device)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D)), ("dS_out", dS_out, (G, D, D)),
+                      ("dz_out", dz_out, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q),
+               torch.empty(G, D, D, device=q.device, dtype=torch.float32),
+               torch.empty(G, D, device=q.device, dtype=torch.float32))
+    dq, dk, dv, dS0, dz0 = out
+    la_chunked_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block,
+                   _dtype_code(q), eps, _stream(stream))
+    return dq, dk, dv, dS0, dz0

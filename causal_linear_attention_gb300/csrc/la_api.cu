@@ -1,0 +1,263 @@
+// la_api.cu -- the C ABI of include/la.h: argument checks, kernel selection, launch.
+//
+// One kernel per (dtype, D, block); each CTA owns one group (G CTAs per call), so no
+// two CTAs ever touch the same output element and results are bitwise reproducible.
+#include "la.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "la_bwd.cuh"
+#include "la_fwd.cuh"
+
+namespace {
+
+using la::Bf16Mma;
+using la::F32Simt;
+
+constexpr int kMaxDevices = 64;
+
+// Dynamic shared memory above 48 KB needs an explicit opt-in per kernel and device.
+struct OptIn {
+    std::atomic<uint64_t> done{0};
+};
+
+int smem_optin_limit(int* dev_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int lim = 0;
+    if (cudaDeviceGetAttribute(&lim, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return -1;
+    if (dev_out) *dev_out = dev;
+    return lim;
+}
+
+// Returns LA_OK, LA_ERR_UNSUPPORTED (does not fit) or LA_ERR_CUDA.
+template <class K>
+la_status prepare(K kernel, OptIn& flag, size_t smem)
+{
+    int dev = 0;
+    const int lim = smem_optin_limit(&dev);
+    if (lim < 0) return LA_ERR_CUDA;
+    if (smem > (size_t)lim) return LA_ERR_UNSUPPORTED;
+    if (dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
+    const uint64_t bit = 1ull << dev;
+    if (!(flag.done.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
+            return LA_ERR_CUDA;
+        flag.done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return LA_OK;
+}
+
+la_status launched()
+{
+    return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+template <class P, int D, int BK, int NW, int ST>
+la_status fwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                     float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    using T = typename P::T;
+    using L = la::FwdLayout<P, D, BK, NW, ST>;
+    static OptIn flag;
+    auto kern = la::la_fwd_kernel<P, D, BK, NW, ST>;
+    const la_status st = prepare(kern, flag, L::BYTES);
+    if (st != LA_OK) return st;
+    kern<<<G, NW * 32, L::BYTES, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
+                                            static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out,
+                                            z_out, C, eps);
+    return launched();
+}
+
+template <class P, int D, int BK, int NW, int ST, bool ALIAS>
+size_t bwd_fixed_bytes()
+{
+    return la::BwdLayout<P, D, BK, NW, ST, ALIAS>::bytes(0);
+}
+
+template <class P, int D, int BK, int NW, int ST, bool ALIAS>
+la_status bwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                     const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv,
+                     float* dS0, float* dz0, int G, int C, float eps, cudaStream_t stream)
+{
+    using T = typename P::T;
+    using L = la::BwdLayout<P, D, BK, NW, ST, ALIAS>;
+    static OptIn flag;
+    auto kern = la::la_bwd_kernel<P, D, BK, NW, ST, ALIAS>;
+    const size_t smem = L::bytes(C);
+    const la_status st = prepare(kern, flag, smem);
+    if (st != LA_OK) return st;
+    kern<<<G, NW * 32, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
+                                        static_cast<const T*>(v), S0, z0, static_cast<const T*>(dO), dS_out,
+                                        dz_out, static_cast<T*>(dq), static_cast<T*>(dk), static_cast<T*>(dv),
+                                        dS0, dz0, C, eps);
+    return launched();
+}
+
+// ---------------------------------------------------------------- kernel table
+// (dtype, D, block) -> instantiation.  NW = warps per CTA, ST = pipeline stages.
+#define LA_FWD_TABLE(X)                  \
+    X(LA_BF16, Bf16Mma, 64, 64, 8, 2)    \
+    X(LA_BF16, Bf16Mma, 128, 64, 8, 2)   \
+    X(LA_BF16, Bf16Mma, 64, 128, 8, 2)   \
+    X(LA_BF16, Bf16Mma, 128, 128, 16, 1) \
+    X(LA_F32, F32Simt, 64, 64, 8, 2)     \
+    X(LA_F32, F32Simt, 128, 64, 8, 1)    \
+    X(LA_F32, F32Simt, 64, 128, 8, 1)
+
+#define LA_BWD_TABLE(X)                         \
+    X(LA_BF16, Bf16Mma, 64, 64, 8, 2, false)    \
+    X(LA_BF16, Bf16Mma, 128, 64, 16, 1, false)  \
+    X(LA_BF16, Bf16Mma, 64, 128, 16, 1, false)  \
+    X(LA_BF16, Bf16Mma, 128, 128, 16, 1, true)  \
+    X(LA_F32, F32Simt, 64, 64, 8, 1, false)
+
+// ---------------------------------------------------------------- argument checks
+struct Buf {
+    const void* p;
+    size_t bytes;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const Buf& a, const Buf& b)
+{
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Every output must be disjoint from every other buffer, except the listed exact
+// in-place pairs (an output pointer equal to its matching input pointer).
+bool disjoint(const Buf* outs, int n_out, const Buf* ins, int n_in, const int* inplace_in)
+{
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_out; ++j)
+            if (i != j && overlaps(outs[i], outs[j])) return false;
+        for (int j = 0; j < n_in; ++j) {
+            if (!overlaps(outs[i], ins[j])) continue;
+            const bool same = inplace_in[i] == j && outs[i].p == ins[j].p && outs[i].bytes == ins[j].bytes;
+            if (!same) return false;
+        }
+    }
+    return true;
+}
+
+la_status check_common(int G, int C, int D, int block, la_dtype dtype, float eps, size_t* esz)
+{
+    if (G < 0 || C < 0) return LA_ERR_INVALID;
+    if (!std::isfinite(eps)) return LA_ERR_INVALID;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if ((D != 64 && D != 128) || (block != 64 && block != 128)) return LA_ERR_UNSUPPORTED;
+    // element counts must stay far inside 64-bit byte offsets
+    if ((double)G * (double)C * (double)D > 4.0e15) return LA_ERR_INVALID;
+    *esz = dtype == LA_F32 ? 4 : 2;
+    return LA_OK;
+}
+
+bool ptrs_ok(const void* const* ps, int n, const bool* required)
+{
+    for (int i = 0; i < n; ++i) {
+        if (!ps[i]) {
+            if (required[i]) return false;
+            continue;
+        }
+        if (!aligned16(ps[i])) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                    void* o, float* S_out, float* z_out, int G, int C, int D, int block,
+                                    la_dtype dtype, float eps, void* stream)
+{
+    size_t esz = 0;
+    la_status st = check_common(G, C, D, block, dtype, eps, &esz);
+    if (st != LA_OK) return st;
+    const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    const bool has_tokens = n_x > 0;
+    const void* ps[] = {q, k, v, o, S0, z0, S_out, z_out};
+    const bool req[] = {has_tokens, has_tokens, has_tokens, has_tokens, false, false, false, false};
+    if (!ptrs_ok(ps, 8, req)) return LA_ERR_INVALID;
+    const Buf ins[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}};
+    const Buf outs[] = {{o, n_x}, {S_out, n_S}, {z_out, n_z}};
+    const int inplace[] = {-1, 3, 4};
+    if (!disjoint(outs, 3, ins, 5, inplace)) return LA_ERR_INVALID;
+    if (G == 0) return LA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+#define LA_FWD_CASE(DT, P, DD, BB, NW, ST)                                                                  \
+    if (dtype == DT && D == DD && block == BB)                                                             \
+        return fwd_launch<P, DD, BB, NW, ST>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+    LA_FWD_TABLE(LA_FWD_CASE)
+#undef LA_FWD_CASE
+    return LA_ERR_UNSUPPORTED;
+}
+
+extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                    const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk,
+                                    void* dv, float* dS0, float* dz0, int G, int C, int D, int block,
+                                    la_dtype dtype, float eps, void* stream)
+{
+    size_t esz = 0;
+    la_status st = check_common(G, C, D, block, dtype, eps, &esz);
+    if (st != LA_OK) return st;
+    const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    const bool t = n_x > 0;
+    const void* ps[] = {q, k, v, dO, dq, dk, dv, S0, z0, dS_out, dz_out, dS0, dz0};
+    const bool req[] = {t, t, t, t, t, t, t, false, false, false, false, false, false};
+    if (!ptrs_ok(ps, 13, req)) return LA_ERR_INVALID;
+    const Buf ins[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}, {dO, n_x}, {dS_out, n_S}, {dz_out, n_z}};
+    const Buf outs[] = {{dq, n_x}, {dk, n_x}, {dv, n_x}, {dS0, n_S}, {dz0, n_z}};
+    const int inplace[] = {-1, -1, -1, 6, 7};
+    if (!disjoint(outs, 5, ins, 8, inplace)) return LA_ERR_INVALID;
+    if (G == 0) return LA_OK;
+    if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+#define LA_BWD_CASE(DT, P, DD, BB, NW, ST, AL)                                                               \
+    if (dtype == DT && D == DD && block == BB)                                                              \
+        return bwd_launch<P, DD, BB, NW, ST, AL>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, \
+                                                 C, eps, s);
+    LA_BWD_TABLE(LA_BWD_CASE)
+#undef LA_BWD_CASE
+    return LA_ERR_UNSUPPORTED;
+}
+
+extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
+{
+    const int lim = smem_optin_limit(nullptr);
+    if (lim < 0) {
+        cudaGetLastError();  // leave no sticky "no device" error behind
+        return 0;
+    }
+#define LA_BWD_MAXC(DT, P, DD, BB, NW, ST, AL)                                   \
+    if (dtype == DT && D == DD && block == BB) {                                 \
+        const size_t fixed = bwd_fixed_bytes<P, DD, BB, NW, ST, AL>();           \
+        return fixed >= (size_t)lim ? 0 : (int)(((size_t)lim - fixed) / 8);      \
+    }
+    LA_BWD_TABLE(LA_BWD_MAXC)
+#undef LA_BWD_MAXC
+    return 0;
+}
+
+extern "C" const char* la_status_string(la_status status)
+{
+    switch (status) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID: return "invalid argument (null, misaligned or overlapping pointer, or negative size)";
+    case LA_ERR_UNSUPPORTED: return "unsupported D, block, dtype or chunk length";
+    case LA_ERR_CUDA: return "CUDA launch failed";
+    case LA_ERR_TIMEOUT: return "bounded on-device wait gave up";
+    }
+    return "unknown status";
+}
+
+extern "C" int la_version(void) { return 100; }

@@ -1,0 +1,117 @@
+/*
+ * la.h -- C ABI of the chunked causal linear attention library (libla.so).
+ *
+ * Method: "Fractus-1B training optimization -- 2026-08-22".
+ *   Section 1, "Bottleneck #1": per group, the running state is the causal
+ *   cumulative sum of outer products (the page's masked einsum
+ *   "tj,bjpq->btpq"); its derivative is a reverse cumsum.
+ *   Section 2, "Opt 2": the chunked form -- inside a block of `block` tokens a
+ *   masked block x block score matrix, across blocks the running state
+ *   (S_run, z_run), updated inclusively AFTER the block has read it; a ragged
+ *   last block is computed exactly.
+ *   Section 2, "Opt 6": the carry (S, z) is read at the start of a chunk and
+ *   handed on at its end (carry_S_flat, carry_z_flat -> S_final, z_final).
+ * The page does not print the output normalisation; this library computes,
+ * for every group g and token t (0-based, inclusive of t):
+ *     S_t = S0 + sum_{j<=t} k_j v_j^T          S[p][c]: p = key dim, c = value dim
+ *     z_t = z0 + sum_{j<=t} k_j
+ *     o_t[c] = sum_p q_t[p] S_t[p][c] / (q_t . z_t + eps)
+ * and the final carry S_out = S_{C-1}, z_out = z_{C-1} (S0, z0 when C == 0).
+ * eps is added as given (no clamp); it receives no gradient.  Inputs with
+ * q_t . z_t + eps == 0 divide by zero (IEEE result, no error).
+ *
+ * Layouts: row-major and contiguous, no strides.
+ *   q, k, v, o, dO, dq, dk, dv : [G][C][D]  of the element type `dtype`
+ *   S0, S_out, dS_out, dS0     : [G][D][D]  float32
+ *   z0, z_out, dz_out, dz0     : [G][D]     float32
+ *
+ * Ownership: every pointer is DEVICE memory owned by the caller.  The library
+ * allocates nothing, keeps no state between calls and never synchronises the
+ * stream.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) and is complete when the stream is.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; a
+ * failed check returns LA_ERR_INVALID or LA_ERR_UNSUPPORTED and enqueues
+ * nothing.  LA_ERR_CUDA means the launch itself failed (the CUDA error is
+ * available from cudaGetLastError()).  Calls are thread-safe.
+ *
+ * Supported: D in {64, 128}; block in {64, 128}; G >= 0; C >= 0 (any C: the
+ * last block may be ragged).  Every pointer 16-byte aligned.  float32 inputs
+ * (LA_F32) compute in float32 throughout; bfloat16 inputs (LA_BF16) use
+ * bfloat16 tensor-core products with float32 accumulation and a float32
+ * state.  LA_F32 supports (D, block) = (64, 64), (128, 64), (64, 128) in the
+ * forward and (64, 64) in the backward; other combinations return
+ * LA_ERR_UNSUPPORTED.  The backward keeps two floats per token of the chunk in
+ * shared memory, so its C is bounded: la_bwd_max_c() gives the bound (several
+ * thousand tokens for D = 64).
+ */
+#ifndef LA_H
+#define LA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_F32 = 0,   /* float32 q, k, v, o, dO, dq, dk, dv */
+    LA_BF16 = 1   /* bfloat16 q, k, v, o, dO, dq, dk, dv */
+} la_dtype;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID = 1,      /* a NULL/misaligned/overlapping pointer or a negative size */
+    LA_ERR_UNSUPPORTED = 2,  /* a valid but unsupported D, block, dtype or C */
+    LA_ERR_CUDA = 3,         /* the CUDA launch failed */
+    LA_ERR_TIMEOUT = 4       /* reserved: a bounded on-device wait gave up */
+} la_status;
+
+/*
+ * Forward of one chunk for G independent groups (Opt 2 of the page).
+ *   q, k, v  [G][C][D] dtype, inputs.  k and v rows beyond C are never read.
+ *   S0, z0   incoming carry, float32; NULL means a zero carry.
+ *   o        [G][C][D] dtype, output.
+ *   S_out, z_out  outgoing carry, float32; NULL skips that output.
+ *            S_out may be the same pointer as S0 and z_out the same as z0
+ *            (in-place carry threading); any other overlap is rejected.
+ *   eps      added to every denominator.
+ */
+la_status la_chunked_fwd(const void* q, const void* k, const void* v,
+                         const float* S0, const float* z0,
+                         void* o, float* S_out, float* z_out,
+                         int G, int C, int D, int block, la_dtype dtype, float eps,
+                         void* stream);
+
+/*
+ * Backward of la_chunked_fwd (the reverse cumsum of section 1), recomputed
+ * from the forward's inputs: nothing saved by the forward is needed.
+ *   q, k, v, S0, z0  as passed to la_chunked_fwd (S0/z0 NULL = zero carry).
+ *   dO       [G][C][D] dtype, gradient of the loss w.r.t. o.
+ *   dS_out, dz_out   gradient w.r.t. the outgoing carry, float32; NULL = zero.
+ *   dq, dk, dv       [G][C][D] dtype, outputs.
+ *   dS0, dz0         [G][D][D], [G][D] float32 gradients w.r.t. the incoming
+ *                    carry; NULL skips.  dS0 may be the same pointer as
+ *                    dS_out and dz0 the same as dz_out.
+ * C must not exceed la_bwd_max_c(D, block, dtype) (else LA_ERR_UNSUPPORTED).
+ */
+la_status la_chunked_bwd(const void* q, const void* k, const void* v,
+                         const float* S0, const float* z0,
+                         const void* dO, const float* dS_out, const float* dz_out,
+                         void* dq, void* dk, void* dv, float* dS0, float* dz0,
+                         int G, int C, int D, int block, la_dtype dtype, float eps,
+                         void* stream);
+
+/* Largest C la_chunked_bwd accepts for this shape on the current device; 0 if
+ * the shape or dtype is unsupported or no device is available. */
+int la_bwd_max_c(int D, int block, la_dtype dtype);
+
+/* Static, NUL-terminated description of a status code. */
+const char* la_status_string(la_status status);
+
+/* Library version, e.g. 100 for 1.0.0. */
+int la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

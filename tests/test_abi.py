@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads and exports every symbol include/la.h declares;
+host-side argument checks reject bad calls before anything touches a GPU."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import causal_linear_attention_gb300 as la
+from causal_linear_attention_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "la.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None, reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def L():
+    la.build()
+    return la.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c",
+                                           "la_status_string", "la_version"])
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(_lib.EXPORTS) == set(declared_functions())
+
+
+def test_status_strings_and_version(L):
+    assert la.la_version() == 100
+    for s in range(5):
+        assert len(la.la_status_string(s)) > 0
+
+
+# Fake, 16-byte aligned "device" addresses.  Every call below must fail its host-side
+# checks (so nothing is ever launched on them, with or without a GPU present).
+A = 0x10000
+
+
+def fwd(**kw):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, S0=None, z0=None, o=A + 0x300000, S_out=None,
+                z_out=None, G=2, C=8, D=64, block=64, dtype=la.LA_BF16, eps=1e-6)
+    args.update(kw)
+    L = la.lib()
+    return L.la_chunked_fwd(args["q"], args["k"], args["v"], args["S0"], args["z0"], args["o"],
+                            args["S_out"], args["z_out"], args["G"], args["C"], args["D"], args["block"],
+                            args["dtype"], args["eps"], None)
+
+
+def bwd(**kw):
+    base = {n: A + i * 0x100000 for i, n in enumerate(("q", "k", "v", "dO", "dq", "dk", "dv"))}
+    args = dict(base, S0=None, z0=None, dS_out=None, dz_out=None, dS0=None, dz0=None, G=2, C=8, D=64,
+                block=64, dtype=la.LA_BF16, eps=1e-6)
+    args.update(kw)
+    L = la.lib()
+    return L.la_chunked_bwd(args["q"], args["k"], args["v"], args["S0"], args["z0"], args["dO"],
+                            args["dS_out"], args["dz_out"], args["dq"], args["dk"], args["dv"], args["dS0"],
+                            args["dz0"], args["G"], args["C"], args["D"], args["block"], args["dtype"],
+                            args["eps"], None)
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(C=-5), INVALID), (dict(q=None), INVALID), (dict(o=None), INVALID),
+    (dict(q=A + 4), INVALID), (dict(eps=float("nan")), INVALID), (dict(eps=float("inf")), INVALID),
+    (dict(D=32), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(block=32), UNSUPPORTED),
+    (dict(dtype=7), UNSUPPORTED),
+    (dict(o=A), INVALID),                       # output overlaps q
+    (dict(S0=A + 0x400000, S_out=A + 0x400010), INVALID),  # partial overlap of the carry
+    (dict(z_out=A + 0x300000), INVALID),        # z_out inside o
+])
+def test_forward_argument_checks(L, kw, status):
+    assert fwd(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(dq=None), INVALID), (dict(dO=None), INVALID), (dict(dk=A + 8), INVALID),
+    (dict(D=48), UNSUPPORTED), (dict(block=256), UNSUPPORTED),
+    (dict(dq=A), INVALID),                      # dq overlaps q
+    (dict(dk=A + 0x400000, dv=A + 0x400000), INVALID),  # two outputs share memory
+    (dict(dS_out=A + 0x800000, dS0=A + 0x800040), INVALID),
+])
+def test_backward_argument_checks(L, kw, status):
+    assert bwd(**kw) == status
+
+
+def test_empty_problems_are_accepted_without_a_launch(L):
+    assert fwd(G=0) == 0
+    assert bwd(G=0) == 0
+    # G = 0 with NULL buffers is fine: there is nothing to read or write
+    assert fwd(G=0, q=None, k=None, v=None, o=None) == 0
+
+
+def test_raw_binding_raises_on_error(L):
+    with pytest.raises(la.LAError) as e:
+        la.la_chunked_fwd(A, A, A, None, None, A, None, None, 1, 8, 64, 64, la.LA_BF16, 1e-6)
+    assert e.value.status == 1  # o overlaps the inputs: rejected before any CUDA call
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.lib()

@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Workloads follow the Fractus-1B attention micro-benchmark shapes (G = B * 40 groups,
+C = 128 tokens, head size 64, carry active) plus wide heads and ragged chunks;
+inputs are seeded and synthetic (causal_linear_attention_gb300.inputs), the same
+bits go to both sides.  Metric and tolerances: tests/parity_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import causal_linear_attention_gb300 as la
+import oracle
+from causal_linear_attention_gb300.inputs import make_inputs
+from parity_util import check, max_rel
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+EPS = 1e-6
+FWD_NAMES = ("o", "S_out", "z_out")
+BWD_NAMES = ("dq", "dk", "dv", "dS0", "dz0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    la.build()
+    oracle.build()
+    yield
+
+
+def run_fwd(x, block, eps=EPS):
+    d = x.to(DEV)
+    out = la.chunked_fwd(d.q, d.k, d.v, d.S0, d.z0, block=block, eps=eps)
+    torch.cuda.synchronize()
+    return out
+
+
+def run_bwd(x, block, eps=EPS):
+    d = x.to(DEV)
+    out = la.chunked_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=block, eps=eps)
+    torch.cuda.synchronize()
+    return out
+
+
+def fwd_case(G, C, D, block, dtype, seed=0, carry=True):
+    x = make_inputs(G, C, D, dtype=dtype, seed=seed, carry=carry)
+    got = run_fwd(x, block)
+    ref = oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS)
+    return check(got, ref, dtype, FWD_NAMES)
+
+
+def bwd_case(G, C, D, block, dtype, seed=0, carry=True, upstream=True):
+    x = make_inputs(G, C, D, dtype=dtype, seed=seed, carry=carry, grads=True)
+    if not upstream:
+        x.dS_out = x.dz_out = None
+    got = run_bwd(x, block)
+    ref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
+    return check(got, ref, dtype, BWD_NAMES)
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_tiny_fp32_forward():
+    """G=8, C=128, D=64, block=64, fp32 in and out, eps=1e-6: 1e-4 on o, S_out, z_out."""
+    fwd_case(8, 128, 64, 64, "f32")
+
+
+def test_tiny_fp32_backward():
+    bwd_case(8, 128, 64, 64, "f32")
+
+
+def test_fractus1b_block_forward():
+    """B=4, niv=2, H=20 -> G=160, C=128, D=64, block=64, bf16."""
+    fwd_case(160, 128, 64, 64, "bf16")
+
+
+def test_fractus1b_forward_backward_b16():
+    """B=16 -> G=640, C=128, D=64, block=64, bf16 forward + backward."""
+    fwd_case(640, 128, 64, 64, "bf16", seed=2)
+    bwd_case(640, 128, 64, 64, "bf16", seed=2)
+
+
+def test_long_stream_carry_threaded():
+    """G=160, D=64, T=8192 as 64 chunks of C=128 with the carry threaded in place;
+    equals one pass of the oracle over all 8192 tokens."""
+    G, C, D, nchunk = 160, 128, 64, 64
+    T = C * nchunk
+    x = make_inputs(G, T, D, dtype="bf16", seed=3)
+    ref_o, ref_S, ref_z = oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS)
+    # chunk-major copies so that each chunk is a contiguous [G, C, D] tensor
+    qc, kc, vc = (t.view(G, nchunk, C, D).transpose(0, 1).contiguous().to(DEV) for t in (x.q, x.k, x.v))
+    S, z = x.S0.to(DEV).clone(), x.z0.to(DEV).clone()
+    o = torch.empty(nchunk, G, C, D, device=DEV, dtype=torch.bfloat16)
+    for c in range(nchunk):
+        la.chunked_fwd(qc[c], kc[c], vc[c], S, z, block=64, eps=EPS, o=o[c], S_out=S, z_out=z)
+    torch.cuda.synchronize()
+    o_full = o.transpose(0, 1).reshape(G, T, D)
+    check((o_full, S, z), (ref_o, ref_S, ref_z), "bf16", FWD_NAMES)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_wide_heads_forward_backward(block):
+    """G=320, C=256, D=128, bf16, block 64 and 128."""
+    fwd_case(320, 256, 128, block, "bf16", seed=4)
+    bwd_case(320, 256, 128, block, "bf16", seed=4)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_wide_heads_ragged_chunk(block):
+    """G=320, C=200, D=128: the last block is partial (exact in-kernel tail)."""
+    fwd_case(320, 200, 128, block, "bf16", seed=5)
+    bwd_case(320, 200, 128, block, "bf16", seed=5)
+
+
+# ------------------------------------------------------------------ shapes, tails, edge cases
+
+SHAPES = [(D, block) for D in (64, 128) for block in (64, 128)]
+
+
+@pytest.mark.parametrize("D,block", SHAPES)
+@pytest.mark.parametrize("C", [1, 15, 64, 65, 127, 130, 300])
+def test_bf16_shapes_and_tails(D, block, C):
+    fwd_case(5, C, D, block, "bf16", seed=C)
+    bwd_case(5, C, D, block, "bf16", seed=C)
+
+
+@pytest.mark.parametrize("D,block", [(64, 64), (128, 64), (64, 128)])
+@pytest.mark.parametrize("C", [1, 33, 128, 200])
+def test_fp32_forward_shapes(D, block, C):
+    fwd_case(3, C, D, block, "f32", seed=C + 1)
+
+
+@pytest.mark.parametrize("C", [1, 33, 128, 200])
+def test_fp32_backward_shapes(C):
+    bwd_case(3, C, 64, 64, "f32", seed=C + 2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_zero_carry_and_no_upstream_carry_grad(dtype):
+    fwd_case(4, 100, 64, 64, dtype, seed=7, carry=False)
+    bwd_case(4, 100, 64, 64, dtype, seed=7, carry=False, upstream=False)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_chunk_passes_carry_through(dtype):
+    x = make_inputs(3, 0, 64, dtype=dtype, seed=8, grads=True)
+    o, S, z = run_fwd(x, 64)
+    assert o.shape == (3, 0, 64)
+    assert torch.equal(S.cpu(), x.S0) and torch.equal(z.cpu(), x.z0)
+    g = run_bwd(x, 64)
+    assert torch.equal(g[3].cpu(), x.dS_out) and torch.equal(g[4].cpu(), x.dz_out)
+
+
+def test_single_group_full_size_and_many_groups():
+    fwd_case(1, 128, 64, 64, "bf16", seed=9)
+    fwd_case(1000, 64, 64, 64, "bf16", seed=10)
+
+
+def test_results_are_deterministic():
+    x = make_inputs(64, 200, 64, dtype="bf16", seed=11, grads=True)
+    a = run_fwd(x, 64) + run_bwd(x, 64)
+    b = run_fwd(x, 64) + run_bwd(x, 64)
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
+
+
+def test_in_place_carry_and_carry_grad():
+    x = make_inputs(6, 96, 64, dtype="bf16", seed=12, grads=True)
+    ref = oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS)
+    d = x.to(DEV)
+    S, z = d.S0.clone(), d.z0.clone()
+    o, S2, z2 = la.chunked_fwd(d.q, d.k, d.v, S, z, block=64, eps=EPS, S_out=S, z_out=z)
+    assert S2.data_ptr() == S.data_ptr()
+    # the backward reads the ORIGINAL carry
+    dS, dz = d.dS_out.clone(), d.dz_out.clone()
+    out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), dS, dz)
+    g = la.chunked_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, dS, dz, block=64, eps=EPS, out=out)
+    torch.cuda.synchronize()
+    check((o, S, z), ref, "bf16", FWD_NAMES)
+    gref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
+    check(g, gref, "bf16", BWD_NAMES)
+
+
+def test_block_size_changes_only_rounding():
+    x = make_inputs(16, 256, 64, dtype="f32", seed=13)
+    a = run_fwd(x, 64)
+    b = run_fwd(x, 128)
+    for u, w in zip(a, b):
+        assert max_rel(u, w) < 1e-5
+
+
+def test_gpu_rejects_bad_arguments_without_launching():
+    x = make_inputs(2, 16, 64, dtype="bf16", seed=14).to(DEV)
+    o = torch.empty_like(x.q)
+    with pytest.raises(la.LAError) as e:
+        la.la_chunked_fwd(x.q, x.k, x.v, None, None, x.q, None, None, 2, 16, 64, 64, la.LA_BF16, EPS)
+    assert e.value.status == 1
+    with pytest.raises(la.LAError) as e:
+        la.la_chunked_fwd(x.q, x.k, x.v, None, None, o, None, None, 2, 16, 96, 64, la.LA_BF16, EPS)
+    assert e.value.status == 2
+    limit = la.la_bwd_max_c(64, 64, la.LA_BF16)
+    assert limit >= 4096
+    with pytest.raises(la.LAError) as e:
+        la.la_chunked_bwd(x.q, x.k, x.v, None, None, x.q, None, None, o, torch.empty_like(o),
+                          torch.empty_like(o), None, None, 2, limit + 1, 64, 64, la.LA_BF16, EPS)
+    assert e.value.status in (1, 2)
+    torch.cuda.synchronize()
