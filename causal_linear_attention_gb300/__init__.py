@@ -20,9 +20,9 @@ from typing import Optional
 
 from . import _lib
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
-                   la_status_string, la_version, lib)
+                   la_device_status, la_status_string, la_version, lib)
 
-__all__ = ["chunked_fwd", "chunked_bwd", "la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c",
+__all__ = ["chunked_fwd", "chunked_bwd", "la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c", "la_device_status",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
 
 

@@ -81,6 +81,8 @@ def lib():
         L.la_chunked_fwd.restype = I
         L.la_chunked_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         L.la_chunked_bwd.restype = I
+        L.la_device_status.argtypes = [I]
+        L.la_device_status.restype = I
         L.la_bwd_max_c.argtypes = [I, I, I]
         L.la_bwd_max_c.restype = I
         L.la_status_string.argtypes = [I]
@@ -91,7 +93,8 @@ def lib():
         return L
 
 
-EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c", "la_status_string", "la_version")
+EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c", "la_device_status", "la_status_string",
+           "la_version")
 
 
 def _p(x) -> Optional[int]:
@@ -125,6 +128,11 @@ def la_chunked_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G:
 
 def la_bwd_max_c(D: int, block: int, dtype: int) -> int:
     return int(lib().la_bwd_max_c(D, block, dtype))
+
+
+def la_device_status(clear: bool = True) -> int:
+    """Synchronise the device; LA_ERR_TIMEOUT (4) if a kernel gave up a bounded wait."""
+    return int(lib().la_device_status(1 if clear else 0))
 
 
 def la_status_string(status: int) -> str:

@@ -4,14 +4,18 @@
 // two CTAs ever touch the same output element and results are bitwise reproducible.
 #include "la.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <utility>
 
 #include "la_bwd.cuh"
 #include "la_fwd.cuh"
+#include "la_fwd_tc.cuh"
 
 namespace {
 
@@ -58,6 +62,30 @@ la_status launched()
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
+// Every kernel is launched with programmatic stream serialization: it may start while
+// the previous kernel in the stream drains, runs its set-up (barriers, TMEM, constant
+// tiles), and waits in griddepcontrol.wait before it reads any input.
+template <class... KArgs, class... Args>
+la_status launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem, cudaStream_t stream,
+                     Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
+    return launched();
+}
+
 template <class P, int D, int BK, int NW, int ST>
 la_status fwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
                      float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
@@ -68,10 +96,8 @@ la_status fwd_launch(const void* q, const void* k, const void* v, const float* S
     auto kern = la::la_fwd_kernel<P, D, BK, NW, ST>;
     const la_status st = prepare(kern, flag, L::BYTES);
     if (st != LA_OK) return st;
-    kern<<<G, NW * 32, L::BYTES, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
-                                            static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out,
-                                            z_out, C, eps);
-    return launched();
+    return launch_pdl(kern, G, NW * 32, L::BYTES, stream, static_cast<const T*>(q), static_cast<const T*>(k),
+                      static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out, z_out, C, eps);
 }
 
 template <class P, int D, int BK, int NW, int ST, bool ALIAS>
@@ -92,11 +118,59 @@ la_status bwd_launch(const void* q, const void* k, const void* v, const float* S
     const size_t smem = L::bytes(C);
     const la_status st = prepare(kern, flag, smem);
     if (st != LA_OK) return st;
-    kern<<<G, NW * 32, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
-                                        static_cast<const T*>(v), S0, z0, static_cast<const T*>(dO), dS_out,
-                                        dz_out, static_cast<T*>(dq), static_cast<T*>(dk), static_cast<T*>(dv),
-                                        dS0, dz0, C, eps);
-    return launched();
+    return launch_pdl(kern, G, NW * 32, smem, stream, static_cast<const T*>(q), static_cast<const T*>(k),
+                      static_cast<const T*>(v), S0, z0, static_cast<const T*>(dO), dS_out, dz_out,
+                      static_cast<T*>(dq), static_cast<T*>(dk), static_cast<T*>(dv), dS0, dz0, C, eps);
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+// cuTensorMapEncodeTiled comes from the driver through the runtime's entry-point query,
+// so the library links only against the CUDA runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// [G][C][D] bf16 tensor seen as a 3-D map (x = feature, y = token, z = group); boxes of
+// 64 features x box_rows tokens, 128-byte swizzle.  Rows past C read as zero and are
+// never written by stores.
+bool tmap_bf16(CUtensorMap* map, const void* base, int G, int C, int D, int box_rows)
+{
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)C, (cuuint64_t)G};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)C * D * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                        float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    static OptIn flag;
+    auto kern = la::la_fwd_tc_kernel;
+    const la_status st = prepare(kern, flag, la::FwdTcLayout::BYTES);
+    if (st != LA_OK) return st;
+    CUtensorMap tq{}, tk{}, tv{};
+    if (C > 0) {
+        constexpr int R = la::FwdTcLayout::BOX_ROWS;
+        if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R))
+            return LA_ERR_CUDA;
+    }
+    return launch_pdl(kern, G, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, S0, z0,
+                      static_cast<__nv_bfloat16*>(o), S_out, z_out, C, eps);
 }
 
 // ---------------------------------------------------------------- kernel table
@@ -193,6 +267,10 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
     if (G == 0) return LA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    // bf16, head size 64: the tensor-core (tcgen05 / TMEM / TMA) kernel, 128-token score
+    // tiles for either block size (the block size changes only the rounding)
+    if (dtype == LA_BF16 && D == 64) return fwd_tc_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+
 #define LA_FWD_CASE(DT, P, DD, BB, NW, ST)                                                                  \
     if (dtype == DT && D == DD && block == BB)                                                             \
         return fwd_launch<P, DD, BB, NW, ST>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
@@ -246,6 +324,18 @@ extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
     LA_BWD_TABLE(LA_BWD_MAXC)
 #undef LA_BWD_MAXC
     return 0;
+}
+
+extern "C" la_status la_device_status(int clear)
+{
+    uint32_t word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&word, la::tc::g_status, sizeof(word)) != cudaSuccess) return LA_ERR_CUDA;
+    if (clear && word) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(la::tc::g_status, &zero, sizeof(zero)) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    return word ? LA_ERR_TIMEOUT : LA_OK;
 }
 
 extern "C" const char* la_status_string(la_status status)

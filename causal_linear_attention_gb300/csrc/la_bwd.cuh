@@ -121,6 +121,7 @@ la_bwd_kernel(const typename P::T* __restrict__ q, const typename P::T* __restri
     auto tile_S = [&](int t, int& m0, int& n0) { m0 = (t / (D / 32)) * 16; n0 = (t % (D / 32)) * 32; };
     auto ident = [](int, int, float x) { return x; };
 
+    pdl_wait();  // inputs may have been written by the previous kernel in the stream
     // carry in (forward sweep state)
     Acc Sacc[SPW];
 #pragma unroll
@@ -141,6 +142,7 @@ la_bwd_kernel(const typename P::T* __restrict__ q, const typename P::T* __restri
         if (needs_load(s)) load_step(s);
         cp_async_commit();
     }
+    pdl_launch_dependents();
 
     auto den_of = [&](int i) {
         float d = eps + qz[i];

@@ -81,6 +81,7 @@ la_fwd_kernel(const typename P::T* __restrict__ q, const typename P::T* __restri
     T* og = o + gofs;
     const int nb = (C + BK - 1) / BK;
 
+    pdl_wait();  // inputs may have been written by the previous kernel in the stream
     // carry in: state tiles of this warp, z, and the operand copy of the state
     Acc Sacc[SPW];
 #pragma unroll
@@ -106,6 +107,7 @@ la_fwd_kernel(const typename P::T* __restrict__ q, const typename P::T* __restri
         if (s < nb) load_block(s, s);
         cp_async_commit();
     }
+    pdl_launch_dependents();
 
     for (int b = 0; b < nb; ++b) {
         const int st = b % STAGES;

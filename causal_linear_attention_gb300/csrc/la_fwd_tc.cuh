@@ -1,0 +1,336 @@
+// la_fwd_tc.cuh -- forward of chunked causal linear attention on the 5th-generation
+// tensor cores (tcgen05 + TMEM + TMA), bf16 inputs, fp32 state, head size 64.
+//
+// "Fractus-1B training optimization -- 2026-08-22", section 2, "Opt 2": masked
+// block x block scores inside a block, the running state (S_run, z_run) across
+// blocks, updated AFTER the block has read it.  For row i of a block (state S, z
+// = everything before the block):
+//     o_i = (S^T q_i + sum_{j<=i in block} (q_i . k_j) v_j) / (q_i . z + sum_{j<=i} q_i . k_j + eps)
+// The result is the same for every block size; the tensor core's native tile is 128
+// rows, so this kernel walks the chunk in blocks of 128 tokens whatever block the
+// caller names (other block sizes change only the rounding).
+//
+// One CTA per group, warp-specialised: warps 0-3 (128 threads) own the rows of a
+// block (thread t <-> TMEM lane t), warp 4 is the producer (TMA loads; one lane issues
+// every tcgen05.mma).  Per block:
+//   I1     [A | num] = Q [K ; S^T]       scores and the inter-block term together
+//                                        (M=128, N=192, K=64: 4 instructions)
+//   ST     state^T += V^T K              (M=64, N=64, K=128: 8 instructions)
+//   EPI1   row t: mask j <= t, fp32 row sum, bf16 row -> the A operand of A V
+//   I2     num += A V                    (M=128, N=64, K=128: 8 instructions)
+//   EPI2   o_t = num_t / (row sum + q_t . z + eps) -> global; state^T -> next block
+//          operand (bf16) or S_out
+// q . z and the column sums of K (z update) run on the CUDA cores while the tensor
+// core works.  The state lives transposed in TMEM (lane = value index c), so a state
+// thread writes one contiguous operand row.  Hand-offs are mbarriers.
+//
+// Shared memory (bytes, 1024-aligned, 128-byte swizzle, K-major unless noted):
+//   QT   16384  Q rows 0-127
+//   KS   24576  B operand of I1: rows 0-127 = K (TMA), rows 128-191 = S^T (bf16, epilogue);
+//               rows 0-127 are also the MN-major B operand of the state update
+//   VT   16384  V rows (MN-major B of A V, MN-major A of the state update)
+//   AT   32768  S0 (fp32) on arrival, then the masked scores (atom 0 = cols 0-63, atom 1 = 64-127)
+// TMEM (256 columns): [0,128) scores, [128,192) numerator, [192,256) state^T (M=64 layout).
+#pragma once
+#include <cuda_bf16.h>
+
+#include "la_tc.cuh"
+
+namespace la {
+
+struct FwdTcLayout {
+    static constexpr uint32_t QT = 0;
+    static constexpr uint32_t KS = 16384;
+    static constexpr uint32_t VT = 40960;
+    static constexpr uint32_t AT = 57344;
+    static constexpr uint32_t ZIN = 90112;    // float[64]: z before the block
+    static constexpr uint32_t ZPART = 90368;  // float[4][64]: per-warp column sums of K
+    static constexpr uint32_t BARS = 91392;   // mbarriers + TMEM address slot
+    static constexpr uint32_t END = 91520;
+    static constexpr uint32_t BYTES = END + 1024;  // slack to align the dynamic base
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t T_SCORE = 0, T_NUM = 128, T_STATE = 192;
+    static constexpr int THREADS = 160;
+    static constexpr int BOX_ROWS = 128;                     // token rows per TMA box (Q, K, V)
+    static constexpr uint32_t LOAD_BYTES = 3 * BOX_ROWS * 128;  // Q, K, V boxes of one block
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 8 fp32 values (bit patterns) times `scale` -> one 16-byte chunk of bf16
+__device__ __forceinline__ uint4 pack8(const uint32_t* r, float scale)
+{
+    return make_uint4(pack_bf16(__uint_as_float(r[0]) * scale, __uint_as_float(r[1]) * scale),
+                      pack_bf16(__uint_as_float(r[2]) * scale, __uint_as_float(r[3]) * scale),
+                      pack_bf16(__uint_as_float(r[4]) * scale, __uint_as_float(r[5]) * scale),
+                      pack_bf16(__uint_as_float(r[6]) * scale, __uint_as_float(r[7]) * scale));
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw_chunk(int row, int chunk)
+{
+    return (uint32_t)row * 128u + ((((uint32_t)chunk ^ (uint32_t)row) & 7u) << 4);
+}
+
+// Named barrier over the 128 epilogue threads (warps 0-3); the producer warp is not in it.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(160, 2)
+la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const float* S0, const float* z0,
+                 __nv_bfloat16* o, float* S_out, float* z_out, int C, float eps)
+{
+    using L = FwdTcLayout;
+    using namespace tc;
+    constexpr int D = 64;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_addr(sm);
+    float* zin = reinterpret_cast<float*>(sm + L::ZIN);
+    float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* bar_s0 = bars + 0;    // S0, z0 landed (bulk copies)
+    uint64_t* bar_load = bars + 1;  // Q, K, V of the block landed (TMA)
+    uint64_t* bar_sst = bars + 2;   // S^T operand rows + state^T hold the block's incoming state (epilogue, 128)
+    uint64_t* bar_mma1 = bars + 3;  // I1 done (MMA)
+    uint64_t* bar_abd = bars + 4;   // masked scores published, score TMEM read (epilogue, 128)
+    uint64_t* bar_mma2 = bars + 5;  // I2 and the state update done (MMA)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 64);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.x;
+    const int nsb = (C + 127) / 128;
+
+    if (tid == 0) {
+        mbar_init(bar_s0, 1);
+        mbar_init(bar_load, 1);
+        mbar_init(bar_sst, 128);
+        mbar_init(bar_mma1, 1);
+        mbar_init(bar_abd, 128);
+        mbar_init(bar_mma2, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp < 4) {  // S0 / z0 absent: zero carry
+        if (!S0)
+            for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::AT)[i] = make_uint4(0, 0, 0, 0);
+        if (!z0 && tid < D) zin[tid] = 0.f;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();  // inputs may have been written by the previous kernel in the stream
+
+    if (warp == 4) {
+        // =================================================== producer (one lane)
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            auto issue_qkv = [&](int sb) {
+                const int row0 = sb * 128;
+                mbar_expect_tx(bar_load, L::LOAD_BYTES);
+                tma_load_3d(sm + L::QT, &tq, bar_load, 0, row0, g);
+                tma_load_3d(sm + L::KS, &tk, bar_load, 0, row0, g);
+                tma_load_3d(sm + L::VT, &tv, bar_load, 0, row0, g);
+            };
+            if (nsb > 0) {
+                // (with neither S0 nor z0 this arrival alone completes the phase)
+                mbar_expect_tx(bar_s0, (S0 ? 16384u : 0u) + (z0 ? 256u : 0u));
+                if (S0) bulk_load(sm + L::AT, S0 + (size_t)g * D * D, 16384, bar_s0);
+                if (z0) bulk_load(sm + L::ZIN, z0 + (size_t)g * D, 256, bar_s0);
+                issue_qkv(0);
+            }
+            pdl_launch_dependents();
+
+            // descriptors: the 14-bit start address field advances by (bytes >> 4)
+            const uint64_t dQ = smem_desc(sbase + L::QT, 16, 1024);
+            const uint64_t dKS = smem_desc(sbase + L::KS, 16, 1024);
+            const uint64_t dV = smem_desc(sbase + L::VT, 16, 1024);
+            const uint64_t dA = smem_desc(sbase + L::AT, 16, 1024);
+            const uint32_t id_qks = idesc_bf16(128, 192, false, false);
+            const uint32_t id_state = idesc_bf16(64, 64, true, true);
+            const uint32_t id_av = idesc_bf16(128, 64, false, true);
+            bool ok = true;
+            for (int sb = 0; sb < nsb && ok; ++sb) {
+                const uint32_t par = sb & 1;
+                ok = mbar_wait(bar_load, par, ERR_TIMEOUT_TMA);
+                // incoming state published (first block: carry-in; later: previous block's EPI2)
+                ok = ok && mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // I1: [A | num] = Q [K ; S^T]
+                    umma_bf16(tmem + L::T_SCORE, dQ + kk * 2, dKS + kk * 2, id_qks, kk > 0);
+                umma_commit(bar_mma1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // state^T += V^T K
+                    umma_bf16(tmem + L::T_STATE, dV + kk * 128, dKS + kk * 128, id_state, true);
+                ok = mbar_wait(bar_abd, par, ERR_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // I2: num += A V
+                    umma_bf16(tmem + L::T_NUM, dA + (kk >> 2) * 1024 + (kk & 3) * 2, dV + kk * 128, id_av, true);
+                umma_commit(bar_mma2);
+                if (sb + 1 < nsb) {  // Q, K, V tiles free again once every MMA of the block is done
+                    ok = mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
+                    if (ok) issue_qkv(sb + 1);
+                }
+            }
+        }
+    } else {
+        // =================================================== epilogue (warps 0-3)
+        const int t = tid;                        // block row / TMEM lane
+        const bool sthr = lane < 16;              // M=64 accumulator rows: lanes 0-15 of each warp quarter
+        const int c = 16 * warp + lane;           // value index of a state thread
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const uint32_t par = sb & 1;
+            const int row0 = sb * 128;
+            const bool last = sb + 1 == nsb;
+            if (sb == 0) {  // carry in: state^T <- S0^T (TMEM), operand rows <- bf16(S0)^T
+                mbar_wait(bar_s0, 0, ERR_TIMEOUT_TMA);
+                const float* s0s = reinterpret_cast<const float*>(sm + L::AT);
+                uint32_t r[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = sthr ? __float_as_uint(s0s[(32 * h + j) * D + c]) : 0u;
+                    if (sthr)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + c, 4 * h + q)) = pack8(r + 8 * q, 1.f);
+                    tmem_st32(tmem + lane_base + L::T_STATE + 32 * h, r);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar_sst);
+            }
+            // ---- column sums of K: thread (cc, rg) sums 8 rows x 8 columns, then the warp's 32 rows
+            mbar_wait(bar_load, par, ERR_TIMEOUT_TMA);
+            {
+                const int cc = t & 7, rg = t >> 3;
+                float s[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = 0.f;
+#pragma unroll
+                for (int r8 = 0; r8 < 8; ++r8) {
+                    const int row = rg * 8 + r8;
+                    const uint4 u = *reinterpret_cast<const uint4*>(sm + L::KS + sw_chunk(row, cc));
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h2[e]);
+                        s[2 * e] += f.x;
+                        s[2 * e + 1] += f.y;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
+                    s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
+                }
+                if (lane < 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) zpart[warp * 64 + 8 * cc + e] = s[e];
+            }
+            // ---- q_t . z (z before the block, for every row of it)
+            float qz = 0.f;
+            {
+                const uint32_t qrow = L::QT + t * 128;
+#pragma unroll
+                for (int cq = 0; cq < 8; ++cq) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(sm + qrow + ((((uint32_t)cq ^ (uint32_t)t) & 7u) << 4));
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h2[e]);
+                        qz = fmaf(f.x, zin[8 * cq + 2 * e], qz);
+                        qz = fmaf(f.y, zin[8 * cq + 2 * e + 1], qz);
+                    }
+                }
+            }
+            // ---- masked score row -> bf16 A operand; fp32 row sum
+            mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            float rsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // score columns [64*half, 64*half + 64) -> atom `half`
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_SCORE + 64 * half, r);
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
+                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
+                        rsum += x0 + x1;
+                        w[e] = pack_bf16(x0, x1);
+                    }
+                    *reinterpret_cast<uint4*>(sm + L::AT + half * 16384 + sw_chunk(t, chunk)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_abd);
+            epi_sync();  // every warp's column sums are in zpart; every q . z has read zin
+            if (t < D) zin[t] += zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
+            // ---- output row straight to global; state hand-off
+            mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            {
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_NUM, r);
+                const float inv = 1.f / (rsum + qz + eps);
+                if (row0 + t < C) {
+                    uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)g * C + row0 + t) * D);
+#pragma unroll
+                    for (int chunk = 0; chunk < 8; ++chunk) dst[chunk] = pack8(r + 8 * chunk, inv);
+                }
+            }
+            {
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_STATE, r);
+                if (sthr) {
+                    if (last) {
+                        if (S_out)
+#pragma unroll
+                            for (int p = 0; p < 64; ++p) S_out[(size_t)g * D * D + (size_t)p * D + c] = __uint_as_float(r[p]);
+                    } else {
+#pragma unroll
+                        for (int chunk = 0; chunk < 8; ++chunk)
+                            *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + c, chunk)) = pack8(r + 8 * chunk, 1.f);
+                    }
+                }
+            }
+            if (last && t < D && z_out) z_out[(size_t)g * D + t] = zin[t];
+            epi_sync();  // the new zin is complete before the next block's q . z
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_sst);  // next block: state operand ready, numerator / state TMEM read
+        }
+        if (nsb == 0) {  // empty chunk: the carry passes through
+            for (int i = t; i < D * D; i += 128)
+                if (S_out) S_out[(size_t)g * D * D + i] = S0 ? S0[(size_t)g * D * D + i] : 0.f;
+            if (t < D && z_out) z_out[(size_t)g * D + t] = z0 ? z0[(size_t)g * D + t] : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+}  // namespace la

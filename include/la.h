@@ -104,6 +104,11 @@ la_status la_chunked_bwd(const void* q, const void* k, const void* v,
  * the shape or dtype is unsupported or no device is available. */
 int la_bwd_max_c(int D, int block, la_dtype dtype);
 
+/* Synchronises the current device, then reports whether any kernel of this library
+ * on it gave up a bounded on-device wait (LA_ERR_TIMEOUT) since the last clear;
+ * such a call's outputs are not valid.  clear != 0 resets the flag. */
+la_status la_device_status(int clear);
+
 /* Static, NUL-terminated description of a status code. */
 const char* la_status_string(la_status status);
 

@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c",
-                                           "la_status_string", "la_version"])
+                                           "la_device_status", "la_status_string", "la_version"])
 
 
 def test_every_declared_symbol_is_exported(L):
