@@ -16,6 +16,7 @@
 #include "la_bwd.cuh"
 #include "la_fwd.cuh"
 #include "la_fwd_tc.cuh"
+#include "la_bwd_tc.cuh"
 
 namespace {
 
@@ -163,14 +164,35 @@ la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float
     auto kern = la::la_fwd_tc_kernel;
     const la_status st = prepare(kern, flag, la::FwdTcLayout::BYTES);
     if (st != LA_OK) return st;
-    CUtensorMap tq{}, tk{}, tv{};
+    CUtensorMap tq{}, tk{}, tv{}, to{};
     if (C > 0) {
         constexpr int R = la::FwdTcLayout::BOX_ROWS;
-        if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R))
+        if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R) ||
+            !tmap_bf16(&to, o, G, C, 64, R))
             return LA_ERR_CUDA;
     }
-    return launch_pdl(kern, G, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, S0, z0,
-                      static_cast<__nv_bfloat16*>(o), S_out, z_out, C, eps);
+    return launch_pdl(kern, G, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, to, S0, z0,
+                      S_out, z_out, C, eps);
+}
+
+la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
+                        const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0, float* dz0,
+                        int G, int C, float eps, cudaStream_t stream)
+{
+    static OptIn flag;
+    auto kern = la::la_bwd_tc_kernel;
+    const la_status st = prepare(kern, flag, la::BwdTcLayout::BYTES);
+    if (st != LA_OK) return st;
+    CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{};
+    if (C > 0) {
+        constexpr int R = la::BwdTcLayout::BOX_ROWS;
+        if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R) ||
+            !tmap_bf16(&tg, dO, G, C, 64, R) || !tmap_bf16(&tdq, dq, G, C, 64, R) || !tmap_bf16(&tdk, dk, G, C, 64, R) ||
+            !tmap_bf16(&tdv, dv, G, C, 64, R))
+            return LA_ERR_CUDA;
+    }
+    return launch_pdl(kern, G, la::BwdTcLayout::THREADS, la::BwdTcLayout::BYTES, stream, tq, tk, tv, tg, tdq, tdk, tdv,
+                      S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
 }
 
 // ---------------------------------------------------------------- kernel table
@@ -297,8 +319,11 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
     const int inplace[] = {-1, -1, -1, 6, 7};
     if (!disjoint(outs, 5, ins, 8, inplace)) return LA_ERR_INVALID;
     if (G == 0) return LA_OK;
-    if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // bf16, head size 64, one 128-token tile: the tensor-core (tcgen05 / TMEM / TMA) kernel
+    if (dtype == LA_BF16 && D == 64 && C <= la::BwdTcLayout::MAX_C)
+        return bwd_tc_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
+    if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
 
 #define LA_BWD_CASE(DT, P, DD, BB, NW, ST, AL)                                                               \
     if (dtype == DT && D == DD && block == BB)                                                              \

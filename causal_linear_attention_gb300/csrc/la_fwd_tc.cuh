@@ -18,8 +18,8 @@
 //   ST     state^T += V^T K              (M=64, N=64, K=128: 8 instructions)
 //   EPI1   row t: mask j <= t, fp32 row sum, bf16 row -> the A operand of A V
 //   I2     num += A V                    (M=128, N=64, K=128: 8 instructions)
-//   EPI2   o_t = num_t / (row sum + q_t . z + eps) -> global; state^T -> next block
-//          operand (bf16) or S_out
+//   EPI2   o_t = num_t / (row sum + q_t . z + eps) -> bf16 staging -> TMA store;
+//          state^T -> next block operand (bf16) or S_out (fp32 staging -> bulk store)
 // q . z and the column sums of K (z update) run on the CUDA cores while the tensor
 // core works.  The state lives transposed in TMEM (lane = value index c), so a state
 // thread writes one contiguous operand row.  Hand-offs are mbarriers.
@@ -29,7 +29,9 @@
 //   KS   24576  B operand of I1: rows 0-127 = K (TMA), rows 128-191 = S^T (bf16, epilogue);
 //               rows 0-127 are also the MN-major B operand of the state update
 //   VT   16384  V rows (MN-major B of A V, MN-major A of the state update)
-//   AT   32768  S0 (fp32) on arrival, then the masked scores (atom 0 = cols 0-63, atom 1 = 64-127)
+//   AT   32768  S0 (fp32) on arrival, then the masked scores (atom 0 = cols 0-63, atom 1 = 64-127),
+//               then the output tile staging (first 16 KB)
+// After the last block, QT stages S_out (fp32 [p][c]).
 // TMEM (256 columns): [0,128) scores, [128,192) numerator, [192,256) state^T (M=64 layout).
 #pragma once
 #include <cuda_bf16.h>
@@ -81,8 +83,8 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 __global__ void __launch_bounds__(160, 2)
 la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                 const __grid_constant__ CUtensorMap tv, const float* S0, const float* z0,
-                 __nv_bfloat16* o, float* S_out, float* z_out, int C, float eps)
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                 const float* S0, const float* z0, float* S_out, float* z_out, int C, float eps)
 {
     using L = FwdTcLayout;
     using namespace tc;
@@ -136,6 +138,7 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
+            prefetch_tmap(&to);
             auto issue_qkv = [&](int sb) {
                 const int row0 = sb * 128;
                 mbar_expect_tx(bar_load, L::LOAD_BYTES);
@@ -261,6 +264,8 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             }
             // ---- masked score row -> bf16 A operand; fp32 row sum
+            if (t == 0) tma_store_wait_read();  // the previous block's output tile has left AT
+            epi_sync();
             mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             float rsum = 0.f;
@@ -288,27 +293,25 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_arrive(bar_abd);
             epi_sync();  // every warp's column sums are in zpart; every q . z has read zin
             if (t < D) zin[t] += zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
-            // ---- output row straight to global; state hand-off
+            // ---- output row -> staging (AT is free once I2 is done); state hand-off
             mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             {
                 uint32_t r[64];
                 tmem_ld32x64(tmem + lane_base + L::T_NUM, r);
                 const float inv = 1.f / (rsum + qz + eps);
-                if (row0 + t < C) {
-                    uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)g * C + row0 + t) * D);
 #pragma unroll
-                    for (int chunk = 0; chunk < 8; ++chunk) dst[chunk] = pack8(r + 8 * chunk, inv);
-                }
+                for (int chunk = 0; chunk < 8; ++chunk)
+                    *reinterpret_cast<uint4*>(sm + L::AT + sw_chunk(t, chunk)) = pack8(r + 8 * chunk, inv);
             }
             {
                 uint32_t r[64];
                 tmem_ld32x64(tmem + lane_base + L::T_STATE, r);
                 if (sthr) {
-                    if (last) {
-                        if (S_out)
+                    if (last) {  // S_out staging in QT (free after the last block), fp32 [p][c]
+                        float* st = reinterpret_cast<float*>(sm + L::QT);
 #pragma unroll
-                            for (int p = 0; p < 64; ++p) S_out[(size_t)g * D * D + (size_t)p * D + c] = __uint_as_float(r[p]);
+                        for (int p = 0; p < 64; ++p) st[p * D + c] = __uint_as_float(r[p]);
                     } else {
 #pragma unroll
                         for (int chunk = 0; chunk < 8; ++chunk)
@@ -317,9 +320,14 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             }
             if (last && t < D && z_out) z_out[(size_t)g * D + t] = zin[t];
-            epi_sync();  // the new zin is complete before the next block's q . z
             fence_async_smem();
             tc_fence_before();
+            epi_sync();  // staging complete; the new zin is complete before the next block's q . z
+            if (t == 0) {
+                tma_store_3d(&to, sm + L::AT, 0, row0, g);
+                if (last && S_out) bulk_store(S_out + (size_t)g * D * D, sm + L::QT, 16384);
+                tma_store_commit();
+            }
             mbar_arrive(bar_sst);  // next block: state operand ready, numerator / state TMEM read
         }
         if (nsb == 0) {  // empty chunk: the carry passes through
@@ -328,6 +336,7 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (t < D && z_out) z_out[(size_t)g * D + t] = z0 ? z0[(size_t)g * D + t] : 0.f;
         }
     }
+    if (tid == 0) tma_store_wait_read();  // shared memory stays valid until the stores have read it
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
