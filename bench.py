@@ -35,6 +35,27 @@ METRIC = "linear-attn tokens·groups/s (G·C/s) fwd and fwd+bwd; % of binding ro
 UNIT = "G·C tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of each kernel on this workload, with the hash of the kernel sources they were taken on
+# (profiles/la_*_tc_fractus1b_G160_C128_D64.md).  Reported as null once the sources differ.
+NCU_TRAFFIC = {
+    "la_fwd": {"bytes": 10573056 + 0, "src": "5cd7767ca8813681"},
+    "la_bwd": {"bytes": 15885824 + 0, "src": "5cd7767ca8813681"},
+}
+
+
+def kernel_source_hash():
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "causal_linear_attention_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
+    files.append(os.path.join(ROOT, "include", "la.h"))
+    h = hashlib.sha256()
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 def algorithmic_bytes(G, C, D, esz):
     """Bytes a launch must move at minimum (each input read once, each output written once)."""
@@ -264,9 +285,12 @@ def run_ours(args, rank, world, local):
         "la_bwd": {"avg_us": bwd_secs * 1e6, "alg_bytes": bwd_bytes, "gbs": bwd_bytes / bwd_secs / 1e9},
     }
     dom = max(kernels, key=lambda k: kernels[k]["avg_us"])
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(dom)
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(kernels[dom]["gbs"], 1), "peak": hbm,
             "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / hbm, 4), "peak_source": peak_src,
-            "traffic": None}
+            "traffic": traffic["bytes"] if traffic and traffic["src"] == src_hash else None,
+            "alg_bytes": kernels[dom]["alg_bytes"]}
     for k in kernels:
         kernels[k]["frac"] = round(kernels[k]["gbs"] / hbm, 4)
         kernels[k]["avg_us"] = round(kernels[k]["avg_us"], 3)
