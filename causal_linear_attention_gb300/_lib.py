@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_BUILD, "libla.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 LA_F32, LA_BF16 = 0, 1
-STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA", 4: "LA_ERR_TIMEOUT"}
+STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA", 4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE"}
 
 _lib = None
 _lock = threading.Lock()
@@ -131,7 +131,8 @@ def la_bwd_max_c(D: int, block: int, dtype: int) -> int:
 
 
 def la_device_status(clear: bool = True) -> int:
-    """Synchronise the device; LA_ERR_TIMEOUT (4) if a kernel gave up a bounded wait."""
+    """Synchronise the device; LA_ERR_TIMEOUT (4) if a kernel gave up a bounded wait,
+    LA_ERR_DEVICE (5) if one found its shared memory misaligned and did nothing."""
     return int(lib().la_device_status(1 if clear else 0))
 
 

@@ -360,7 +360,8 @@ extern "C" la_status la_device_status(int clear)
         const uint32_t zero = 0;
         if (cudaMemcpyToSymbol(la::tc::g_status, &zero, sizeof(zero)) != cudaSuccess) return LA_ERR_CUDA;
     }
-    return word ? LA_ERR_TIMEOUT : LA_OK;
+    if (word & la::tc::kTimeoutBits) return LA_ERR_TIMEOUT;
+    return word ? LA_ERR_DEVICE : LA_OK;
 }
 
 extern "C" const char* la_status_string(la_status status)
@@ -371,6 +372,7 @@ extern "C" const char* la_status_string(la_status status)
     case LA_ERR_UNSUPPORTED: return "unsupported D, block, dtype or chunk length";
     case LA_ERR_CUDA: return "CUDA launch failed";
     case LA_ERR_TIMEOUT: return "bounded on-device wait gave up";
+    case LA_ERR_DEVICE: return "a kernel found its launch unusable (shared memory base not 1024-byte aligned)";
     }
     return "unknown status";
 }

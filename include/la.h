@@ -62,7 +62,9 @@ typedef enum {
     LA_ERR_INVALID = 1,      /* a NULL/misaligned/overlapping pointer or a negative size */
     LA_ERR_UNSUPPORTED = 2,  /* a valid but unsupported D, block, dtype or C */
     LA_ERR_CUDA = 3,         /* the CUDA launch failed */
-    LA_ERR_TIMEOUT = 4       /* reserved: a bounded on-device wait gave up */
+    LA_ERR_TIMEOUT = 4,      /* a bounded on-device wait gave up (from la_device_status) */
+    LA_ERR_DEVICE = 5        /* a kernel found its launch unusable and wrote nothing
+                                (from la_device_status) */
 } la_status;
 
 /*
@@ -105,8 +107,10 @@ la_status la_chunked_bwd(const void* q, const void* k, const void* v,
 int la_bwd_max_c(int D, int block, la_dtype dtype);
 
 /* Synchronises the current device, then reports whether any kernel of this library
- * on it gave up a bounded on-device wait (LA_ERR_TIMEOUT) since the last clear;
- * such a call's outputs are not valid.  clear != 0 resets the flag. */
+ * on it gave up a bounded on-device wait (LA_ERR_TIMEOUT) or returned without
+ * working because its dynamic shared memory was not 1024-byte aligned
+ * (LA_ERR_DEVICE) since the last clear; such a call's outputs are not valid.
+ * clear != 0 resets the flag. */
 la_status la_device_status(int clear);
 
 /* Static, NUL-terminated description of a status code. */

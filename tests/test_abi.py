@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings_and_version(L):
     assert la.la_version() == 100
-    for s in range(5):
+    for s in range(6):
         assert len(la.la_status_string(s)) > 0
 
 
