@@ -23,9 +23,12 @@
 //   E2  dd from q . U and dN . AV;  dA columns 0-63 -> AD (A is dead);  dz0 -> global
 //   M3  P_hi = dN V[64:128]^T -> [0,64);  dR = Q^T dN -> [128,192) (M = 64);  dq += dA_lo K_lo
 //   E3  dA columns 64-127 -> AD;  then, while M4 runs: dv -> staging in GN -> TMA store,
-//       dS0 = dS_out + dR -> global
+//       dS0 += dR by fire-and-forget float4 adds (dS0 is dS_out itself, or a copy of it
+//       bulk-stored at the start)
 //   M4  dq += dA_hi K_hi -> [64,128);  dk = dA^T Q + V R^T -> [0,64)
 //   E4  dq + dd z0, dk + dz_out -> staging in AD -> TMA stores
+// M2 and M3 commit in two parts (what the next epilogue needs first, then dv / dR and
+// dA_lo K_lo), so the epilogues start while the rest of the round runs.
 // Every transposed product reads a resident tile through an MN-major descriptor; dN V^T
 // is split in two column halves so that the scores, the state products and dv fit in
 // 256 TMEM columns.
@@ -94,29 +97,35 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* bar_aux = bars + 0;   // S0, dS_out, z0, dz_out landed (bulk)
-    uint64_t* bar_load = bars + 1;  // Q, K, V, dO landed (TMA)
-    uint64_t* bar_prep = bars + 2;  // bf16 S and R published (epilogue, 128)
-    uint64_t* bar_m1 = bars + 3;
-    uint64_t* bar_e1 = bars + 4;    // A, dN published; A read from TMEM (epilogue, 128)
-    uint64_t* bar_m2 = bars + 5;
-    uint64_t* bar_e2 = bars + 6;    // dA columns 0-63 published; P_lo, U, AV read (epilogue, 128)
-    uint64_t* bar_m3 = bars + 7;
-    uint64_t* bar_e3 = bars + 8;    // dA columns 64-127 published; P_hi read (epilogue, 128)
-    uint64_t* bar_m4 = bars + 9;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 80);
+    uint64_t* bar_qk = bars + 1;    // Q, K landed (TMA)
+    uint64_t* bar_vg = bars + 2;    // V, dO landed (TMA)
+    uint64_t* bar_prep = bars + 3;  // bf16 S and R published (epilogue, 128)
+    uint64_t* bar_m1 = bars + 4;    // A
+    uint64_t* bar_e1 = bars + 5;    // A, dN published; A read from TMEM (epilogue, 128)
+    uint64_t* bar_m2 = bars + 6;    // P_lo, U, AV
+    uint64_t* bar_m2b = bars + 7;   // dv (its readers of A and dN are done)
+    uint64_t* bar_e2 = bars + 8;    // dA columns 0-63 published; P_lo, U, AV read (epilogue, 128)
+    uint64_t* bar_m3 = bars + 9;    // P_hi
+    uint64_t* bar_m3b = bars + 10;  // dR, dq += dA_lo K_lo (the last reader of dN is done)
+    uint64_t* bar_e3 = bars + 11;   // dA columns 64-127 published; P_hi read (epilogue, 128)
+    uint64_t* bar_m4 = bars + 12;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 104);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t g = blockIdx.x;
 
     if (tid == 0) {
         mbar_init(bar_aux, 1);
-        mbar_init(bar_load, 1);
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_vg, 1);
         mbar_init(bar_prep, 128);
         mbar_init(bar_m1, 1);
         mbar_init(bar_e1, 128);
         mbar_init(bar_m2, 1);
+        mbar_init(bar_m2b, 1);
         mbar_init(bar_e2, 128);
         mbar_init(bar_m3, 1);
+        mbar_init(bar_m3b, 1);
         mbar_init(bar_e3, 128);
         mbar_init(bar_m4, 1);
         fence_mbar_init();
@@ -162,11 +171,12 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (dS_out) bulk_load(sm + L::AD + 16384, dS_out + g * D * D, 16384, bar_aux);
             if (z0) bulk_load(sm + L::Z0, z0 + g * D, 256, bar_aux);
             if (dz_out) bulk_load(sm + L::DZ, dz_out + g * D, 256, bar_aux);
-            mbar_expect_tx(bar_load, L::LOAD_BYTES);
-            tma_load_3d(sm + L::QT, &tq, bar_load, 0, 0, (int)g);
-            tma_load_3d(sm + L::KT, &tk, bar_load, 0, 0, (int)g);
-            tma_load_3d(sm + L::VT, &tv, bar_load, 0, 0, (int)g);
-            tma_load_3d(sm + L::GN, &tg, bar_load, 0, 0, (int)g);
+            mbar_expect_tx(bar_qk, L::LOAD_BYTES / 2);
+            tma_load_3d(sm + L::QT, &tq, bar_qk, 0, 0, (int)g);
+            tma_load_3d(sm + L::KT, &tk, bar_qk, 0, 0, (int)g);
+            mbar_expect_tx(bar_vg, L::LOAD_BYTES / 2);
+            tma_load_3d(sm + L::VT, &tv, bar_vg, 0, 0, (int)g);
+            tma_load_3d(sm + L::GN, &tg, bar_vg, 0, 0, (int)g);
             pdl_launch_dependents();
 
             // K-major operands advance 32 B (2 descriptor units) per K=16 step inside a
@@ -185,13 +195,14 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t id_mm = idesc_bf16(128, 64, true, true);      // MN-major A and B
             const uint32_t id_dr = idesc_bf16(64, 64, true, true);       // M = 64, MN-major A and B
 
-            bool ok = mbar_wait(bar_load, 0, ERR_TIMEOUT_TMA);
+            bool ok = mbar_wait(bar_qk, 0, ERR_TIMEOUT_TMA);
             if (ok) {  // M1: A = Q K^T
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + L::T_P, dQ + kk * 2, dK + kk * 2, id_128, kk > 0);
                 umma_commit(bar_m1);
-                ok = mbar_wait(bar_e1, 0, ERR_TIMEOUT_MMA) && mbar_wait(bar_prep, 0, ERR_TIMEOUT_MMA);
+                ok = mbar_wait(bar_e1, 0, ERR_TIMEOUT_MMA) && mbar_wait(bar_prep, 0, ERR_TIMEOUT_MMA) &&
+                     mbar_wait(bar_vg, 0, ERR_TIMEOUT_TMA);
             }
             if (ok) {  // M2
                 tc_fence_after();
@@ -204,13 +215,14 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // AV = A V  (V read MN-major: N = c, K = j)
                     umma_bf16(tmem + L::T_AV, dAk + (kk >> 2) * 1024 + (kk & 3) * 2, dV + kk * 128, id_km, kk > 0);
+                umma_commit(bar_m2);  // what E2 needs first; dv follows
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dv = A^T dN  (M = j, K = i)
                     umma_bf16(tmem + L::T_DV, dAm + kk * 128, dG + kk * 128, id_mm, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // dv += K R  (R read MN-major: N = c, K = p)
                     umma_bf16(tmem + L::T_DV, dK + kk * 2, dR + kk * 128, id_km, true);
-                umma_commit(bar_m2);
+                umma_commit(bar_m2b);
                 ok = mbar_wait(bar_e2, 0, ERR_TIMEOUT_MMA);
             }
             if (ok) {  // M3
@@ -218,13 +230,14 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // P_hi = dN V[64:128]^T  (V rows 64+ start 8 KB in)
                     umma_bf16(tmem + L::T_P, dG + kk * 2, dV + 512 + kk * 2, id_kk, kk > 0);
+                umma_commit(bar_m3);  // E3 turns P_hi into dA while the rest of M3 runs
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dR = Q^T dN  (M = p: Q read MN-major; N = c, K = i)
                     umma_bf16(tmem + L::T_DR, dQ + kk * 128, dG + kk * 128, id_dr, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // dq += dA[:, 0:64] K[0:64]  (K read MN-major: N = p, K = j)
                     umma_bf16(tmem + L::T_DQ, dAk + kk * 2, dK + kk * 128, id_km, true);
-                umma_commit(bar_m3);
+                umma_commit(bar_m3b);
                 ok = mbar_wait(bar_e3, 0, ERR_TIMEOUT_MMA);
             }
             if (ok) {  // M4
@@ -249,6 +262,11 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         // ---- E0: bf16 S [p][c] -> ST and R = bf16(dS_out) [p][c] -> RT.  Warp w converts
         //      rows 16w..16w+15, lane l columns 2l and 2l+1: conflict-free on both sides.
         mbar_wait(bar_aux, 0, ERR_TIMEOUT_TMA);
+        const bool copy_dS = dS0 && dS_out && dS0 != dS_out;
+        if (t == 0 && copy_dS) {  // dS0 starts as a copy of dS_out; E3 adds dR to it
+            bulk_store(dS0 + g * D * D, sm + L::AD + 16384, 16384);
+            tma_store_commit();
+        }
         {
             const float* s0s = reinterpret_cast<const float*>(sm + L::AD);
             const float* dss = reinterpret_cast<const float*>(sm + L::AD + 16384);
@@ -265,7 +283,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_arrive(bar_prep);
 
         // ---- q_t . z0 while M1 runs
-        mbar_wait(bar_load, 0, ERR_TIMEOUT_TMA);
+        mbar_wait(bar_qk, 0, ERR_TIMEOUT_TMA);
         float qz = 0.f;
 #pragma unroll
         for (int cq = 0; cq < 8; ++cq) {
@@ -281,7 +299,8 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         // ---- E1: masked scores -> bf16 A (AD), den; dO -> dN in place
         mbar_wait(bar_m1, 0, ERR_TIMEOUT_MMA);
         tc_fence_after();
-        epi_sync();  // every thread is done reading the fp32 carries in AD
+        if (t == 0) tma_store_wait_read();  // the dS_out copy has read AD
+        epi_sync();                          // every thread is done reading the fp32 carries in AD
         float rsum = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -304,6 +323,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         const float den = rsum + qz + eps;
         const float inv = row_ok ? 1.f / den : 0.f;
+        mbar_wait(bar_vg, 0, ERR_TIMEOUT_TMA);
 #pragma unroll
         for (int chunk = 0; chunk < 8; ++chunk) {
             uint4* p4 = reinterpret_cast<uint4*>(sm + L::GN + sw_chunk(t, chunk));
@@ -371,6 +391,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
         };
+        mbar_wait(bar_m2b, 0, ERR_TIMEOUT_MMA);  // dv = A^T dN has finished reading A
         store_dA(0);
         fence_async_smem();
         tc_fence_before();
@@ -417,7 +438,9 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(bar_e3);
-        {  // dv -> staging in GN (dN's last reader was M3) -> TMA store
+        mbar_wait(bar_m3b, 0, ERR_TIMEOUT_MMA);  // dR, the last reader of dN, is done
+        tc_fence_after();
+        {  // dv -> staging in GN -> TMA store
             uint32_t r[64];
             tmem_ld32x64(tmem + lane_base + L::T_DV, r);
 #pragma unroll
@@ -425,25 +448,31 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 *reinterpret_cast<uint4*>(sm + L::GN + sw_chunk(t, chunk)) = pack8(r + 8 * chunk, 1.f);
         }
         fence_async_smem();
+        if (t == 0 && copy_dS) {  // the dS_out -> dS0 copy is complete and visible before the adds
+            tma_store_wait_all();
+            fence_async_global();
+        }
         epi_sync();
         if (t == 0) {
             tma_store_3d(&tdv, sm + L::GN, 0, 0, (int)g);
             tma_store_commit();
         }
-        {  // dS0 = dS_out + dR.  M = 64 layout: thread (w, l < 16) holds row p = 16w + l.
+        {  // dS0 = dS_out + dR.  M = 64 layout: thread (w, l < 16) holds row p = 16w + l.  dS0
+           // already holds dS_out (in place, or copied at the start), so every element gets one
+           // fire-and-forget add; with no dS_out the row is stored.
             uint32_t r[64];
             tmem_ld32x64(tmem + lane_base + L::T_DR, r);
             if (lane < 16 && dS0) {
-                const int p = 16 * warp + lane;
-                float4* dst = reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)p * D);
-                const float4* src = reinterpret_cast<const float4*>(dS_out + g * D * D + (size_t)p * D);
-                float4 a[16];  // every load before any store: dS0 may be the same buffer as dS_out
+                float4* dst = reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)(16 * warp + lane) * D);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = dS_out ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    dst[j] = make_float4(a[j].x + __uint_as_float(r[4 * j]), a[j].y + __uint_as_float(r[4 * j + 1]),
-                                         a[j].z + __uint_as_float(r[4 * j + 2]), a[j].w + __uint_as_float(r[4 * j + 3]));
+                for (int j = 0; j < 16; ++j) {
+                    const float4 x = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    if (dS_out)
+                        atomicAdd(dst + j, x);
+                    else
+                        dst[j] = x;
+                }
             }
         }
 

@@ -84,6 +84,8 @@ __device__ __forceinline__ void fence_async_smem()  // generic-proxy smem writes
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// async-proxy global writes (bulk stores) -> visible to generic-proxy accesses, and back
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

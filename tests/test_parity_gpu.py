@@ -206,3 +206,16 @@ def test_gpu_rejects_bad_arguments_without_launching():
                           torch.empty_like(o), None, None, 2, limit + 1, 64, 64, la.LA_BF16, EPS)
     assert e.value.status in (1, 2)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("C", [128, 300])
+def test_backward_without_carry_gradient_outputs(C):
+    """dS0 = dz0 = NULL skips those outputs; dq, dk, dv are unchanged."""
+    x = make_inputs(5, C, 64, dtype="bf16", seed=15, grads=True)
+    d = x.to(DEV)
+    out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), None, None)
+    got = la.chunked_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS, out=out)
+    torch.cuda.synchronize()
+    assert got[3] is None and got[4] is None
+    ref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
+    check(got[:3], ref[:3], "bf16", BWD_NAMES[:3])
