@@ -157,6 +157,21 @@ bool tmap_bf16(CUtensorMap* map, const void* base, int G, int C, int D, int box_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [G][D][D] fp32 carry seen as a 3-D map (x = value column, y = key row, z = group); boxes
+// of 32 columns (128 bytes) x D rows, 128-byte swizzle.
+bool tmap_state_f32(CUtensorMap* map, const float* base, int G, int D)
+{
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)G};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
+    cuuint32_t box[3] = {32u, (cuuint32_t)D, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
                         float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
 {
@@ -183,16 +198,16 @@ la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float
     auto kern = la::la_bwd_tc_kernel;
     const la_status st = prepare(kern, flag, la::BwdTcLayout::BYTES);
     if (st != LA_OK) return st;
-    CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{};
+    CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{}, tds{};
     if (C > 0) {
         constexpr int R = la::BwdTcLayout::BOX_ROWS;
         if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R) ||
             !tmap_bf16(&tg, dO, G, C, 64, R) || !tmap_bf16(&tdq, dq, G, C, 64, R) || !tmap_bf16(&tdk, dk, G, C, 64, R) ||
-            !tmap_bf16(&tdv, dv, G, C, 64, R))
+            !tmap_bf16(&tdv, dv, G, C, 64, R) || (dS0 && !tmap_state_f32(&tds, dS0, G, 64)))
             return LA_ERR_CUDA;
     }
     return launch_pdl(kern, G, la::BwdTcLayout::THREADS, la::BwdTcLayout::BYTES, stream, tq, tk, tv, tg, tdq, tdk, tdv,
-                      S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
+                      tds, S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
 }
 
 // ---------------------------------------------------------------- kernel table

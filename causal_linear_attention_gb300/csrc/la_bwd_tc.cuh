@@ -15,18 +15,19 @@
 //
 // One CTA per group and two CTAs per SM (112.6 KB of shared memory and 256 TMEM columns
 // each), warp-specialised: warps 0-3 own rows (thread t <-> TMEM lane t); warp 4 is the
-// producer (bulk / TMA loads; one lane issues every tcgen05.mma).  Four UMMA rounds:
+// producer (TMA loads, L2 prefetch of the carries; one lane issues every tcgen05.mma).
+// Q and K are loaded first, so M1 and the score epilogue overlap the rest of the loads.
 //   M1  A = Q K^T -> [0,128)                                        4 x (M128 N128)
-//   E1  mask A, den = row sum + q . z0, bf16 A -> AD; dO -> dN in place
+//   E1  mask A, den = row sum + q . z0, bf16 A -> AD; the fp32 carries are read from
+//       global (L2) straight into bf16 S -> ST and R -> RT; dO -> dN in place
 //   M2  P_lo = dN V[0:64]^T -> [0,64);  U = dN S^T -> [64,128) (the dq accumulator);
 //       AV = A V -> [128,192);  dv = A^T dN + K R -> [192,256)       28 instructions
 //   E2  dd from q . U and dN . AV;  dA columns 0-63 -> AD (A is dead);  dz0 -> global
 //   M3  P_hi = dN V[64:128]^T -> [0,64);  dR = Q^T dN -> [128,192) (M = 64);  dq += dA_lo K_lo
-//   E3  dA columns 64-127 -> AD;  then, while M4 runs: dv -> staging in GN -> TMA store,
-//       dS0 += dR by fire-and-forget float4 adds (dS0 is dS_out itself, or a copy of it
-//       bulk-stored at the start)
+//   E3  dA columns 64-127 -> AD;  then, while M4 runs: dR -> swizzled fp32 staging in GN ->
+//       one TMA reduce-add into dS0 (which holds dS_out: in place, or copied in E1)
 //   M4  dq += dA_hi K_hi -> [64,128);  dk = dA^T Q + V R^T -> [0,64)
-//   E4  dq + dd z0, dk + dz_out -> staging in AD -> TMA stores
+//   E4  dv -> staging in QT, dq + dd z0 and dk + dz_out -> staging in AD -> TMA stores
 // M2 and M3 commit in two parts (what the next epilogue needs first, then dv / dR and
 // dA_lo K_lo), so the epilogues start while the rest of the round runs.
 // Every transposed product reads a resident tile through an MN-major descriptor; dN V^T
@@ -35,12 +36,11 @@
 //
 // Shared memory (bytes, 128-byte swizzle; the dynamic base must be 1024-aligned and the
 // kernel checks it, because there is no room left to round it up):
-//   QT  16384  Q [i][p]           KT  16384  K [j][p]           VT  16384  V [j][c]
-//   GN  16384  dO -> dN (in place) -> dv staging
+//   QT  16384  Q [i][p] -> dv staging          KT  16384  K [j][p]          VT  16384  V [j][c]
+//   GN  16384  dO -> dN (in place) -> dR staging (fp32, two 64 x 32 swizzled boxes)
 //   ST   8192  bf16 S0 [p][c] (B operand of dN S^T); after M2: dd per row, column partials
 //   RT   8192  bf16 dS_out [p][c] (B operand of K R and V R^T)
-//   AD  32768  fp32 S0 | dS_out on arrival -> bf16 masked A -> bf16 dA -> dq | dk staging
-//               (two 64-column atoms of 16 KB each)
+//   AD  32768  bf16 masked A -> bf16 dA -> dq | dk staging (two 64-column atoms of 16 KB)
 //   MISC  640  z0, dz_out, mbarriers, TMEM address
 #pragma once
 #include <cuda_bf16.h>
@@ -60,7 +60,7 @@ struct BwdTcLayout {
     static constexpr uint32_t AD = 81920;
     static constexpr uint32_t Z0 = 114688;   // float[64]
     static constexpr uint32_t DZ = 114944;   // float[64] dz_out
-    static constexpr uint32_t BARS = 115200; // 10 mbarriers, then the TMEM address
+    static constexpr uint32_t BARS = 115200; // 12 mbarriers, then the TMEM address
     static constexpr uint32_t END = 115328;
     static constexpr uint32_t BYTES = END;   // two CTAs per SM: 2 x (BYTES + 1 KB reserved) <= 228 KB
     static constexpr uint32_t DDS = ST;            // float[128] dd per row (ST is dead after M2)
@@ -74,11 +74,12 @@ struct BwdTcLayout {
 };
 static_assert(BwdTcLayout::BYTES <= 115712, "two backward CTAs must fit one SM");
 
+
 __global__ void __launch_bounds__(160, 2)
 la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
-                 const __grid_constant__ CUtensorMap tdv,
+                 const __grid_constant__ CUtensorMap tdv, const __grid_constant__ CUtensorMap tds,
                  const float* S0, const float* z0, const float* dS_out, const float* dz_out,
                  float* dS0, float* dz0, int C, float eps)
 {
@@ -96,20 +97,19 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     float* dds = reinterpret_cast<float*>(sm + L::DDS);
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
-    uint64_t* bar_aux = bars + 0;   // S0, dS_out, z0, dz_out landed (bulk)
+    uint64_t* bar_aux = bars + 0;   // z0, dz_out landed (bulk)
     uint64_t* bar_qk = bars + 1;    // Q, K landed (TMA)
-    uint64_t* bar_vg = bars + 2;    // V, dO landed (TMA)
-    uint64_t* bar_prep = bars + 3;  // bf16 S and R published (epilogue, 128)
-    uint64_t* bar_m1 = bars + 4;    // A
-    uint64_t* bar_e1 = bars + 5;    // A, dN published; A read from TMEM (epilogue, 128)
-    uint64_t* bar_m2 = bars + 6;    // P_lo, U, AV
-    uint64_t* bar_m2b = bars + 7;   // dv (its readers of A and dN are done)
-    uint64_t* bar_e2 = bars + 8;    // dA columns 0-63 published; P_lo, U, AV read (epilogue, 128)
-    uint64_t* bar_m3 = bars + 9;    // P_hi
-    uint64_t* bar_m3b = bars + 10;  // dR, dq += dA_lo K_lo (the last reader of dN is done)
-    uint64_t* bar_e3 = bars + 11;   // dA columns 64-127 published; P_hi read (epilogue, 128)
-    uint64_t* bar_m4 = bars + 12;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 104);
+    uint64_t* bar_vg = bars + 2;    // dO, V landed (TMA)
+    uint64_t* bar_m1 = bars + 3;    // A
+    uint64_t* bar_e1 = bars + 4;    // A, S, R, dN published; A read from TMEM (epilogue, 128)
+    uint64_t* bar_m2 = bars + 5;    // P_lo, U, AV
+    uint64_t* bar_m2b = bars + 6;   // dv (its readers of A and dN are done)
+    uint64_t* bar_e2 = bars + 7;    // dA columns 0-63 published; P_lo, U, AV read (epilogue, 128)
+    uint64_t* bar_m3 = bars + 8;    // P_hi
+    uint64_t* bar_m3b = bars + 9;   // dR, dq += dA_lo K_lo (the last reader of dN is done)
+    uint64_t* bar_e3 = bars + 10;   // dA columns 64-127 published; P_hi read (epilogue, 128)
+    uint64_t* bar_m4 = bars + 11;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 96);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t g = blockIdx.x;
@@ -118,7 +118,6 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(bar_aux, 1);
         mbar_init(bar_qk, 1);
         mbar_init(bar_vg, 1);
-        mbar_init(bar_prep, 128);
         mbar_init(bar_m1, 1);
         mbar_init(bar_e1, 128);
         mbar_init(bar_m2, 1);
@@ -134,16 +133,9 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         tmem_alloc(tslot, L::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp < 4) {  // absent carries / upstream carry gradients are zeros
-        if (!S0)
-            for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::AD)[i] = make_uint4(0, 0, 0, 0);
-        if (!dS_out)
-            for (int i = tid; i < 16384 / 16; i += 128)
-                reinterpret_cast<uint4*>(sm + L::AD + 16384)[i] = make_uint4(0, 0, 0, 0);
-        if (tid < D) {
-            if (!z0) z0s[tid] = 0.f;
-            if (!dz_out) dzs[tid] = 0.f;
-        }
+    if (tid < D) {  // an absent carry / upstream carry gradient is zero
+        if (!z0) z0s[tid] = 0.f;
+        if (!dz_out) dzs[tid] = 0.f;
     }
     fence_async_smem();
     tc_fence_before();
@@ -165,18 +157,19 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             prefetch_tmap(&tg);
-            // (with no S0, dS_out, z0, dz_out this arrival alone completes the phase)
-            mbar_expect_tx(bar_aux, (S0 ? 16384u : 0u) + (dS_out ? 16384u : 0u) + (z0 ? 256u : 0u) + (dz_out ? 256u : 0u));
-            if (S0) bulk_load(sm + L::AD, S0 + g * D * D, 16384, bar_aux);
-            if (dS_out) bulk_load(sm + L::AD + 16384, dS_out + g * D * D, 16384, bar_aux);
-            if (z0) bulk_load(sm + L::Z0, z0 + g * D, 256, bar_aux);
-            if (dz_out) bulk_load(sm + L::DZ, dz_out + g * D, 256, bar_aux);
+            // in the order the work needs them: Q, K (M1), the carries (E1), dO (E1), V (M2)
             mbar_expect_tx(bar_qk, L::LOAD_BYTES / 2);
             tma_load_3d(sm + L::QT, &tq, bar_qk, 0, 0, (int)g);
             tma_load_3d(sm + L::KT, &tk, bar_qk, 0, 0, (int)g);
+            if (S0) prefetch_l2(S0 + g * D * D, 16384);
+            if (dS_out) prefetch_l2(dS_out + g * D * D, 16384);
+            // (with neither z0 nor dz_out this arrival alone completes the phase)
+            mbar_expect_tx(bar_aux, (z0 ? 256u : 0u) + (dz_out ? 256u : 0u));
+            if (z0) bulk_load(sm + L::Z0, z0 + g * D, 256, bar_aux);
+            if (dz_out) bulk_load(sm + L::DZ, dz_out + g * D, 256, bar_aux);
             mbar_expect_tx(bar_vg, L::LOAD_BYTES / 2);
-            tma_load_3d(sm + L::VT, &tv, bar_vg, 0, 0, (int)g);
             tma_load_3d(sm + L::GN, &tg, bar_vg, 0, 0, (int)g);
+            tma_load_3d(sm + L::VT, &tv, bar_vg, 0, 0, (int)g);
             pdl_launch_dependents();
 
             // K-major operands advance 32 B (2 descriptor units) per K=16 step inside a
@@ -201,8 +194,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + L::T_P, dQ + kk * 2, dK + kk * 2, id_128, kk > 0);
                 umma_commit(bar_m1);
-                ok = mbar_wait(bar_e1, 0, ERR_TIMEOUT_MMA) && mbar_wait(bar_prep, 0, ERR_TIMEOUT_MMA) &&
-                     mbar_wait(bar_vg, 0, ERR_TIMEOUT_TMA);
+                ok = mbar_wait(bar_e1, 0, ERR_TIMEOUT_MMA) && mbar_wait(bar_vg, 0, ERR_TIMEOUT_TMA);
             }
             if (ok) {  // M2
                 tc_fence_after();
@@ -259,30 +251,9 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const int t = tid;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const bool row_ok = t < C;
-        // ---- E0: bf16 S [p][c] -> ST and R = bf16(dS_out) [p][c] -> RT.  Warp w converts
-        //      rows 16w..16w+15, lane l columns 2l and 2l+1: conflict-free on both sides.
-        mbar_wait(bar_aux, 0, ERR_TIMEOUT_TMA);
         const bool copy_dS = dS0 && dS_out && dS0 != dS_out;
-        if (t == 0 && copy_dS) {  // dS0 starts as a copy of dS_out; E3 adds dR to it
-            bulk_store(dS0 + g * D * D, sm + L::AD + 16384, 16384);
-            tma_store_commit();
-        }
-        {
-            const float* s0s = reinterpret_cast<const float*>(sm + L::AD);
-            const float* dss = reinterpret_cast<const float*>(sm + L::AD + 16384);
-#pragma unroll 4
-            for (int pp = 0; pp < 16; ++pp) {
-                const int p = 16 * warp + pp;
-                const float2 s = *reinterpret_cast<const float2*>(s0s + p * D + 2 * lane);
-                const float2 r = *reinterpret_cast<const float2*>(dss + p * D + 2 * lane);
-                *reinterpret_cast<uint32_t*>(sm + L::ST + sw128_offset(p, 2 * lane)) = pack_bf16(s.x, s.y);
-                *reinterpret_cast<uint32_t*>(sm + L::RT + sw128_offset(p, 2 * lane)) = pack_bf16(r.x, r.y);
-            }
-        }
-        fence_async_smem();
-        mbar_arrive(bar_prep);
-
         // ---- q_t . z0 while M1 runs
+        mbar_wait(bar_aux, 0, ERR_TIMEOUT_TMA);
         mbar_wait(bar_qk, 0, ERR_TIMEOUT_TMA);
         float qz = 0.f;
 #pragma unroll
@@ -296,11 +267,9 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 qz = fmaf(f.y, z0s[8 * cq + 2 * e + 1], qz);
             }
         }
-        // ---- E1: masked scores -> bf16 A (AD), den; dO -> dN in place
+        // ---- E1: masked scores -> bf16 A (AD), den
         mbar_wait(bar_m1, 0, ERR_TIMEOUT_MMA);
         tc_fence_after();
-        if (t == 0) tma_store_wait_read();  // the dS_out copy has read AD
-        epi_sync();                          // every thread is done reading the fp32 carries in AD
         float rsum = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -323,6 +292,30 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         const float den = rsum + qz + eps;
         const float inv = row_ok ? 1.f / den : 0.f;
+        // ---- the carries, read from global (L2) into bf16 S -> ST and R -> RT.  Warp w takes
+        //      rows 16w..16w+15, lane l columns 2l, 2l+1: 256-byte coalesced row reads and
+        //      conflict-free swizzled writes.  Every load is issued before the first use.
+        {
+            const float2* s0g = S0 ? reinterpret_cast<const float2*>(S0 + g * D * D) : nullptr;
+            const float2* dsg = dS_out ? reinterpret_cast<const float2*>(dS_out + g * D * D) : nullptr;
+            float2 s[16], r[16];
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) {
+                const int p = 16 * warp + pp;
+                s[pp] = s0g ? s0g[p * 32 + lane] : make_float2(0.f, 0.f);
+                r[pp] = dsg ? dsg[p * 32 + lane] : make_float2(0.f, 0.f);
+            }
+            float2* cpy = copy_dS ? reinterpret_cast<float2*>(dS0 + g * D * D) : nullptr;
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) {
+                const int p = 16 * warp + pp;
+                *reinterpret_cast<uint32_t*>(sm + L::ST + sw128_offset(p, 2 * lane)) = pack_bf16(s[pp].x, s[pp].y);
+                *reinterpret_cast<uint32_t*>(sm + L::RT + sw128_offset(p, 2 * lane)) = pack_bf16(r[pp].x, r[pp].y);
+                if (cpy) cpy[p * 32 + lane] = r[pp];  // dS0 starts as dS_out; E3 adds dR to it
+            }
+            if (cpy) fence_async_global();  // the copy is ordered before E3's TMA reduce-add
+        }
+        // ---- dO -> dN = dO / den in place
         mbar_wait(bar_vg, 0, ERR_TIMEOUT_TMA);
 #pragma unroll
         for (int chunk = 0; chunk < 8; ++chunk) {
@@ -431,7 +424,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         epi_sync();
         if (t < D && dz0) dz0[g * D + t] = dzs[t] + zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
 
-        // ---- E3: dA columns 64-127, then dv and dS0 while M4 runs
+        // ---- E3: dA columns 64-127, then dS0 and dv while M4 runs
         mbar_wait(bar_m3, 0, ERR_TIMEOUT_MMA);
         tc_fence_after();
         store_dA(1);
@@ -440,45 +433,46 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_arrive(bar_e3);
         mbar_wait(bar_m3b, 0, ERR_TIMEOUT_MMA);  // dR, the last reader of dN, is done
         tc_fence_after();
-        {  // dv -> staging in GN -> TMA store
+        {  // dR -> fp32 staging in GN: box b (columns 32b..32b+31) is 64 rows x 128 B with the
+           // 16-byte chunks of row p XOR-swizzled by p & 7, the layout of the dS0 tensor map.
+           // M = 64 accumulator layout: thread (w, l < 16) holds row p = 16w + l.
+            uint32_t r[64];
+            tmem_ld32x64(tmem + lane_base + L::T_DR, r);
+            if (lane < 16) {
+                const uint32_t p = 16 * warp + lane;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<uint4*>(sm + L::GN + (j >> 3) * 8192 + p * 128 + ((((uint32_t)j & 7u) ^ (p & 7u)) << 4)) =
+                        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
+        }
+        fence_async_smem();
+        epi_sync();
+        if (t == 0 && dS0) {  // dS0 += dR (dS0 holds dS_out), or dS0 = dR when there is no dS_out
+            if (dS_out) {
+                tma_reduce_add_3d(&tds, sm + L::GN, 0, 0, (int)g);
+                tma_reduce_add_3d(&tds, sm + L::GN + 8192, 32, 0, (int)g);
+            } else {
+                tma_store_3d(&tds, sm + L::GN, 0, 0, (int)g);
+                tma_store_3d(&tds, sm + L::GN + 8192, 32, 0, (int)g);
+            }
+            tma_store_commit();
+        }
+        uint32_t pv[32];  // dv as bf16 pairs, staged once Q is dead
+        {
             uint32_t r[64];
             tmem_ld32x64(tmem + lane_base + L::T_DV, r);
 #pragma unroll
-            for (int chunk = 0; chunk < 8; ++chunk)
-                *reinterpret_cast<uint4*>(sm + L::GN + sw_chunk(t, chunk)) = pack8(r + 8 * chunk, 1.f);
-        }
-        fence_async_smem();
-        if (t == 0 && copy_dS) {  // the dS_out -> dS0 copy is complete and visible before the adds
-            tma_store_wait_all();
-            fence_async_global();
-        }
-        epi_sync();
-        if (t == 0) {
-            tma_store_3d(&tdv, sm + L::GN, 0, 0, (int)g);
-            tma_store_commit();
-        }
-        {  // dS0 = dS_out + dR.  M = 64 layout: thread (w, l < 16) holds row p = 16w + l.  dS0
-           // already holds dS_out (in place, or copied at the start), so every element gets one
-           // fire-and-forget add; with no dS_out the row is stored.
-            uint32_t r[64];
-            tmem_ld32x64(tmem + lane_base + L::T_DR, r);
-            if (lane < 16 && dS0) {
-                float4* dst = reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)(16 * warp + lane) * D);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 x = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    if (dS_out)
-                        atomicAdd(dst + j, x);
-                    else
-                        dst[j] = x;
-                }
-            }
+            for (int j = 0; j < 32; ++j) pv[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
         }
 
-        // ---- E4: dq + dd z0, dk + dz_out -> staging in AD (dA's last reader was M4) -> TMA stores
-        mbar_wait(bar_m4, 0, ERR_TIMEOUT_MMA);
+        // ---- E4: dv -> staging in QT, dq + dd z0, dk + dz_out -> staging in AD -> TMA stores
+        mbar_wait(bar_m4, 0, ERR_TIMEOUT_MMA);  // M4 was the last reader of Q and dA
         tc_fence_after();
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk)
+            *reinterpret_cast<uint4*>(sm + L::QT + sw_chunk(t, chunk)) =
+                make_uint4(pv[4 * chunk], pv[4 * chunk + 1], pv[4 * chunk + 2], pv[4 * chunk + 3]);
         {
             uint32_t r[64];
             tmem_ld32x64(tmem + lane_base + L::T_DQ, r);
@@ -500,6 +494,7 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         fence_async_smem();
         epi_sync();
         if (t == 0) {
+            tma_store_3d(&tdv, sm + L::QT, 0, 0, (int)g);
             tma_store_3d(&tdq, sm + L::AD, 0, 0, (int)g);
             tma_store_3d(&tdk, sm + L::AD + 16384, 0, 0, (int)g);
             tma_store_commit();

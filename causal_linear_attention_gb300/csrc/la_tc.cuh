@@ -101,6 +101,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
                  :: "l"(map), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z) : "memory");
 }
+// Element-wise add of a shared-memory box into global memory (the element type and the
+// swizzle come from the tensor map; fp32 adds are performed at L2).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y, int z)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 :: "l"(map), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z) : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the smem sources of all committed stores have been read.
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -117,6 +124,11 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                  :: "l"(dst), "r"(smem_addr(src)), "r"(bytes) : "memory");
 }
 
+// Start pulling `bytes` (multiple of 16, 16-byte aligned) into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
