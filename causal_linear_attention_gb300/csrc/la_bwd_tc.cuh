@@ -252,19 +252,18 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const bool row_ok = t < C;
         const bool copy_dS = dS0 && dS_out && dS0 != dS_out;
-        // ---- q_t . z0 while M1 runs
-        mbar_wait(bar_aux, 0, ERR_TIMEOUT_TMA);
-        mbar_wait(bar_qk, 0, ERR_TIMEOUT_TMA);
-        float qz = 0.f;
+        // ---- the fp32 carries, read from global (the producer prefetched them into L2) while
+        //      M1 runs: warp w takes rows 16w..16w+15, lane l columns 2l, 2l+1 (256-byte
+        //      coalesced row reads)
+        float2 cs[16], cr[16];
+        {
+            const float2* s0g = S0 ? reinterpret_cast<const float2*>(S0 + g * D * D) : nullptr;
+            const float2* dsg = dS_out ? reinterpret_cast<const float2*>(dS_out + g * D * D) : nullptr;
 #pragma unroll
-        for (int cq = 0; cq < 8; ++cq) {
-            const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + sw_chunk(t, cq));
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(h2[e]);
-                qz = fmaf(f.x, z0s[8 * cq + 2 * e], qz);
-                qz = fmaf(f.y, z0s[8 * cq + 2 * e + 1], qz);
+            for (int pp = 0; pp < 16; ++pp) {
+                const int p = 16 * warp + pp;
+                cs[pp] = s0g ? s0g[p * 32 + lane] : make_float2(0.f, 0.f);
+                cr[pp] = dsg ? dsg[p * 32 + lane] : make_float2(0.f, 0.f);
             }
         }
         // ---- E1: masked scores -> bf16 A (AD), den
@@ -290,28 +289,32 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
+        // ---- q_t . z0 (M2 needs den only through dN)
+        mbar_wait(bar_aux, 0, ERR_TIMEOUT_TMA);
+        mbar_wait(bar_qk, 0, ERR_TIMEOUT_TMA);
+        float qz = 0.f;
+#pragma unroll
+        for (int cq = 0; cq < 8; ++cq) {
+            const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + sw_chunk(t, cq));
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                qz = fmaf(f.x, z0s[8 * cq + 2 * e], qz);
+                qz = fmaf(f.y, z0s[8 * cq + 2 * e + 1], qz);
+            }
+        }
         const float den = rsum + qz + eps;
         const float inv = row_ok ? 1.f / den : 0.f;
-        // ---- the carries, read from global (L2) into bf16 S -> ST and R -> RT.  Warp w takes
-        //      rows 16w..16w+15, lane l columns 2l, 2l+1: 256-byte coalesced row reads and
-        //      conflict-free swizzled writes.  Every load is issued before the first use.
+        // ---- the carries -> bf16 S -> ST and R -> RT (conflict-free swizzled writes)
         {
-            const float2* s0g = S0 ? reinterpret_cast<const float2*>(S0 + g * D * D) : nullptr;
-            const float2* dsg = dS_out ? reinterpret_cast<const float2*>(dS_out + g * D * D) : nullptr;
-            float2 s[16], r[16];
-#pragma unroll
-            for (int pp = 0; pp < 16; ++pp) {
-                const int p = 16 * warp + pp;
-                s[pp] = s0g ? s0g[p * 32 + lane] : make_float2(0.f, 0.f);
-                r[pp] = dsg ? dsg[p * 32 + lane] : make_float2(0.f, 0.f);
-            }
             float2* cpy = copy_dS ? reinterpret_cast<float2*>(dS0 + g * D * D) : nullptr;
 #pragma unroll
             for (int pp = 0; pp < 16; ++pp) {
                 const int p = 16 * warp + pp;
-                *reinterpret_cast<uint32_t*>(sm + L::ST + sw128_offset(p, 2 * lane)) = pack_bf16(s[pp].x, s[pp].y);
-                *reinterpret_cast<uint32_t*>(sm + L::RT + sw128_offset(p, 2 * lane)) = pack_bf16(r[pp].x, r[pp].y);
-                if (cpy) cpy[p * 32 + lane] = r[pp];  // dS0 starts as dS_out; E3 adds dR to it
+                *reinterpret_cast<uint32_t*>(sm + L::ST + sw128_offset(p, 2 * lane)) = pack_bf16(cs[pp].x, cs[pp].y);
+                *reinterpret_cast<uint32_t*>(sm + L::RT + sw128_offset(p, 2 * lane)) = pack_bf16(cr[pp].x, cr[pp].y);
+                if (cpy) cpy[p * 32 + lane] = cr[pp];  // dS0 starts as dS_out; E3 adds dR to it
             }
             if (cpy) fence_async_global();  // the copy is ordered before E3's TMA reduce-add
         }

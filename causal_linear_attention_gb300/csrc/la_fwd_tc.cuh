@@ -10,29 +10,35 @@
 // rows, so this kernel walks the chunk in blocks of 128 tokens whatever block the
 // caller names (other block sizes change only the rounding).
 //
-// One CTA per group, warp-specialised: warps 0-3 (128 threads) own the rows of a
-// block (thread t <-> TMEM lane t), warp 4 is the producer (TMA loads; one lane issues
-// every tcgen05.mma).  Per block:
-//   I1     [A | num] = Q [K ; S^T]       scores and the inter-block term together
-//                                        (M=128, N=192, K=64: 4 instructions)
-//   ST     state^T += V^T K              (M=64, N=64, K=128: 8 instructions)
+// One CTA per group (two CTAs per SM), warp-specialised: warps 0-3 (128 threads) own the
+// rows of a block (thread t <-> TMEM lane t), warp 4 is the producer (TMA loads; one lane
+// issues every tcgen05.mma).  Per block:
+//   I1a    A = Q K^T                     (M=128, N=128, K=64: 4 instructions)
 //   EPI1   row t: mask j <= t, fp32 row sum, bf16 row -> the A operand of A V
+//   I1b    num = Q S                     (S^T rows as the B operand; M=128, N=64: 4)
 //   I2     num += A V                    (M=128, N=64, K=128: 8 instructions)
+//   ST     (S - S0)^T += V^T K           (M=64, N=64, K=128: 8 instructions; committed
+//                                        separately, the output does not wait for it)
 //   EPI2   o_t = num_t / (row sum + q_t . z + eps) -> bf16 staging -> TMA store;
-//          state^T -> next block operand (bf16) or S_out (fp32 staging -> bulk store)
-// q . z and the column sums of K (z update) run on the CUDA cores while the tensor
-// core works.  The state lives transposed in TMEM (lane = value index c), so a state
-// thread writes one contiguous operand row.  Hand-offs are mbarriers.
+//          S0 + (S - S0) -> next block operand (bf16 S^T rows) or S_out (fp32 staging ->
+//          bulk store)
+// Q and K are loaded first, then the carry, then V, so I1a and EPI1 run while the rest
+// lands; the carry-in (first block) follows EPI1.  q . z and the column sums of K (z
+// update) run on the CUDA cores after EPI1, while I2 runs.  TMEM holds S - S0 transposed
+// (lane = value index c); EPI2 adds S0 from shared memory, so a state thread writes one
+// contiguous operand row, and S_out leaves from the S0 region updated in place.
+// Hand-offs are mbarriers.
 //
-// Shared memory (bytes, 1024-aligned, 128-byte swizzle, K-major unless noted):
+// Shared memory (bytes, 128-byte swizzle, K-major unless noted; the dynamic base must be
+// 1024-aligned and the kernel checks it):
 //   QT   16384  Q rows 0-127
-//   KS   24576  B operand of I1: rows 0-127 = K (TMA), rows 128-191 = S^T (bf16, epilogue);
-//               rows 0-127 are also the MN-major B operand of the state update
+//   KS   24576  rows 0-127 = K (TMA; B operand of I1a, MN-major B of the state update),
+//               rows 128-191 = S^T (bf16, epilogue; B operand of I1b)
 //   VT   16384  V rows (MN-major B of A V, MN-major A of the state update)
-//   AT   32768  S0 (fp32) on arrival, then the masked scores (atom 0 = cols 0-63, atom 1 = 64-127),
-//               then the output tile staging (first 16 KB)
-// After the last block, QT stages S_out (fp32 [p][c]).
-// TMEM (256 columns): [0,128) scores, [128,192) numerator, [192,256) state^T (M=64 layout).
+//   AT   32768  the masked scores (atom 0 = cols 0-63, atom 1 = 64-127), then the output
+//               tile staging (first 16 KB)
+//   S0F  16384  S0 (fp32 [p][c]) as it arrives; after the last block, S_out (staging)
+// TMEM (256 columns): [0,128) scores, [128,192) numerator, [192,256) (S - S0)^T (M=64 layout).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -45,17 +51,19 @@ struct FwdTcLayout {
     static constexpr uint32_t KS = 16384;
     static constexpr uint32_t VT = 40960;
     static constexpr uint32_t AT = 57344;
-    static constexpr uint32_t ZIN = 90112;    // float[64]: z before the block
-    static constexpr uint32_t ZPART = 90368;  // float[4][64]: per-warp column sums of K
-    static constexpr uint32_t BARS = 91392;   // mbarriers + TMEM address slot
-    static constexpr uint32_t END = 91520;
-    static constexpr uint32_t BYTES = END + 1024;  // slack to align the dynamic base
+    static constexpr uint32_t S0F = 90112;    // S0 (fp32 [p][c]) as it arrives
+    static constexpr uint32_t ZIN = 106496;   // float[64]: z before the block
+    static constexpr uint32_t ZPART = 106752; // float[4][64]: per-warp column sums of K
+    static constexpr uint32_t BARS = 107776;  // mbarriers + TMEM address slot
+    static constexpr uint32_t END = 107904;
+    static constexpr uint32_t BYTES = END;    // two CTAs per SM; the base alignment is checked instead
     static constexpr uint32_t TMEM_COLS = 256;
     static constexpr uint32_t T_SCORE = 0, T_NUM = 128, T_STATE = 192;
     static constexpr int THREADS = 160;
     static constexpr int BOX_ROWS = 128;                     // token rows per TMA box (Q, K, V)
     static constexpr uint32_t LOAD_BYTES = 3 * BOX_ROWS * 128;  // Q, K, V boxes of one block
 };
+static_assert(FwdTcLayout::BYTES <= 115712, "two forward CTAs must fit one SM");
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 {
@@ -89,19 +97,25 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     using L = FwdTcLayout;
     using namespace tc;
     constexpr int D = 64;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {  // swizzled operand tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
     const uint32_t sbase = smem_addr(sm);
     float* zin = reinterpret_cast<float*>(sm + L::ZIN);
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* bar_s0 = bars + 0;    // S0, z0 landed (bulk copies)
-    uint64_t* bar_load = bars + 1;  // Q, K, V of the block landed (TMA)
-    uint64_t* bar_sst = bars + 2;   // S^T operand rows + state^T hold the block's incoming state (epilogue, 128)
-    uint64_t* bar_mma1 = bars + 3;  // I1 done (MMA)
+    uint64_t* bar_qk = bars + 1;    // Q, K of the block landed (TMA)
+    uint64_t* bar_v = bars + 6;     // V of the block landed (TMA)
+    uint64_t* bar_sst = bars + 2;   // S^T operand rows hold the block's incoming state (epilogue, 128)
+    uint64_t* bar_mma1 = bars + 3;  // I1a done (MMA)
     uint64_t* bar_abd = bars + 4;   // masked scores published, score TMEM read (epilogue, 128)
-    uint64_t* bar_mma2 = bars + 5;  // I2 and the state update done (MMA)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 64);
+    uint64_t* bar_mma2 = bars + 5;  // I1b and I2 done (MMA)
+    uint64_t* bar_mma2s = bars + 8; // the state update done (MMA)
+    uint64_t* bar_qkr = bars + 7;   // the epilogue is done reading the block's Q and K (epilogue, 128)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 96);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x;
@@ -109,11 +123,14 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     if (tid == 0) {
         mbar_init(bar_s0, 1);
-        mbar_init(bar_load, 1);
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_qkr, 128);
         mbar_init(bar_sst, 128);
         mbar_init(bar_mma1, 1);
         mbar_init(bar_abd, 128);
         mbar_init(bar_mma2, 1);
+        mbar_init(bar_mma2s, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -122,7 +139,7 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     }
     if (warp < 4) {  // S0 / z0 absent: zero carry
         if (!S0)
-            for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::AT)[i] = make_uint4(0, 0, 0, 0);
+            for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::S0F)[i] = make_uint4(0, 0, 0, 0);
         if (!z0 && tid < D) zin[tid] = 0.f;
     }
     fence_async_smem();
@@ -139,19 +156,22 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             prefetch_tmap(&to);
-            auto issue_qkv = [&](int sb) {
-                const int row0 = sb * 128;
-                mbar_expect_tx(bar_load, L::LOAD_BYTES);
-                tma_load_3d(sm + L::QT, &tq, bar_load, 0, row0, g);
-                tma_load_3d(sm + L::KS, &tk, bar_load, 0, row0, g);
-                tma_load_3d(sm + L::VT, &tv, bar_load, 0, row0, g);
+            auto issue_qk = [&](int sb) {
+                mbar_expect_tx(bar_qk, L::LOAD_BYTES / 3 * 2);
+                tma_load_3d(sm + L::QT, &tq, bar_qk, 0, sb * 128, g);
+                tma_load_3d(sm + L::KS, &tk, bar_qk, 0, sb * 128, g);
             };
-            if (nsb > 0) {
+            auto issue_v = [&](int sb) {
+                mbar_expect_tx(bar_v, L::LOAD_BYTES / 3);
+                tma_load_3d(sm + L::VT, &tv, bar_v, 0, sb * 128, g);
+            };
+            if (nsb > 0) {  // in the order the work needs them: Q, K (I1), the carry (I1), V
+                issue_qk(0);
                 // (with neither S0 nor z0 this arrival alone completes the phase)
                 mbar_expect_tx(bar_s0, (S0 ? 16384u : 0u) + (z0 ? 256u : 0u));
-                if (S0) bulk_load(sm + L::AT, S0 + (size_t)g * D * D, 16384, bar_s0);
+                if (S0) bulk_load(sm + L::S0F, S0 + (size_t)g * D * D, 16384, bar_s0);
                 if (z0) bulk_load(sm + L::ZIN, z0 + (size_t)g * D, 256, bar_s0);
-                issue_qkv(0);
+                issue_v(0);
             }
             pdl_launch_dependents();
 
@@ -160,34 +180,44 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint64_t dKS = smem_desc(sbase + L::KS, 16, 1024);
             const uint64_t dV = smem_desc(sbase + L::VT, 16, 1024);
             const uint64_t dA = smem_desc(sbase + L::AT, 16, 1024);
-            const uint32_t id_qks = idesc_bf16(128, 192, false, false);
+            const uint64_t dST = smem_desc(sbase + L::KS + 16384, 16, 1024);
+            const uint32_t id_qk = idesc_bf16(128, 128, false, false);
+            const uint32_t id_qs = idesc_bf16(128, 64, false, false);
             const uint32_t id_state = idesc_bf16(64, 64, true, true);
             const uint32_t id_av = idesc_bf16(128, 64, false, true);
             bool ok = true;
             for (int sb = 0; sb < nsb && ok; ++sb) {
                 const uint32_t par = sb & 1;
-                ok = mbar_wait(bar_load, par, ERR_TIMEOUT_TMA);
-                // incoming state published (first block: carry-in; later: previous block's EPI2)
-                ok = ok && mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
+                ok = mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // I1: [A | num] = Q [K ; S^T]
-                    umma_bf16(tmem + L::T_SCORE, dQ + kk * 2, dKS + kk * 2, id_qks, kk > 0);
+                for (int kk = 0; kk < 4; ++kk)  // I1a: A = Q K^T
+                    umma_bf16(tmem + L::T_SCORE, dQ + kk * 2, dKS + kk * 2, id_qk, kk > 0);
                 umma_commit(bar_mma1);
+                // incoming state published (first block: carry-in; later: previous block's EPI2)
+                ok = mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // state^T += V^T K
-                    umma_bf16(tmem + L::T_STATE, dV + kk * 128, dKS + kk * 128, id_state, true);
-                ok = mbar_wait(bar_abd, par, ERR_TIMEOUT_MMA);
+                for (int kk = 0; kk < 4; ++kk)  // I1b: num = Q S  (S^T rows as K-major B: N = c, K = p)
+                    umma_bf16(tmem + L::T_NUM, dQ + kk * 2, dST + kk * 2, id_qs, kk > 0);
+                ok = mbar_wait(bar_v, par, ERR_TIMEOUT_TMA) && mbar_wait(bar_abd, par, ERR_TIMEOUT_MMA);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // I2: num += A V
                     umma_bf16(tmem + L::T_NUM, dA + (kk >> 2) * 1024 + (kk & 3) * 2, dV + kk * 128, id_av, true);
-                umma_commit(bar_mma2);
-                if (sb + 1 < nsb) {  // Q, K, V tiles free again once every MMA of the block is done
-                    ok = mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
-                    if (ok) issue_qkv(sb + 1);
+                umma_commit(bar_mma2);  // the output needs only this; the state update follows
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // (S - S0)^T += V^T K
+                    umma_bf16(tmem + L::T_STATE, dV + kk * 128, dKS + kk * 128, id_state, sb > 0 || kk > 0);
+                umma_commit(bar_mma2s);
+                if (sb + 1 < nsb) {  // the tiles are free again once every MMA of the block is done
+                    ok = mbar_wait(bar_mma2s, par, ERR_TIMEOUT_MMA);
+                    if (ok) issue_v(sb + 1);
+                    ok = ok && mbar_wait(bar_qkr, par, ERR_TIMEOUT_MMA);  // and q . z / column sums too
+                    if (ok) issue_qk(sb + 1);
                 }
             }
         }
@@ -201,26 +231,52 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t par = sb & 1;
             const int row0 = sb * 128;
             const bool last = sb + 1 == nsb;
-            if (sb == 0) {  // carry in: state^T <- S0^T (TMEM), operand rows <- bf16(S0)^T
+            // ---- masked score row -> bf16 A operand; fp32 row sum
+            if (t == 0) tma_store_wait_read();  // the previous block's output tile has left AT
+            epi_sync();
+            mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            float rsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // score columns [64*half, 64*half + 64) -> atom `half`
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_SCORE + 64 * half, r);
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
+                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
+                        rsum += x0 + x1;
+                        w[e] = pack_bf16(x0, x1);
+                    }
+                    *reinterpret_cast<uint4*>(sm + L::AT + half * 16384 + sw_chunk(t, chunk)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_abd);
+            if (sb == 0) {  // carry in: S^T operand rows <- bf16(S0)^T.  Thread t converts column
+                            // c = t % 64, rows p in [32h, 32h+32) with h = t / 64 (conflict-free reads)
                 mbar_wait(bar_s0, 0, ERR_TIMEOUT_TMA);
-                const float* s0s = reinterpret_cast<const float*>(sm + L::AT);
+                const float* s0s = reinterpret_cast<const float*>(sm + L::S0F);
+                const int cc = t & 63, h = t >> 6;
                 uint32_t r[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int q = 0; q < 4; ++q) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = sthr ? __float_as_uint(s0s[(32 * h + j) * D + c]) : 0u;
-                    if (sthr)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + c, 4 * h + q)) = pack8(r + 8 * q, 1.f);
-                    tmem_st32(tmem + lane_base + L::T_STATE + 32 * h, r);
+                    for (int j = 0; j < 8; ++j) r[8 * q + j] = __float_as_uint(s0s[(32 * h + 8 * q + j) * D + cc]);
+                    *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + cc, 4 * h + q)) = pack8(r + 8 * q, 1.f);
                 }
                 fence_async_smem();
-                tc_fence_before();
                 mbar_arrive(bar_sst);
             }
-            // ---- column sums of K: thread (cc, rg) sums 8 rows x 8 columns, then the warp's 32 rows
-            mbar_wait(bar_load, par, ERR_TIMEOUT_TMA);
+            // ---- while I2 runs: column sums of K (thread (cc, rg) sums 8 rows x 8 columns, then
+            //      the warp's 32 rows) and q_t . z
+            mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
             {
                 const int cc = t & 7, rg = t >> 3;
                 float s[8];
@@ -263,59 +319,48 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     }
                 }
             }
-            // ---- masked score row -> bf16 A operand; fp32 row sum
-            if (t == 0) tma_store_wait_read();  // the previous block's output tile has left AT
-            epi_sync();
-            mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
-            tc_fence_after();
-            float rsum = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {  // score columns [64*half, 64*half + 64) -> atom `half`
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_SCORE + 64 * half, r);
-#pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * half + 8 * chunk + 2 * e;
-                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
-                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
-                        rsum += x0 + x1;
-                        w[e] = pack_bf16(x0, x1);
-                    }
-                    *reinterpret_cast<uint4*>(sm + L::AT + half * 16384 + sw_chunk(t, chunk)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_abd);
+            mbar_arrive(bar_qkr);
             epi_sync();  // every warp's column sums are in zpart; every q . z has read zin
             if (t < D) zin[t] += zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
             // ---- output row -> staging (AT is free once I2 is done); state hand-off
             mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             {
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_NUM, r);
                 const float inv = 1.f / (rsum + qz + eps);
 #pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk)
-                    *reinterpret_cast<uint4*>(sm + L::AT + sw_chunk(t, chunk)) = pack8(r + 8 * chunk, inv);
-            }
-            {
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_STATE, r);
-                if (sthr) {
-                    if (last) {  // S_out staging in QT (free after the last block), fp32 [p][c]
-                        float* st = reinterpret_cast<float*>(sm + L::QT);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_NUM + 32 * h, r);
 #pragma unroll
-                        for (int p = 0; p < 64; ++p) st[p * D + c] = __uint_as_float(r[p]);
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(sm + L::AT + sw_chunk(t, 4 * h + q)) = pack8(r + 8 * q, inv);
+                }
+            }
+            if (last) {  // the output tile leaves while the state is staged
+                fence_async_smem();
+                epi_sync();
+                if (t == 0) {
+                    tma_store_3d(&to, sm + L::AT, 0, row0, g);
+                    tma_store_commit();
+                }
+            }
+            mbar_wait(bar_mma2s, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // S = S0 + (S - S0): state thread c holds column c
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + L::T_STATE + 32 * h, r);
+                if (sthr) {
+                    float* s0s = reinterpret_cast<float*>(sm + L::S0F) + 32 * h * D + c;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + s0s[j * D]);
+                    if (last) {  // S_out staging: S0F in place (its S0 is no longer needed)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s0s[j * D] = __uint_as_float(r[j]);
                     } else {
 #pragma unroll
-                        for (int chunk = 0; chunk < 8; ++chunk)
-                            *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + c, chunk)) = pack8(r + 8 * chunk, 1.f);
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(sm + L::KS + sw_chunk(128 + c, 4 * h + q)) = pack8(r + 8 * q, 1.f);
                     }
                 }
             }
@@ -324,8 +369,8 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tc_fence_before();
             epi_sync();  // staging complete; the new zin is complete before the next block's q . z
             if (t == 0) {
-                tma_store_3d(&to, sm + L::AT, 0, row0, g);
-                if (last && S_out) bulk_store(S_out + (size_t)g * D * D, sm + L::QT, 16384);
+                if (!last) tma_store_3d(&to, sm + L::AT, 0, row0, g);
+                if (last && S_out) bulk_store(S_out + (size_t)g * D * D, sm + L::S0F, 16384);
                 tma_store_commit();
             }
             mbar_arrive(bar_sst);  // next block: state operand ready, numerator / state TMEM read
