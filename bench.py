@@ -39,8 +39,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of each kernel on this workload, with the hash of the kernel sources they were taken on
 # (profiles/la_*_tc_fractus1b_G160_C128_D64.md).  Reported as null once the sources differ.
 NCU_TRAFFIC = {
-    "la_fwd": {"bytes": 10573056 + 0, "src": "5cd7767ca8813681"},
-    "la_bwd": {"bytes": 15885824 + 0, "src": "5cd7767ca8813681"},
+    "la_fwd": {"bytes": 10573056 + 0, "src": "dcce567ed8c9cf5d"},
+    "la_bwd": {"bytes": 15884544 + 0, "src": "dcce567ed8c9cf5d"},
 }
 
 
