@@ -17,6 +17,7 @@ One JSON line is printed by rank 0.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -39,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of each kernel on this workload, with the hash of the kernel sources they were taken on
 # (profiles/la_*_tc_fractus1b_G160_C128_D64.md).  Reported as null once the sources differ.
 NCU_TRAFFIC = {
-    "la_fwd": {"bytes": 10573056 + 0, "src": "dcce567ed8c9cf5d"},
-    "la_bwd": {"bytes": 15884544 + 0, "src": "dcce567ed8c9cf5d"},
+    "la_fwd": {"bytes": 10573056 + 0, "src": "4543ef3249fa8b73"},
+    "la_bwd": {"bytes": 15884544 + 0, "src": "4543ef3249fa8b73"},
 }
 
 
@@ -48,8 +49,7 @@ def kernel_source_hash():
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "causal_linear_attention_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
-    files.append(os.path.join(ROOT, "include", "la.h"))
+    files = sorted(glob.glob(os.path.join(csrc, "*.cuh")))  # the kernel bodies
     h = hashlib.sha256()
     for f in files:
         with open(f, "rb") as fh:
@@ -275,7 +275,7 @@ def run_ours(args, rank, world, local):
     bwd_secs = max_over_ranks(timed(bwd, n_k)) / n_k
 
     # end to end through the public API: pinned host inputs -> device -> fwd + bwd -> host outputs
-    e2e = run_e2e(args, host, one, fwd, bwd, stream, barrier, max_over_ranks, G, C)
+    e2e = run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks)
 
     tokens = G * C
     value = world * tokens * args.steps / secs
@@ -318,40 +318,107 @@ def run_ours(args, rank, world, local):
     return out
 
 
-def run_e2e(args, host, one, fwd, bwd, stream, barrier, max_over_ranks, G, C):
+def gpu_local_cpus(local):
+    """CPUs of the NUMA node the GPU is attached to (Linux sysfs), intersected with this
+    process's allowed CPUs; None when that cannot be determined."""
     import torch
-    pinned_in = {k: t.pin_memory() for k, t in host.tensors().items()}
-    outs = [one.o, one.S_out, one.z_out, *one.grads]
-    pinned_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
-    dev_in = one.x.tensors()
+    props = torch.cuda.get_device_properties(local)
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    else:
+        try:
+            cudart = ctypes.CDLL(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64",
+                                              "libcudart.so"))
+        except OSError:
+            return None
+        buf = ctypes.create_string_buffer(64)
+        if cudart.cudaDeviceGetPCIBusId(buf, 64, local) != 0:
+            return None
+        bus = buf.value.decode().lower()
+    try:
+        node = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+        if node < 0:
+            return None
+        cpus = set()
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+    except (OSError, ValueError):
+        return None
+    cpus &= os.sched_getaffinity(0)
+    return cpus or None
 
-    def e2e_step():
-        for k, t in pinned_in.items():
-            dev_in[k].copy_(t, non_blocking=True)
-        fwd(one)
-        bwd(one)
-        for d, h in zip(outs, pinned_out):
-            h.copy_(d, non_blocking=True)
 
-    n = min(args.steps, 1000)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(n):
-            e2e_step()
-    torch.cuda.synchronize()
-    secs = max_over_ranks(time.perf_counter() - t0)
-    barrier()
+def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
+    """End to end through the C ABI with HOST buffers: every step copies its inputs from
+    pinned host memory into a device workspace, runs forward + backward and copies every
+    output back (la_chunked_step_host).  Two streams with a workspace and an output set
+    each let one step's copies overlap the next step's, as a pipelined caller would."""
+    import torch
+
+    import causal_linear_attention_gb300 as la
+    dev = torch.device("cuda", local)
+    old_aff = os.sched_getaffinity(0)
+    near = gpu_local_cpus(local)
+    if near:
+        os.sched_setaffinity(0, near)  # pinned buffers get first-touched next to the GPU
+    try:
+        pin = {k: (None if t is None else t.pin_memory()) for k, t in host.__dict__.items()}
+        q = pin["q"]
+
+        def outs():
+            f = lambda *shape: torch.empty(*shape, dtype=torch.float32, pin_memory=True)
+            return (torch.empty_like(q, pin_memory=True), f(G, D, D), f(G, D), torch.empty_like(q, pin_memory=True),
+                    torch.empty_like(q, pin_memory=True), torch.empty_like(q, pin_memory=True), f(G, D, D), f(G, D))
+
+        sets = [(outs(), la.step_workspace(G, C, D, q.dtype, dev), torch.cuda.Stream(device=dev)) for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in sets[0][0])
+
+        def step(i):
+            out, ws, s = sets[i % 2]
+            la.chunked_step_host(pin["q"], pin["k"], pin["v"], pin["S0"], pin["z0"], pin["dO"], pin["dS_out"],
+                                 pin["dz_out"], out=out, workspace=ws, block=block, eps=eps, stream=s)
+
+        n = min(args.steps, 2000)
+        for i in range(4):
+            step(i)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n):
+            step(i)
+        for _, _, s in sets:
+            s.synchronize()
+        secs = max_over_ranks(time.perf_counter() - t0)
+        barrier()
+        # the copies alone, for context: one H2D of the step's input bytes, one D2H of its output bytes
+        s = sets[0][2]
+        hb = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
+        db = torch.empty(max(h2d, d2h), dtype=torch.uint8, device=dev)
+        gbs = {}
+        for name, (dst, src, nb) in {"h2d": (db[:h2d], hb, h2d), "d2h": (hb[:d2h], db[:d2h], d2h)}.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    dst.copy_(src, non_blocking=True)
+                e0.record(s)
+                for _ in range(20):
+                    dst.copy_(src, non_blocking=True)
+                e1.record(s)
+            s.synchronize()
+            gbs[name] = round(20 * nb / (e0.elapsed_time(e1) / 1e3) / 1e9, 1)
+    finally:
+        os.sched_setaffinity(0, old_aff)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": world * G * C * n / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "api": "causal_linear_attention_gb300.chunked_fwd/chunked_bwd, pinned host buffers"}
+            "steps": n, "api": "la_chunked_step_host (C ABI, pinned host buffers), two streams",
+            "host_cpus": f"{len(near)} cpus of the GPU's NUMA node" if near else "unrestricted",
+            "copy_gbs": gbs}
 
 
 # ---------------------------------------------------------------- the oracle on the host cores

@@ -20,9 +20,11 @@ from typing import Optional
 
 from . import _lib
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
-                   la_device_status, la_status_string, la_version, lib)
+                   la_chunked_step_host, la_device_status, la_status_string, la_step_workspace_bytes, la_version,
+                   lib)
 
-__all__ = ["chunked_fwd", "chunked_bwd", "la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c", "la_device_status",
+__all__ = ["chunked_fwd", "chunked_bwd", "chunked_step_host", "step_workspace", "la_chunked_fwd", "la_chunked_bwd",
+           "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
 
 
@@ -89,3 +91,47 @@ def chunked_bwd(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 6
     la_chunked_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block,
                    _dtype_code(q), eps, _stream(stream))
     return dq, dk, dv, dS0, dz0
+
+
+def step_workspace(G: int, C: int, D: int, dtype, device=None):
+    """Device workspace (uint8 CUDA tensor) for chunked_step_host on this shape."""
+    import torch
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32 if dtype == torch.float32 else None
+    if code is None:
+        raise TypeError(f"dtype must be bfloat16 or float32, got {dtype}")
+    n = la_step_workspace_bytes(G, C, D, code)
+    if n == 0 and G * C * D > 0:
+        raise ValueError(f"unsupported shape G={G} C={C} D={D}")
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def chunked_step_host(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, out, workspace, block: int = 64,
+                      eps: float = 1e-6, stream=None):
+    """Forward + backward of one chunk with HOST tensors (CPU, ideally pinned): copies the
+    inputs into `workspace` (from step_workspace), runs the two kernels and copies the
+    results into `out` = (o, S_out, z_out, dq, dk, dv, dS0, dz0) (CPU tensors; the carry
+    entries may be None), all on `stream`.  The results are valid once the stream is done."""
+    import torch
+    G, C, D = q.shape
+    dt = q.dtype
+    cpu = torch.device("cpu")
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _check_tensor(n, t, q.shape, dt, cpu)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D)), ("dS_out", dS_out, (G, D, D)),
+                      ("dz_out", dz_out, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, cpu)
+    o, S_out, z_out, dq, dk, dv, dS0, dz0 = out
+    for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(n, t, q.shape, dt, cpu)
+    for n, t, shp in (("S_out", S_out, (G, D, D)), ("z_out", z_out, (G, D)), ("dS0", dS0, (G, D, D)),
+                      ("dz0", dz0, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, cpu)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    la_chunked_step_host(q, k, v, S0, z0, dO, dS_out, dz_out, o, S_out, z_out, dq, dk, dv, dS0, dz0,
+                         workspace, workspace.numel() * workspace.element_size(), G, C, D, block,
+                         _dtype_code(q), eps, _stream(stream) if stream is not None else
+                         torch.cuda.current_stream(workspace.device).cuda_stream)
+    return out

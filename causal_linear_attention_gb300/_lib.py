@@ -83,6 +83,10 @@ def lib():
         L.la_chunked_bwd.restype = I
         L.la_device_status.argtypes = [I]
         L.la_device_status.restype = I
+        L.la_step_workspace_bytes.argtypes = [I, I, I, I]
+        L.la_step_workspace_bytes.restype = ctypes.c_size_t
+        L.la_chunked_step_host.argtypes = [P] * 17 + [ctypes.c_size_t, I, I, I, I, I, F, P]
+        L.la_chunked_step_host.restype = I
         L.la_bwd_max_c.argtypes = [I, I, I]
         L.la_bwd_max_c.restype = I
         L.la_status_string.argtypes = [I]
@@ -93,8 +97,8 @@ def lib():
         return L
 
 
-EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c", "la_device_status", "la_status_string",
-           "la_version")
+EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
+           "la_device_status", "la_status_string", "la_version")
 
 
 def _p(x) -> Optional[int]:
@@ -124,6 +128,19 @@ def la_chunked_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G:
     _check(lib().la_chunked_bwd(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(dO), _p(dS_out), _p(dz_out),
                                 _p(dq), _p(dk), _p(dv), _p(dS0), _p(dz0), G, C, D, block, dtype, eps,
                                 _p(stream)))
+
+
+def la_step_workspace_bytes(G: int, C: int, D: int, dtype: int) -> int:
+    return int(lib().la_step_workspace_bytes(G, C, D, dtype))
+
+
+def la_chunked_step_host(q, k, v, S0, z0, dO, dS_out, dz_out, o, S_out, z_out, dq, dk, dv, dS0, dz0,
+                         workspace, workspace_bytes: int, G: int, C: int, D: int, block: int, dtype: int,
+                         eps: float, stream=None) -> None:
+    """Raw C-ABI call: tensors are HOST pointers / CPU tensors, workspace is device memory."""
+    _check(lib().la_chunked_step_host(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(dO), _p(dS_out), _p(dz_out),
+                                      _p(o), _p(S_out), _p(z_out), _p(dq), _p(dk), _p(dv), _p(dS0), _p(dz0),
+                                      _p(workspace), workspace_bytes, G, C, D, block, dtype, eps, _p(stream)))
 
 
 def la_bwd_max_c(D: int, block: int, dtype: int) -> int:

@@ -349,6 +349,87 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
     return LA_ERR_UNSUPPORTED;
 }
 
+// ---------------------------------------------------------------- host-buffer step
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+size_t ws_round(size_t n) { return (n + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+// Workspace slots, in order: q, k, v, dO, S0, z0, dS_out, dz_out (inputs), then
+// o, dq, dk, dv, S_out, z_out, dS0, dz0 (outputs).  Returns the total size.
+size_t ws_layout(size_t n_x, size_t n_S, size_t n_z, size_t off[16])
+{
+    const size_t sizes[16] = {n_x, n_x, n_x, n_x, n_S, n_z, n_S, n_z, n_x, n_x, n_x, n_x, n_S, n_z, n_S, n_z};
+    size_t at = 0;
+    for (int i = 0; i < 16; ++i) {
+        off[i] = at;
+        at += ws_round(sizes[i]);
+    }
+    return at;
+}
+
+}  // namespace
+
+extern "C" size_t la_step_workspace_bytes(int G, int C, int D, la_dtype dtype)
+{
+    size_t esz = 0;
+    if (check_common(G, C, D, 64, dtype, 0.f, &esz) != LA_OK) return 0;
+    size_t off[16];
+    return ws_layout((size_t)G * C * D * esz, (size_t)G * D * D * 4, (size_t)G * D * 4, off);
+}
+
+extern "C" la_status la_chunked_step_host(const void* q, const void* k, const void* v, const float* S0,
+                                          const float* z0, const void* dO, const float* dS_out,
+                                          const float* dz_out, void* o, float* S_out, float* z_out, void* dq,
+                                          void* dk, void* dv, float* dS0, float* dz0, void* workspace,
+                                          size_t workspace_bytes, int G, int C, int D, int block, la_dtype dtype,
+                                          float eps, void* stream)
+{
+    size_t esz = 0;
+    la_status st = check_common(G, C, D, block, dtype, eps, &esz);
+    if (st != LA_OK) return st;
+    const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    size_t off[16];
+    const size_t need = ws_layout(n_x, n_S, n_z, off);
+    const bool t = n_x > 0;
+    const void* host[16] = {q, k, v, dO, S0, z0, dS_out, dz_out, o, dq, dk, dv, S_out, z_out, dS0, dz0};
+    const bool req[16] = {t, t, t, t, false, false, false, false, t, t, t, t, false, false, false, false};
+    for (int i = 0; i < 16; ++i)
+        if (req[i] && !host[i]) return LA_ERR_INVALID;
+    const Buf ins[] = {{q, n_x}, {k, n_x}, {v, n_x}, {dO, n_x}, {S0, n_S}, {z0, n_z}, {dS_out, n_S}, {dz_out, n_z}};
+    const Buf outs[] = {{o, n_x}, {dq, n_x}, {dk, n_x}, {dv, n_x}, {S_out, n_S}, {z_out, n_z}, {dS0, n_S}, {dz0, n_z}};
+    const int inplace[] = {-1, -1, -1, -1, 4, 5, 6, 7};
+    if (!disjoint(outs, 8, ins, 8, inplace)) return LA_ERR_INVALID;
+    if (G == 0) return LA_OK;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kWsAlign != 0 || workspace_bytes < need)
+        return LA_ERR_INVALID;
+    const size_t bytes[16] = {n_x, n_x, n_x, n_x, n_S, n_z, n_S, n_z, n_x, n_x, n_x, n_x, n_S, n_z, n_S, n_z};
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    void* dev[16];
+    for (int i = 0; i < 16; ++i) dev[i] = host[i] && bytes[i] ? ws + off[i] : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < 8; ++i)
+        if (dev[i] && cudaMemcpyAsync(dev[i], host[i], bytes[i], cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_CUDA;
+        }
+    auto F = [](void* p) { return static_cast<float*>(p); };
+    st = la_chunked_fwd(dev[0], dev[1], dev[2], F(dev[4]), F(dev[5]), dev[8], F(dev[12]), F(dev[13]), G, C, D, block,
+                        dtype, eps, stream);
+    if (st != LA_OK) return st;
+    st = la_chunked_bwd(dev[0], dev[1], dev[2], F(dev[4]), F(dev[5]), dev[3], F(dev[6]), F(dev[7]), dev[9], dev[10],
+                        dev[11], F(dev[14]), F(dev[15]), G, C, D, block, dtype, eps, stream);
+    if (st != LA_OK) return st;
+    for (int i = 8; i < 16; ++i)
+        if (dev[i] && cudaMemcpyAsync(const_cast<void*>(host[i]), dev[i], bytes[i], cudaMemcpyDeviceToHost, s) !=
+                          cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_CUDA;
+        }
+    return LA_OK;
+}
+
 extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
 {
     const int lim = smem_optin_limit(nullptr);

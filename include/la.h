@@ -48,6 +48,8 @@
 #ifndef LA_H
 #define LA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -112,6 +114,45 @@ int la_bwd_max_c(int D, int block, la_dtype dtype);
  * (LA_ERR_DEVICE) since the last clear; such a call's outputs are not valid.
  * clear != 0 resets the flag. */
 la_status la_device_status(int clear);
+
+/*
+ * Host-buffer form of one training step of a chunk (forward, then the backward of
+ * section 1 on the same inputs), for callers whose tensors start and end in host
+ * memory.  The page has no counterpart: its chunked form runs on device tensors.
+ *
+ * la_step_workspace_bytes gives the device workspace the call needs for this shape:
+ * room for every input and output tensor, each at a 256-byte boundary; 0 when the
+ * shape or dtype is invalid or unsupported.  It makes no CUDA call.
+ *
+ * la_chunked_step_host enqueues on `stream`, in this order: one cudaMemcpyAsync per
+ * present input (q, k, v, S0, z0, dO, dS_out, dz_out; host -> workspace), the
+ * la_chunked_fwd and la_chunked_bwd launches on those copies, and one cudaMemcpyAsync
+ * per requested output (o, S_out, z_out, dq, dk, dv, dS0, dz0; workspace -> host).
+ *   - Every tensor pointer is HOST memory with the layouts above.  Page-locked memory
+ *     (cudaHostAlloc / cudaHostRegister) keeps the copies asynchronous; pageable
+ *     memory works, but then the copies synchronise with the host.  The outputs are
+ *     valid once the stream has completed.
+ *   - S0, z0, dS_out, dz_out may be NULL (zeros); S_out, z_out, dS0, dz0 may be NULL
+ *     (not computed).  q, k, v, dO, o, dq, dk, dv are required when G * C > 0.
+ *     S_out may equal S0, z_out z0, dS0 dS_out and dz0 dz_out (the inputs are copied
+ *     in before any output is copied out); no other overlap is allowed.
+ *   - workspace: DEVICE memory owned by the caller, 256-byte aligned, at least
+ *     la_step_workspace_bytes(G, C, D, dtype) bytes, not used by anything else until
+ *     the stream has completed.  The library allocates nothing.
+ *   - Errors: argument checks run first and enqueue nothing on failure
+ *     (LA_ERR_INVALID / LA_ERR_UNSUPPORTED); LA_ERR_CUDA means a copy or launch failed
+ *     and part of the step may already be enqueued.
+ */
+size_t la_step_workspace_bytes(int G, int C, int D, la_dtype dtype);
+
+la_status la_chunked_step_host(const void* q, const void* k, const void* v,
+                               const float* S0, const float* z0,
+                               const void* dO, const float* dS_out, const float* dz_out,
+                               void* o, float* S_out, float* z_out,
+                               void* dq, void* dk, void* dv, float* dS0, float* dz0,
+                               void* workspace, size_t workspace_bytes,
+                               int G, int C, int D, int block, la_dtype dtype, float eps,
+                               void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* la_status_string(la_status status);

@@ -29,8 +29,9 @@ def declared_functions():
 
 
 def test_header_declares_the_boundary():
-    assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_bwd_max_c",
-                                           "la_device_status", "la_status_string", "la_version"])
+    assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_step_workspace_bytes",
+                                           "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
+                                           "la_status_string", "la_version"])
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -110,6 +111,58 @@ def test_raw_binding_raises_on_error(L):
     with pytest.raises(la.LAError) as e:
         la.la_chunked_fwd(A, A, A, None, None, A, None, None, 1, 8, 64, 64, la.LA_BF16, 1e-6)
     assert e.value.status == 1  # o overlaps the inputs: rejected before any CUDA call
+
+
+@pytest.mark.parametrize("G,C,D,dtype", [(160, 128, 64, 1), (3, 200, 128, 1), (8, 128, 64, 0), (1, 1, 64, 1),
+                                         (0, 128, 64, 1), (5, 0, 64, 0)])
+def test_step_workspace_bytes_closed_form(L, G, C, D, dtype):
+    """Sixteen slots (8 token tensors, 4 D x D carries, 4 length-D carries), each
+    rounded up to 256 bytes."""
+    e = 4 if dtype == 0 else 2
+    r = lambda n: (n + 255) // 256 * 256
+    want = 8 * r(G * C * D * e) + 4 * r(G * D * D * 4) + 4 * r(G * D * 4)
+    assert la.la_step_workspace_bytes(G, C, D, dtype) == want
+
+
+def test_step_workspace_bytes_rejects_bad_shapes(L):
+    assert la.la_step_workspace_bytes(2, 8, 96, 1) == 0
+    assert la.la_step_workspace_bytes(-1, 8, 64, 1) == 0
+    assert la.la_step_workspace_bytes(2, 8, 64, 9) == 0
+
+
+# Host-buffer step: fake host pointers; every call below must fail its argument checks
+# before any copy is enqueued (G = 0 returns before touching anything).
+H = 0x7F0000000000
+
+
+def step(**kw):
+    names = ("q", "k", "v", "S0", "z0", "dO", "dS_out", "dz_out", "o", "S_out", "z_out", "dq", "dk", "dv", "dS0",
+             "dz0")
+    args = {n: H + i * 0x1000000 for i, n in enumerate(names)}
+    for n in ("S0", "z0", "dS_out", "dz_out", "S_out", "z_out", "dS0", "dz0"):
+        args[n] = None
+    args.update(workspace=0x20000000, workspace_bytes=1 << 30, G=2, C=8, D=64, block=64, dtype=la.LA_BF16,
+                eps=1e-6)
+    args.update(kw)
+    L = la.lib()
+    return L.la_chunked_step_host(*(args[n] for n in names), args["workspace"], args["workspace_bytes"],
+                                  args["G"], args["C"], args["D"], args["block"], args["dtype"], args["eps"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), INVALID), (dict(dO=None), INVALID), (dict(o=None), INVALID), (dict(dv=None), INVALID),
+    (dict(workspace=None), INVALID), (dict(workspace_bytes=1000), INVALID), (dict(workspace=0x20000010), INVALID),
+    (dict(o=H), INVALID),                                   # output overlaps q
+    (dict(dq=H + 0x8000000 + 0x100), INVALID),             # dq overlaps o
+    (dict(S0=H + 0x30000000, S_out=H + 0x30000040), INVALID),  # partial overlap of the carry
+    (dict(D=96), UNSUPPORTED), (dict(dtype=5), UNSUPPORTED), (dict(G=-3), INVALID),
+])
+def test_host_step_argument_checks(L, kw, status):
+    assert step(**kw) == status
+
+
+def test_host_step_empty_problem_is_accepted_without_copies(L):
+    assert step(G=0) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
