@@ -82,6 +82,34 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(rank):
+    """Each rank draws its own groups: weak scaling over independent groups, no collective
+    in the data path."""
+    return 1000 + rank
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """The slowest rank's time (the job's time); a no-op on one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_value(world, G, C, steps, secs):
+    """Whole-job throughput: the G*C tokens every rank processed in each step / the job time."""
+    return world * G * C * steps / secs
+
+
 def cpu_model():
     try:
         out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
@@ -190,7 +218,7 @@ def run_ours(args, rank, world, local):
 
     # one seeded set of inputs (each rank draws its own groups), replicated into enough
     # buffer sets that the rotation touches > 4x L2 between two uses of a set
-    host = make_inputs(G, C, D, dtype="bf16", seed=1000 + rank, grads=True)
+    host = make_inputs(G, C, D, dtype="bf16", seed=rank_seed(rank), grads=True)
     base = host.to(dev)
     one = StepBuffers(base, G, C, D)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -234,7 +262,7 @@ def run_ours(args, rank, world, local):
         if g_full is not None:  # one untimed replay: graph upload / first-launch costs
             g_full.replay()
         torch.cuda.synchronize()
-        barrier()
+        bar()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -246,39 +274,29 @@ def run_ours(args, rank, world, local):
                 g_rest.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-        barrier()
+        bar()
         return e0.elapsed_time(e1) / 1e3
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    bar = lambda: barrier(world)
+    mor = lambda x: max_over_ranks(x, world, dev)
 
     clocks = ClockSampler(local)
     clocks.start()
     t_wall0 = time.time()
-    secs = max_over_ranks(timed(step, args.steps))
+    secs = mor(timed(step, args.steps))
     clocks.mark(t_wall0, time.time())
     clock_info = clocks.stop()
 
     # per-kernel average launch durations (same rotation, same stream)
     n_k = max(args.steps, 64)
-    fwd_secs = max_over_ranks(timed(fwd, n_k)) / n_k
-    bwd_secs = max_over_ranks(timed(bwd, n_k)) / n_k
+    fwd_secs = mor(timed(fwd, n_k)) / n_k
+    bwd_secs = mor(timed(bwd, n_k)) / n_k
 
     # end to end through the public API: pinned host inputs -> device -> fwd + bwd -> host outputs
-    e2e = run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks)
+    e2e = run_e2e(args, host, G, C, D, block, eps, local, bar, mor)
 
     tokens = G * C
-    value = world * tokens * args.steps / secs
+    value = job_value(world, G, C, args.steps, secs)
     hbm, peak_src = measured_peaks()
     kernels = {
         "la_fwd": {"avg_us": fwd_secs * 1e6, "alg_bytes": fwd_bytes, "gbs": fwd_bytes / fwd_secs / 1e9},
@@ -295,7 +313,7 @@ def run_ours(args, rank, world, local):
         kernels[k]["frac"] = round(kernels[k]["gbs"] / hbm, 4)
         kernels[k]["avg_us"] = round(kernels[k]["avg_us"], 3)
         kernels[k]["gbs"] = round(kernels[k]["gbs"], 1)
-    fwd_only = world * tokens / fwd_secs
+    fwd_only = job_value(world, G, C, 1, fwd_secs)
 
     out = None
     if rank == 0:
@@ -415,7 +433,8 @@ def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
     finally:
         os.sched_setaffinity(0, old_aff)
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    return {"value": world * G * C * n / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    return {"value": job_value(world, G, C, n, secs), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
             "steps": n, "api": "la_chunked_step_host (C ABI, pinned host buffers), two streams",
             "host_cpus": f"{len(near)} cpus of the GPU's NUMA node" if near else "unrestricted",
             "copy_gbs": gbs}
@@ -455,14 +474,14 @@ def run_reference(args, rank, world):
     from causal_linear_attention_gb300.inputs import make_inputs
     G, C, D, eps = (WORKLOAD[k] for k in ("G", "C", "D", "eps"))
     oracle.build()
-    host = make_inputs(G, C, D, dtype="bf16", seed=1000, grads=True)
+    host = make_inputs(G, C, D, dtype="bf16", seed=rank_seed(0), grads=True)
     # each step: a bounded sample of the workload sized so the whole run takes a few minutes
     t0 = time.perf_counter()
     oracle_step(host, eps)
     one = time.perf_counter() - t0
-    budget_per_step = 120.0 / max(1, args.steps + args.warmup)
+    budget_per_step = args.ref_seconds / max(1, args.steps + args.warmup)
     g_sample = max(1, min(G, int(G * budget_per_step / max(one, 1e-9))))
-    sample = make_inputs(g_sample, C, D, dtype="bf16", seed=1000, grads=True)
+    sample = make_inputs(g_sample, C, D, dtype="bf16", seed=rank_seed(0), grads=True)
     for _ in range(args.warmup):
         oracle_step(sample, eps)
     t0 = time.perf_counter()
@@ -490,6 +509,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: CPU seconds the whole run aims at (sizes the bounded sample)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
