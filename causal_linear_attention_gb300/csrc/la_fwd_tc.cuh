@@ -14,7 +14,8 @@
 // rows of a block (thread t <-> TMEM lane t), warp 4 is the producer (TMA loads; one lane
 // issues every tcgen05.mma).  Per block:
 //   I1a    A = Q K^T                     (M=128, N=128, K=64: 4 instructions)
-//   EPI1   row t: mask j <= t, fp32 row sum, bf16 row -> the A operand of A V
+//   EPI1   row t: mask j <= t, fp32 row sum, bf16 row -> the A operand of A V, kept in
+//          TMEM over the scores it came from (the tensor core reads A from TMEM)
 //   I1b    num = Q S                     (S^T rows as the B operand; M=128, N=64: 4)
 //   I2     num += A V                    (M=128, N=64, K=128: 8 instructions)
 //   ST     (S - S0)^T += V^T K           (M=64, N=64, K=128: 8 instructions; committed
@@ -35,10 +36,10 @@
 //   KS   24576  rows 0-127 = K (TMA; B operand of I1a, MN-major B of the state update),
 //               rows 128-191 = S^T (bf16, epilogue; B operand of I1b)
 //   VT   16384  V rows (MN-major B of A V, MN-major A of the state update)
-//   AT   32768  the masked scores (atom 0 = cols 0-63, atom 1 = 64-127), then the output
-//               tile staging (first 16 KB)
+//   AT   16384  the output tile staging
 //   S0F  16384  S0 (fp32 [p][c]) as it arrives; after the last block, S_out (staging)
-// TMEM (256 columns): [0,128) scores, [128,192) numerator, [192,256) (S - S0)^T (M=64 layout).
+// TMEM (256 columns): [0,128) scores, then [0,64) the bf16 A operand (two keys per column);
+// [128,192) numerator; [192,256) (S - S0)^T (M=64 layout).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -51,14 +52,14 @@ struct FwdTcLayout {
     static constexpr uint32_t KS = 16384;
     static constexpr uint32_t VT = 40960;
     static constexpr uint32_t AT = 57344;
-    static constexpr uint32_t S0F = 90112;    // S0 (fp32 [p][c]) as it arrives
-    static constexpr uint32_t ZIN = 106496;   // float[64]: z before the block
-    static constexpr uint32_t ZPART = 106752; // float[4][64]: per-warp column sums of K
-    static constexpr uint32_t BARS = 107776;  // mbarriers + TMEM address slot
-    static constexpr uint32_t END = 107904;
+    static constexpr uint32_t S0F = 73728;    // S0 (fp32 [p][c]) as it arrives
+    static constexpr uint32_t ZIN = 90112;    // float[64]: z before the block
+    static constexpr uint32_t ZPART = 90368;  // float[4][64]: per-warp column sums of K
+    static constexpr uint32_t BARS = 91392;   // mbarriers + TMEM address slot
+    static constexpr uint32_t END = 91520;
     static constexpr uint32_t BYTES = END;    // two CTAs per SM; the base alignment is checked instead
     static constexpr uint32_t TMEM_COLS = 256;
-    static constexpr uint32_t T_SCORE = 0, T_NUM = 128, T_STATE = 192;
+    static constexpr uint32_t T_SCORE = 0, T_A = 0, T_NUM = 128, T_STATE = 192;
     static constexpr int THREADS = 160;
     static constexpr int BOX_ROWS = 128;                     // token rows per TMA box (Q, K, V)
     static constexpr uint32_t LOAD_BYTES = 3 * BOX_ROWS * 128;  // Q, K, V boxes of one block
@@ -165,12 +166,12 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 mbar_expect_tx(bar_v, L::LOAD_BYTES / 3);
                 tma_load_3d(sm + L::VT, &tv, bar_v, 0, sb * 128, g);
             };
-            if (nsb > 0) {  // in the order the work needs them: Q, K (I1), the carry (I1), V
-                issue_qk(0);
+            if (nsb > 0) {  // the carry first (its conversion runs while Q, K land), then Q, K, V
                 // (with neither S0 nor z0 this arrival alone completes the phase)
                 mbar_expect_tx(bar_s0, (S0 ? 16384u : 0u) + (z0 ? 256u : 0u));
                 if (S0) bulk_load(sm + L::S0F, S0 + (size_t)g * D * D, 16384, bar_s0);
                 if (z0) bulk_load(sm + L::ZIN, z0 + (size_t)g * D, 256, bar_s0);
+                issue_qk(0);
                 issue_v(0);
             }
             pdl_launch_dependents();
@@ -179,7 +180,6 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint64_t dQ = smem_desc(sbase + L::QT, 16, 1024);
             const uint64_t dKS = smem_desc(sbase + L::KS, 16, 1024);
             const uint64_t dV = smem_desc(sbase + L::VT, 16, 1024);
-            const uint64_t dA = smem_desc(sbase + L::AT, 16, 1024);
             const uint64_t dST = smem_desc(sbase + L::KS + 16384, 16, 1024);
             const uint32_t id_qk = idesc_bf16(128, 128, false, false);
             const uint32_t id_qs = idesc_bf16(128, 64, false, false);
@@ -206,8 +206,8 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // I2: num += A V
-                    umma_bf16(tmem + L::T_NUM, dA + (kk >> 2) * 1024 + (kk & 3) * 2, dV + kk * 128, id_av, true);
+                for (int kk = 0; kk < 8; ++kk)  // I2: num += A V  (A from TMEM, 8 columns per K = 16 step)
+                    umma_bf16_ts(tmem + L::T_NUM, tmem + L::T_A + 8 * kk, dV + kk * 128, id_av, true);
                 umma_commit(bar_mma2);  // the output needs only this; the state update follows
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // (S - S0)^T += V^T K
@@ -231,34 +231,6 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t par = sb & 1;
             const int row0 = sb * 128;
             const bool last = sb + 1 == nsb;
-            // ---- masked score row -> bf16 A operand; fp32 row sum
-            if (t == 0) tma_store_wait_read();  // the previous block's output tile has left AT
-            epi_sync();
-            mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
-            tc_fence_after();
-            float rsum = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {  // score columns [64*half, 64*half + 64) -> atom `half`
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_SCORE + 64 * half, r);
-#pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * half + 8 * chunk + 2 * e;
-                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
-                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
-                        rsum += x0 + x1;
-                        w[e] = pack_bf16(x0, x1);
-                    }
-                    *reinterpret_cast<uint4*>(sm + L::AT + half * 16384 + sw_chunk(t, chunk)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_abd);
             if (sb == 0) {  // carry in: S^T operand rows <- bf16(S0)^T.  Thread t converts column
                             // c = t % 64, rows p in [32h, 32h+32) with h = t / 64 (conflict-free reads)
                 mbar_wait(bar_s0, 0, ERR_TIMEOUT_TMA);
@@ -274,6 +246,29 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 fence_async_smem();
                 mbar_arrive(bar_sst);
             }
+            // ---- masked score row -> bf16 A operand in TMEM (row t in lane t, two keys per
+            //      column: keys [64h, 64h+64) of the row land in columns [32h, 32h+32), over
+            //      score columns this thread has already read); fp32 row sum
+            mbar_wait(bar_mma1, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            float rsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_SCORE + 64 * half, r);
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 64 * half + 2 * e;
+                    const float x0 = j <= t ? __uint_as_float(r[2 * e]) : 0.f;
+                    const float x1 = j + 1 <= t ? __uint_as_float(r[2 * e + 1]) : 0.f;
+                    rsum += x0 + x1;
+                    w[e] = pack_bf16(x0, x1);
+                }
+                tmem_st32(tmem + lane_base + L::T_A + 32 * half, w);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_abd);
             // ---- while I2 runs: column sums of K (thread (cc, rg) sums 8 rows x 8 columns, then
             //      the warp's 32 rows) and q_t . z
             mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
@@ -320,9 +315,10 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             }
             mbar_arrive(bar_qkr);
-            epi_sync();  // every warp's column sums are in zpart; every q . z has read zin
+            if (t == 0) tma_store_wait_read();  // the previous block's output tile has left AT
+            epi_sync();  // every warp's column sums are in zpart; every q . z has read zin; AT is free
             if (t < D) zin[t] += zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
-            // ---- output row -> staging (AT is free once I2 is done); state hand-off
+            // ---- output row -> staging; state hand-off
             mbar_wait(bar_mma2, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             {
