@@ -17,6 +17,7 @@
 #include "la_fwd.cuh"
 #include "la_fwd_tc.cuh"
 #include "la_bwd_tc.cuh"
+#include "la_fwd_tc128.cuh"
 
 namespace {
 
@@ -190,6 +191,24 @@ la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float
                       S_out, z_out, C, eps);
 }
 
+la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                           float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    static OptIn flag;
+    auto kern = la::la_fwd_tc128_kernel;
+    const la_status st = prepare(kern, flag, la::FwdTc128Layout::BYTES);
+    if (st != LA_OK) return st;
+    CUtensorMap tq{}, tk{}, tv{}, to{};
+    if (C > 0) {
+        constexpr int R = la::FwdTc128Layout::BOX_ROWS;
+        if (!tmap_bf16(&tq, q, G, C, 128, R) || !tmap_bf16(&tk, k, G, C, 128, R) || !tmap_bf16(&tv, v, G, C, 128, R) ||
+            !tmap_bf16(&to, o, G, C, 128, R))
+            return LA_ERR_CUDA;
+    }
+    return launch_pdl(kern, G, la::FwdTc128Layout::THREADS, la::FwdTc128Layout::BYTES, stream, tq, tk, tv, to, S0,
+                      z0, S_out, z_out, C, eps);
+}
+
 la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
                         const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0, float* dz0,
                         int G, int C, float eps, cudaStream_t stream)
@@ -307,6 +326,7 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
     // bf16, head size 64: the tensor-core (tcgen05 / TMEM / TMA) kernel, 128-token score
     // tiles for either block size (the block size changes only the rounding)
     if (dtype == LA_BF16 && D == 64) return fwd_tc_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+    if (dtype == LA_BF16 && D == 128) return fwd_tc128_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
 
 #define LA_FWD_CASE(DT, P, DD, BB, NW, ST)                                                                  \
     if (dtype == DT && D == DD && block == BB)                                                             \
