@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -18,6 +19,7 @@
 #include "la_fwd_tc.cuh"
 #include "la_bwd_tc.cuh"
 #include "la_fwd_tc128.cuh"
+#include "la_bwd_tcm.cuh"
 
 namespace {
 
@@ -229,6 +231,44 @@ la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float
                       tds, S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
 }
 
+// Multi-tile tensor-core backward (bf16, head size 64 or 128, any C up to the stash bound).
+template <int D>
+int bwd_tcm_max_c()
+{
+    const int lim = smem_optin_limit(nullptr);
+    if (lim < 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    const size_t fixed = la::BwdTcmLayout<D>::FIXED;
+    return fixed >= (size_t)lim ? 0 : (int)(((size_t)lim - fixed) / 8 / 128 * 128);
+}
+
+template <int D>
+la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
+                         const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0,
+                         float* dz0, int G, int C, float eps, cudaStream_t stream)
+{
+    using L = la::BwdTcmLayout<D>;
+    static OptIn flag;
+    auto kern = la::la_bwd_tcm_kernel<D>;
+    // each CTA holds all 512 TMEM columns: ask for enough shared memory that a second CTA
+    // never lands on the same SM only to wait in tcgen05.alloc
+    const size_t smem = std::max(L::smem_bytes(C), (size_t)118 * 1024);
+    const la_status st = prepare(kern, flag, smem);
+    if (st != LA_OK) return st;
+    CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{};
+    if (C > 0) {
+        constexpr int R = L::BOX_ROWS;
+        if (!tmap_bf16(&tq, q, G, C, D, R) || !tmap_bf16(&tk, k, G, C, D, R) || !tmap_bf16(&tv, v, G, C, D, R) ||
+            !tmap_bf16(&tg, dO, G, C, D, R) || !tmap_bf16(&tdq, dq, G, C, D, R) || !tmap_bf16(&tdk, dk, G, C, D, R) ||
+            !tmap_bf16(&tdv, dv, G, C, D, R))
+            return LA_ERR_CUDA;
+    }
+    return launch_pdl(kern, G, L::THREADS, smem, stream, tq, tk, tv, tg, tdq, tdk, tdv, S0, z0, dS_out, dz_out, dS0,
+                      dz0, C, eps);
+}
+
 // ---------------------------------------------------------------- kernel table
 // (dtype, D, block) -> instantiation.  NW = warps per CTA, ST = pipeline stages.
 #define LA_FWD_TABLE(X)                  \
@@ -358,6 +398,12 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
     // bf16, head size 64, one 128-token tile: the tensor-core (tcgen05 / TMEM / TMA) kernel
     if (dtype == LA_BF16 && D == 64 && C <= la::BwdTcLayout::MAX_C)
         return bwd_tc_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
+    // bf16, longer chunks or head size 128: the multi-tile tensor-core kernel
+    if (dtype == LA_BF16 && (D == 64 || D == 128)) {
+        if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
+        return D == 64 ? bwd_tcm_launch<64>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s)
+                       : bwd_tcm_launch<128>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
+    }
     if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
 
 #define LA_BWD_CASE(DT, P, DD, BB, NW, ST, AL)                                                               \
@@ -452,6 +498,10 @@ extern "C" la_status la_chunked_step_host(const void* q, const void* k, const vo
 
 extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
 {
+    if (dtype == LA_BF16 && (block == 64 || block == 128)) {
+        if (D == 64) return bwd_tcm_max_c<64>();
+        if (D == 128) return bwd_tcm_max_c<128>();
+    }
     const int lim = smem_optin_limit(nullptr);
     if (lim < 0) {
         cudaGetLastError();  // leave no sticky "no device" error behind

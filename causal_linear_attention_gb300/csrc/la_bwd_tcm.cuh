@@ -1,0 +1,574 @@
+// la_bwd_tcm.cuh -- backward of chunked causal linear attention on the tensor cores
+// (tcgen05 + TMEM + TMA) for chunks of any length, bf16 inputs, fp32 state, head size
+// 64 or 128.  (Chunks of at most 128 tokens at head size 64 use la_bwd_tc.cuh.)
+//
+// "Fractus-1B training optimization -- 2026-08-22", section 1, "Bottleneck #1": the
+// derivative of a cumsum is a reverse cumsum.  The chunk is cut into 128-token tiles b;
+// S_b, z_b are the state before tile b (S_0 = S0), R_b the gradient reaching the state
+// after tile b (R_last = dS_out).  For rows i / keys j of tile b:
+//     A = masked Q K^T,  den_i = q_i . z_b + sum_j A_ij + eps,  dN = dO / den,
+//     U = dN S_b^T (U[i][p] = sum_c dN[i][c] S_b[p][c]),  dd_i = -(q_i . U_i + dN_i . (A V)_i) / den_i
+//     dA = masked (dN V^T + dd 1^T)
+//     dq = U + dA K + dd z_b^T                       (needs S_b: a sweep in token order)
+//     dk = dA^T Q + V R_b^T + 1 r_b^T,  dv = A^T dN + K R_b
+//     R_{b-1} = R_b + Q^T dN,  r_{b-1} = r_b + Q^T dd   (a sweep in reverse order)
+//     dS0 = R_{-1},  dz0 = r_{-1}
+// So the kernel makes two passes over the tiles of its group:
+//   pass 1 (b = 0, 1, ...):   M1  A = Q K^T
+//                             E1  mask, den, 1/den -> stash, dO -> dN
+//                             M2  P = dN V^T, U = dN S^T (dq accumulator), AV = A V | S += K^T V
+//                             E2  dd -> stash, dA -> shared memory (over A)
+//                             M3  dq += dA K
+//                             E3  dq + dd z -> staging -> TMA store, z += column sums of K,
+//                                 S -> bf16 operand for the next tile
+//   pass 2 (b = last, ..., 0): M1  A = Q K^T (again)
+//                             E1  mask, dN = dO * stash
+//                             M2  P = dN V^T, dv = A^T dN + K R
+//                             E2  dA = mask(P + stash dd) (over A), dv -> staging -> TMA store
+//                             M3  dk = dA^T Q + V R^T, R += Q^T dN
+//                             E3  dk + r -> staging -> TMA store, r += Q^T dd, R -> bf16
+//                                 operand (dS0, dz0 after tile 0)
+// den and dd of every token stay in shared memory between the passes (8 bytes a token,
+// which bounds the chunk length); pass 2 re-reads the tiles, mostly from L2.
+//
+// One CTA per group, warp-specialised: warps 0-3 own the 128 rows of a tile (thread t <->
+// TMEM lane t), warp 4 is the producer (TMA loads; one lane issues every tcgen05.mma).
+// The state S (pass 1) and R (pass 2) live in TMEM as D x D fp32 accumulators with rows p
+// in lanes (head size 64: the M=64 layout, rows in lanes 0-15 of each 32-lane quarter).
+//
+// Shared memory (128-byte swizzle; a 128-row tile of D bf16 columns is D/64 atoms of
+// 16 KB; the dynamic base must be 1024-aligned, which is checked):
+//   QT, KT, VT, GN   Q, K, V, dO -> dN (D*256 bytes each); QT stages dq (pass 1) and the
+//                    dS0 tile (after pass 2), KT stages dv, GN stages dk (pass 2)
+//   AD   32768       bf16 A -> dA [i][j] (two 64-key atoms)
+//   SR   D*D*2       bf16 S (pass 1) / R (pass 2) [p][c]
+//   ZIN, RZ, ZPART   z (pass 1), r (pass 2), per-warp column partial sums
+//   BARS
+//   STASH            float 1/den [C'] then float dd [C'] (C' = C rounded up to 128)
+#pragma once
+#include <cuda_bf16.h>
+
+#include "la_fwd_tc.cuh"
+#include "la_tc.cuh"
+
+namespace la {
+
+template <int D>
+struct BwdTcmLayout {
+    static constexpr uint32_t TILE = 128 * D * 2;
+    static constexpr uint32_t QT = 0;
+    static constexpr uint32_t KT = TILE;
+    static constexpr uint32_t VT = 2 * TILE;
+    static constexpr uint32_t GN = 3 * TILE;
+    static constexpr uint32_t AD = 4 * TILE;
+    static constexpr uint32_t SR = AD + 32768;
+    static constexpr uint32_t SR_ATOM = D * 128;  // one D-row x 64-column atom of SR
+    static constexpr uint32_t ZIN = SR + D * D * 2;
+    static constexpr uint32_t RZ = ZIN + D * 4;
+    static constexpr uint32_t ZPART = RZ + D * 4;
+    static constexpr uint32_t BARS = ZPART + 4 * D * 4;
+    static constexpr uint32_t STASH = BARS + 128;
+    static constexpr uint32_t FIXED = STASH;      // + 8 bytes per token of the padded chunk
+    static constexpr uint32_t TMEM_COLS = 512;
+    // TMEM columns; pass 2 reuses pass 1's
+    static constexpr uint32_t T_SC = 0;           // scores, then P = dN V^T (128)
+    static constexpr uint32_t T_DQ = 128;         // U -> dq (pass 1) / dv (pass 2)
+    static constexpr uint32_t T_DV = 128;
+    static constexpr uint32_t T_AV = 128 + D;     // A V (pass 1) / dk (pass 2)
+    static constexpr uint32_t T_DK = 128 + D;
+    static constexpr uint32_t T_ST = 128 + 2 * D; // S (pass 1) / R (pass 2): D x D, rows p
+    static constexpr int THREADS = 160;
+    static constexpr int BOX_ROWS = 128;
+    static constexpr uint32_t HALF_BYTES = 2 * TILE;  // Q + K, or dO + V, of a tile
+    static constexpr size_t smem_bytes(int C) { return FIXED + (size_t)8 * (((C + 127) / 128) * 128); }
+};
+
+// 16-byte chunk `chunk` (8 bf16) of row `row` in a tile made of 64-column atoms of
+// `atom` bytes each
+__device__ __forceinline__ uint32_t chunk_at(int row, int chunk, uint32_t atom)
+{
+    return (uint32_t)(chunk >> 3) * atom + sw_chunk(row, chunk & 7);
+}
+
+template <int D>
+__global__ void __launch_bounds__(160, 1)
+la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+                  const __grid_constant__ CUtensorMap tdv,
+                  const float* S0, const float* z0, const float* dS_out, const float* dz_out,
+                  float* dS0, float* dz0, int C, float eps)
+{
+    using L = BwdTcmLayout<D>;
+    using namespace tc;
+    constexpr int NA = D / 64;      // 64-column atoms per feature row
+    constexpr int KD = D / 16;      // K = 16 steps over a feature dimension
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {  // swizzled operand tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t sbase = smem_addr(sm);
+    const int nsb = (C + 127) / 128;
+    float* zin = reinterpret_cast<float*>(sm + L::ZIN);
+    float* rz = reinterpret_cast<float*>(sm + L::RZ);
+    float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    float* st_inv = reinterpret_cast<float*>(sm + L::STASH);
+    float* st_dd = st_inv + nsb * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* bar_qk = bars + 0;   // Q, K of the tile landed (TMA)
+    uint64_t* bar_vg = bars + 1;   // dO, V of the tile landed (TMA)
+    uint64_t* bar_m1 = bars + 2;   // scores (MMA)
+    uint64_t* bar_e1 = bars + 3;   // A and dN published (and, at a pass start, the S / R operand and TMEM)
+    uint64_t* bar_m2 = bars + 4;   // second round (pass 1: P, U, A V; pass 2: P, dv)
+    uint64_t* bar_m2b = bars + 5;  // pass 1: the state update
+    uint64_t* bar_e2 = bars + 6;   // dA published
+    uint64_t* bar_m3 = bars + 7;   // third round (pass 1: dq; pass 2: dk, R)
+    uint64_t* bar_e3 = bars + 8;   // the tile is done: its buffers may be reloaded
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 72);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t g = blockIdx.x;
+
+    if (tid == 0) {
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_vg, 1);
+        mbar_init(bar_m1, 1);
+        mbar_init(bar_e1, 128);
+        mbar_init(bar_m2, 1);
+        mbar_init(bar_m2b, 1);
+        mbar_init(bar_e2, 128);
+        mbar_init(bar_m3, 1);
+        mbar_init(bar_e3, 128);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();  // inputs may have been written by the previous kernel in the stream
+
+    if (nsb == 0) {  // empty chunk: the carry gradients pass straight through
+        if (warp < 4) {
+            for (int i = tid; i < D * D; i += 128)
+                if (dS0) dS0[g * D * D + i] = dS_out ? dS_out[g * D * D + i] : 0.f;
+            if (tid < D && dz0) dz0[g * D + tid] = dz_out ? dz_out[g * D + tid] : 0.f;
+        }
+    } else if (warp == 4) {
+        // =================================================== producer (one lane)
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            prefetch_tmap(&tg);
+            auto load = [&](int b) {
+                mbar_expect_tx(bar_qk, L::HALF_BYTES);
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+                    tma_load_3d(sm + L::QT + a * 16384, &tq, bar_qk, 64 * a, b * 128, (int)g);
+                    tma_load_3d(sm + L::KT + a * 16384, &tk, bar_qk, 64 * a, b * 128, (int)g);
+                }
+                mbar_expect_tx(bar_vg, L::HALF_BYTES);
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+                    tma_load_3d(sm + L::GN + a * 16384, &tg, bar_vg, 64 * a, b * 128, (int)g);
+                    tma_load_3d(sm + L::VT + a * 16384, &tv, bar_vg, 64 * a, b * 128, (int)g);
+                }
+            };
+            load(0);
+            pdl_launch_dependents();
+
+            // K-major operands: +32 B (2 units) per K = 16 step inside a 64-column atom, the
+            // next atom 1024 units on (16 KB: 128-row tiles, and the SR tile at D = 128).
+            // MN-major operands span their 64-wide atoms through LBO and advance 16 rows
+            // (2048 B = 128 units) per K = 16 step.
+            const uint64_t dQ = smem_desc(sbase + L::QT, 16, 1024), dQm = smem_desc(sbase + L::QT, 16384, 1024);
+            const uint64_t dK = smem_desc(sbase + L::KT, 16, 1024), dKm = smem_desc(sbase + L::KT, 16384, 1024);
+            const uint64_t dV = smem_desc(sbase + L::VT, 16, 1024), dVm = smem_desc(sbase + L::VT, 16384, 1024);
+            const uint64_t dG = smem_desc(sbase + L::GN, 16, 1024), dGm = smem_desc(sbase + L::GN, 16384, 1024);
+            const uint64_t dAk = smem_desc(sbase + L::AD, 16, 1024), dAm = smem_desc(sbase + L::AD, 16384, 1024);
+            const uint64_t dS = smem_desc(sbase + L::SR, 16, 1024), dRm = smem_desc(sbase + L::SR, L::SR_ATOM, 1024);
+            const uint32_t id_sq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
+            const uint32_t id_kk = idesc_bf16(128, D, false, false);    // N = D, both K-major
+            const uint32_t id_km = idesc_bf16(128, D, false, true);     // N = D, K-major A, MN-major B
+            const uint32_t id_mm = idesc_bf16(128, D, true, true);      // N = D, both MN-major
+            const uint32_t id_dd = idesc_bf16(D, D, true, true);        // D x D, both MN-major
+            auto kstep = [](uint64_t d, int kk) { return d + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2); };
+
+            bool ok = true;
+            for (int it = 0; it < 2 * nsb && ok; ++it) {
+                const bool p1 = it < nsb;
+                const uint32_t par = it & 1;
+                ok = mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < KD; ++kk)  // M1: A = Q K^T
+                    umma_bf16(tmem + L::T_SC, kstep(dQ, kk), kstep(dK, kk), id_sq, kk > 0);
+                umma_commit(bar_m1);
+                ok = mbar_wait(bar_e1, par, ERR_TIMEOUT_MMA) && mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < KD; ++kk)  // P = dN V^T  (V rows j as K-major B, K = c)
+                    umma_bf16(tmem + L::T_SC, kstep(dG, kk), kstep(dV, kk), id_sq, kk > 0);
+                if (p1) {
+#pragma unroll
+                    for (int kk = 0; kk < KD; ++kk)  // U = dN S^T  (S rows p as K-major B, K = c)
+                        umma_bf16(tmem + L::T_DQ, kstep(dG, kk), kstep(dS, kk), id_kk, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // AV = A V  (V read MN-major: N = c, K = j)
+                        umma_bf16(tmem + L::T_AV, kstep(dAk, kk), dVm + kk * 128, id_km, kk > 0);
+                    umma_commit(bar_m2);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // S += K^T V  (M = p, N = c, K = j)
+                        umma_bf16(tmem + L::T_ST, dKm + kk * 128, dVm + kk * 128, id_dd, true);
+                    umma_commit(bar_m2b);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dv = A^T dN  (M = j, K = i)
+                        umma_bf16(tmem + L::T_DV, dAm + kk * 128, dGm + kk * 128, id_mm, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < KD; ++kk)  // dv += K R  (R read MN-major: N = c, K = p)
+                        umma_bf16(tmem + L::T_DV, kstep(dK, kk), dRm + kk * 128, id_km, true);
+                    umma_commit(bar_m2);
+                }
+                ok = mbar_wait(bar_e2, par, ERR_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                if (p1) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dq += dA K  (K read MN-major: N = p, K = j)
+                        umma_bf16(tmem + L::T_DQ, kstep(dAk, kk), dKm + kk * 128, id_km, true);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dk = dA^T Q  (M = j, K = i)
+                        umma_bf16(tmem + L::T_DK, dAm + kk * 128, dQm + kk * 128, id_mm, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < KD; ++kk)  // dk += V R^T  (R rows p as K-major B, K = c)
+                        umma_bf16(tmem + L::T_DK, kstep(dV, kk), kstep(dS, kk), id_kk, true);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // R += Q^T dN  (M = p, N = c, K = i)
+                        umma_bf16(tmem + L::T_ST, dQm + kk * 128, dGm + kk * 128, id_dd, true);
+                }
+                umma_commit(bar_m3);
+                ok = mbar_wait(bar_e3, par, ERR_TIMEOUT_MMA);
+                if (ok && it + 1 < 2 * nsb) load(it + 1 < nsb ? it + 1 : 2 * nsb - 2 - it);
+            }
+        }
+    } else {
+        // =================================================== epilogue (warps 0-3)
+        const int t = tid;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        // rows of the D x D accumulators (S, R): lane = row at D = 128; at D = 64 the M=64
+        // layout puts row 16w + l in lane l < 16 of warp w
+        const bool srow = D == 128 || lane < 16;
+        const int prow = D == 128 ? t : 16 * warp + lane;
+        for (int it = 0; it < 2 * nsb; ++it) {
+            const bool p1 = it < nsb;
+            const int b = p1 ? it : 2 * nsb - 1 - it;
+            const uint32_t par = it & 1;
+            const int row0 = b * 128;
+            const bool row_ok = row0 + t < C;
+            if (it == 0 || it == nsb) {
+                // ---- a pass starts: S0 (pass 1) or dS_out (pass 2) -> the D x D TMEM accumulator
+                //      (fp32) and the bf16 operand SR; z0 -> z, or dz_out -> r
+                const float* src = it == 0 ? S0 : dS_out;
+                const float* srcv = it == 0 ? z0 : dz_out;
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    if (srow && src) {
+                        const float4* s4 = reinterpret_cast<const float4*>(src + g * D * D + (size_t)prow * D + 32 * h);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 f = s4[j];
+                            r[4 * j] = __float_as_uint(f.x);
+                            r[4 * j + 1] = __float_as_uint(f.y);
+                            r[4 * j + 2] = __float_as_uint(f.z);
+                            r[4 * j + 3] = __float_as_uint(f.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    tmem_st32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    if (srow)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                                pack8(r + 8 * q, 1.f);
+                }
+                if (t < D) (it == 0 ? zin : rz)[t] = srcv ? srcv[g * D + t] : 0.f;
+                epi_sync();  // z / r complete before any thread reads them
+            }
+            // ---- E1: masked scores -> bf16 A (AD); den (pass 1) or the stashed 1/den (pass 2)
+            mbar_wait(bar_m1, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            float rsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * half, r);
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
+                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
+                        rsum += x0 + x1;
+                        w[e] = pack_bf16(x0, x1);
+                    }
+                    *reinterpret_cast<uint4*>(sm + L::AD + half * 16384 + sw_chunk(t, chunk)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            float den = 1.f, inv;
+            if (p1) {
+                mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
+                float qz = 0.f;
+#pragma unroll
+                for (int cq = 0; cq < D / 8; ++cq) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + chunk_at(t, cq, 16384));
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h2[e]);
+                        qz = fmaf(f.x, zin[8 * cq + 2 * e], qz);
+                        qz = fmaf(f.y, zin[8 * cq + 2 * e + 1], qz);
+                    }
+                }
+                den = rsum + qz + eps;
+                inv = row_ok ? 1.f / den : 0.f;
+                st_inv[row0 + t] = inv;
+            } else {
+                inv = st_inv[row0 + t];
+            }
+            mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
+#pragma unroll
+            for (int chunk = 0; chunk < D / 8; ++chunk) {  // dO -> dN = dO / den in place
+                uint4* p4 = reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, chunk, 16384));
+                uint4 u = *p4;
+                __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    h2[e] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                }
+                *p4 = u;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_e1);
+
+            // ---- E2: dd (pass 1: -(dN . AV + q . U) / den; pass 2: stashed), dA -> AD (over A)
+            mbar_wait(bar_m2, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            float dd;
+            if (p1) {
+                float dot = 0.f;
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_AV + 32 * h, r);  // AV . dN
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(sm + L::GN + chunk_at(t, 4 * h + q, 16384));
+                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(h2[e]);
+                            dot = fmaf(f.x, __uint_as_float(r[8 * q + 2 * e]), dot);
+                            dot = fmaf(f.y, __uint_as_float(r[8 * q + 2 * e + 1]), dot);
+                        }
+                    }
+                    tmem_ld32(tmem + lane_base + L::T_DQ + 32 * h, r);  // U . q
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + chunk_at(t, 4 * h + q, 16384));
+                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(h2[e]);
+                            dot = fmaf(f.x, __uint_as_float(r[8 * q + 2 * e]), dot);
+                            dot = fmaf(f.y, __uint_as_float(r[8 * q + 2 * e + 1]), dot);
+                        }
+                    }
+                }
+                dd = row_ok ? -dot / den : 0.f;
+                st_dd[row0 + t] = dd;
+            } else {
+                dd = st_dd[row0 + t];
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // dA = masked (P + dd)
+                uint32_t r[64];
+                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * half, r);
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const float x0 = (row_ok && j <= t) ? __uint_as_float(r[8 * chunk + 2 * e]) + dd : 0.f;
+                        const float x1 = (row_ok && j + 1 <= t) ? __uint_as_float(r[8 * chunk + 2 * e + 1]) + dd : 0.f;
+                        w[e] = pack_bf16(x0, x1);
+                    }
+                    *reinterpret_cast<uint4*>(sm + L::AD + half * 16384 + sw_chunk(t, chunk)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_e2);
+            if (!p1) {  // dv -> staging in KT (its last reader, K R, is done) -> TMA store
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_DV + 32 * h, r);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(sm + L::KT + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                }
+                fence_async_smem();
+                epi_sync();
+                if (t == 0) {
+#pragma unroll
+                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdv, sm + L::KT + a * 16384, 64 * a, row0, (int)g);
+                    tma_store_commit();
+                }
+            }
+
+            // ---- E3
+            // per-warp sums over the tile's 128 rows of a bf16 tile's columns, optionally
+            // weighted per row: thread (cc, rg) sums D/8 rows x 8 columns, then the warp's rows
+            auto column_sums = [&](uint32_t tile, const float* wrow) {
+                constexpr int CH = D / 8;
+                const int cc = t % CH, rg = t / CH;
+                float s[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = 0.f;
+#pragma unroll 4
+                for (int rr = 0; rr < CH; ++rr) {
+                    const int row = rg * CH + rr;
+                    const float w = wrow ? wrow[row] : 1.f;
+                    const uint4 u = *reinterpret_cast<const uint4*>(sm + tile + chunk_at(row, cc, 16384));
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h2[e]);
+                        s[2 * e] = fmaf(w, f.x, s[2 * e]);
+                        s[2 * e + 1] = fmaf(w, f.y, s[2 * e + 1]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (CH == 8) s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
+                    s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
+                }
+                if (lane < CH)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) zpart[warp * D + 8 * cc + e] = s[e];
+            };
+            mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            if (p1) {
+                // dq = U + dA K + dd z -> staging in QT (Q's last readers, M1 and q . U, are done)
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_DQ + 32 * h, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + dd * zin[32 * h + j]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(sm + L::QT + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                }
+                column_sums(L::KT, nullptr);  // z after the tile = z + sum_j k_j
+                // S after the tile -> bf16 operand for the next tile (the state update is its own group)
+                mbar_wait(bar_m2b, par, ERR_TIMEOUT_MMA);
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    if (srow)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                                pack8(r + 8 * q, 1.f);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                epi_sync();  // dq staging and column partials complete; every dq has read z
+                if (t == 0) {
+#pragma unroll
+                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdq, sm + L::QT + a * 16384, 64 * a, row0, (int)g);
+                    tma_store_commit();
+                }
+                if (t < D) zin[t] += zpart[t] + zpart[D + t] + zpart[2 * D + t] + zpart[3 * D + t];
+            } else {
+                // dk = dA^T Q + V R^T + r -> staging in GN (dN's last reader, R += Q^T dN, is done)
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_DK + 32 * h, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + rz[32 * h + j]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                }
+                column_sums(L::QT, st_dd + row0);  // r before the tile = r + sum_i dd_i q_i
+                // R before the tile -> bf16 operand for the next (earlier) tile; after tile 0: dS0
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    if (srow) {
+                        if (b > 0) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                                    pack8(r + 8 * q, 1.f);
+                        } else if (dS0) {
+                            float4* dst = reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)prow * D + 32 * h);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        }
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                epi_sync();  // dk staging and column partials complete; every dk has read r
+                if (t == 0) {
+#pragma unroll
+                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdk, sm + L::GN + a * 16384, 64 * a, row0, (int)g);
+                    tma_store_commit();
+                }
+                if (t < D) {
+                    rz[t] += zpart[t] + zpart[D + t] + zpart[2 * D + t] + zpart[3 * D + t];
+                    if (b == 0 && dz0) dz0[g * D + t] = rz[t];
+                }
+            }
+            epi_sync();                         // z / r updated before the next tile reads them
+            if (t == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
+            mbar_arrive(bar_e3);
+        }
+    }
+    if (tid == 0) tma_store_wait_read();  // shared memory stays valid until the stores have read it
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+}  // namespace la
