@@ -23,7 +23,6 @@
 
 namespace {
 
-using la::Bf16Mma;
 using la::F32Simt;
 
 constexpr int kMaxDevices = 64;
@@ -272,19 +271,11 @@ la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const floa
 // ---------------------------------------------------------------- kernel table
 // (dtype, D, block) -> instantiation.  NW = warps per CTA, ST = pipeline stages.
 #define LA_FWD_TABLE(X)                  \
-    X(LA_BF16, Bf16Mma, 64, 64, 8, 2)    \
-    X(LA_BF16, Bf16Mma, 128, 64, 8, 2)   \
-    X(LA_BF16, Bf16Mma, 64, 128, 8, 2)   \
-    X(LA_BF16, Bf16Mma, 128, 128, 16, 1) \
     X(LA_F32, F32Simt, 64, 64, 8, 2)     \
     X(LA_F32, F32Simt, 128, 64, 8, 1)    \
     X(LA_F32, F32Simt, 64, 128, 8, 1)
 
 #define LA_BWD_TABLE(X)                         \
-    X(LA_BF16, Bf16Mma, 64, 64, 8, 2, false)    \
-    X(LA_BF16, Bf16Mma, 128, 64, 16, 1, false)  \
-    X(LA_BF16, Bf16Mma, 64, 128, 16, 1, false)  \
-    X(LA_BF16, Bf16Mma, 128, 128, 16, 1, true)  \
     X(LA_F32, F32Simt, 64, 64, 8, 1, false)
 
 // ---------------------------------------------------------------- argument checks

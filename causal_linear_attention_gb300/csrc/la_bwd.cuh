@@ -18,7 +18,7 @@
 //   then R += Q_b^T dN_b, r += Q_b^T dd_b.   Finally dS0 = R, dz0 = r.
 // The reverse sweep computes the transposed score tiles directly
 // (A^T = K Q^T and P^T / den = V dN^T), so every product reads its operands from
-// shared memory in a layout ldmatrix (or the SIMT loop) handles.
+// shared memory in a layout the SIMT loop walks conflict-free.
 // The same registers hold S_run in the forward sweep and R in the reverse sweep.
 // With ALIAS, the A^T and dA^T tiles share one buffer and are produced and used
 // one after the other (for shapes whose shared memory is otherwise too small).
