@@ -230,19 +230,7 @@ la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float
                       tds, S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
 }
 
-// Multi-tile tensor-core backward (bf16, head size 64 or 128, any C up to the stash bound).
-template <int D>
-int bwd_tcm_max_c()
-{
-    const int lim = smem_optin_limit(nullptr);
-    if (lim < 0) {
-        cudaGetLastError();
-        return 0;
-    }
-    const size_t fixed = la::BwdTcmLayout<D>::FIXED;
-    return fixed >= (size_t)lim ? 0 : (int)(((size_t)lim - fixed) / 8 / 128 * 128);
-}
-
+// Multi-tile tensor-core backward (bf16, head size 64 or 128, any C).
 template <int D>
 la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
                          const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0,
@@ -253,7 +241,7 @@ la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const floa
     auto kern = la::la_bwd_tcm_kernel<D>;
     // each CTA holds all 512 TMEM columns: ask for enough shared memory that a second CTA
     // never lands on the same SM only to wait in tcgen05.alloc
-    const size_t smem = std::max(L::smem_bytes(C), (size_t)118 * 1024);
+    const size_t smem = std::max((size_t)L::BYTES, (size_t)118 * 1024);
     const la_status st = prepare(kern, flag, smem);
     if (st != LA_OK) return st;
     CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{};
@@ -265,7 +253,7 @@ la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const floa
             return LA_ERR_CUDA;
     }
     return launch_pdl(kern, G, L::THREADS, smem, stream, tq, tk, tv, tg, tdq, tdk, tdv, S0, z0, dS_out, dz_out, dS0,
-                      dz0, C, eps);
+                      dz0, static_cast<__nv_bfloat16*>(dk), C, eps);
 }
 
 // ---------------------------------------------------------------- kernel table
@@ -489,10 +477,8 @@ extern "C" la_status la_chunked_step_host(const void* q, const void* k, const vo
 
 extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
 {
-    if (dtype == LA_BF16 && (block == 64 || block == 128)) {
-        if (D == 64) return bwd_tcm_max_c<64>();
-        if (D == 128) return bwd_tcm_max_c<128>();
-    }
+    // bf16: the tensor-core kernels keep nothing per token on chip
+    if (dtype == LA_BF16 && (block == 64 || block == 128) && (D == 64 || D == 128)) return 1 << 30;
     const int lim = smem_optin_limit(nullptr);
     if (lim < 0) {
         cudaGetLastError();  // leave no sticky "no device" error behind

@@ -28,8 +28,9 @@
 //                             M3  dk = dA^T Q + V R^T, R += Q^T dN
 //                             E3  dk + r -> staging -> TMA store, r += Q^T dd, R -> bf16
 //                                 operand (dS0, dz0 after tile 0)
-// den and dd of every token stay in shared memory between the passes (8 bytes a token,
-// which bounds the chunk length); pass 2 re-reads the tiles, mostly from L2.
+// 1/den and dd of every token wait between the passes in the first 8 bytes of the token's
+// dk row (dk is only written in pass 2, after they have been read back), so the chunk
+// length is not bounded by on-chip memory; pass 2 re-reads the tiles, mostly from L2.
 //
 // One CTA per group, warp-specialised: warps 0-3 own the 128 rows of a tile (thread t <->
 // TMEM lane t), warp 4 is the producer (TMA loads; one lane issues every tcgen05.mma).
@@ -43,8 +44,7 @@
 //   AD   32768       bf16 A -> dA [i][j] (two 64-key atoms)
 //   SR   D*D*2       bf16 S (pass 1) / R (pass 2) [p][c]
 //   ZIN, RZ, ZPART   z (pass 1), r (pass 2), per-warp column partial sums
-//   BARS
-//   STASH            float 1/den [C'] then float dd [C'] (C' = C rounded up to 128)
+//   BARS, DDT        mbarriers; dd of the tile's rows
 #pragma once
 #include <cuda_bf16.h>
 
@@ -67,8 +67,8 @@ struct BwdTcmLayout {
     static constexpr uint32_t RZ = ZIN + D * 4;
     static constexpr uint32_t ZPART = RZ + D * 4;
     static constexpr uint32_t BARS = ZPART + 4 * D * 4;
-    static constexpr uint32_t STASH = BARS + 128;
-    static constexpr uint32_t FIXED = STASH;      // + 8 bytes per token of the padded chunk
+    static constexpr uint32_t DDT = BARS + 128;   // float[128]
+    static constexpr uint32_t BYTES = DDT + 512;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns; pass 2 reuses pass 1's
     static constexpr uint32_t T_SC = 0;           // scores, then P = dN V^T (128)
@@ -80,7 +80,6 @@ struct BwdTcmLayout {
     static constexpr int THREADS = 160;
     static constexpr int BOX_ROWS = 128;
     static constexpr uint32_t HALF_BYTES = 2 * TILE;  // Q + K, or dO + V, of a tile
-    static constexpr size_t smem_bytes(int C) { return FIXED + (size_t)8 * (((C + 127) / 128) * 128); }
 };
 
 // 16-byte chunk `chunk` (8 bf16) of row `row` in a tile made of 64-column atoms of
@@ -97,7 +96,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
                   const __grid_constant__ CUtensorMap tdv,
                   const float* S0, const float* z0, const float* dS_out, const float* dz_out,
-                  float* dS0, float* dz0, int C, float eps)
+                  float* dS0, float* dz0, __nv_bfloat16* dk, int C, float eps)
 {
     using L = BwdTcmLayout<D>;
     using namespace tc;
@@ -113,8 +112,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     float* zin = reinterpret_cast<float*>(sm + L::ZIN);
     float* rz = reinterpret_cast<float*>(sm + L::RZ);
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
-    float* st_inv = reinterpret_cast<float*>(sm + L::STASH);
-    float* st_dd = st_inv + nsb * 128;
+    float* ddt = reinterpret_cast<float*>(sm + L::DDT);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* bar_qk = bars + 0;   // Q, K of the tile landed (TMA)
     uint64_t* bar_vg = bars + 1;   // dO, V of the tile landed (TMA)
@@ -307,7 +305,11 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (t < D) (it == 0 ? zin : rz)[t] = srcv ? srcv[g * D + t] : 0.f;
                 epi_sync();  // z / r complete before any thread reads them
             }
-            // ---- E1: masked scores -> bf16 A (AD); den (pass 1) or the stashed 1/den (pass 2)
+            // the row's (1/den, dd), parked in its dk row between the passes
+            float2* stash = reinterpret_cast<float2*>(dk + ((size_t)g * C + row0 + t) * D);
+            float2 parked = make_float2(0.f, 0.f);
+            if (!p1 && row_ok) parked = *stash;
+            // ---- E1: masked scores -> bf16 A (AD); den (pass 1) or the parked 1/den (pass 2)
             mbar_wait(bar_m1, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             float rsum = 0.f;
@@ -347,9 +349,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 den = rsum + qz + eps;
                 inv = row_ok ? 1.f / den : 0.f;
-                st_inv[row0 + t] = inv;
             } else {
-                inv = st_inv[row0 + t];
+                inv = parked.x;
             }
             mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
 #pragma unroll
@@ -403,10 +404,11 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
                 }
                 dd = row_ok ? -dot / den : 0.f;
-                st_dd[row0 + t] = dd;
+                if (row_ok) *stash = make_float2(inv, dd);
             } else {
-                dd = st_dd[row0 + t];
+                dd = parked.y;
             }
+            ddt[t] = dd;  // for the weighted column sums of pass 2 (read after the next barrier)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {  // dA = masked (P + dd)
                 uint32_t r[64];
@@ -526,7 +528,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     for (int q = 0; q < 4; ++q)
                         *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
                 }
-                column_sums(L::QT, st_dd + row0);  // r before the tile = r + sum_i dd_i q_i
+                column_sums(L::QT, ddt);  // r before the tile = r + sum_i dd_i q_i
                 // R before the tile -> bf16 operand for the next (earlier) tile; after tile 0: dS0
 #pragma unroll
                 for (int h = 0; h < D / 32; ++h) {
@@ -548,6 +550,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
                 }
                 fence_async_smem();
+                fence_async_global();  // the parked values were read before the dk store overwrites them
                 tc_fence_before();
                 epi_sync();  // dk staging and column partials complete; every dk has read r
                 if (t == 0) {

@@ -41,9 +41,10 @@
  * bfloat16 tensor-core products with float32 accumulation and a float32
  * state.  LA_F32 supports (D, block) = (64, 64), (128, 64), (64, 128) in the
  * forward and (64, 64) in the backward; other combinations return
- * LA_ERR_UNSUPPORTED.  The backward keeps two floats per token of the chunk in
- * shared memory, so its C is bounded: la_bwd_max_c() gives the bound (several
- * thousand tokens for D = 64).
+ * LA_ERR_UNSUPPORTED.  The float32 backward keeps two floats per token of the
+ * chunk in shared memory, so its C is bounded: la_bwd_max_c() gives the bound
+ * (several thousand tokens); the bfloat16 backward parks those two floats in the
+ * dk output between its passes and accepts any C.
  */
 #ifndef LA_H
 #define LA_H
@@ -104,8 +105,9 @@ la_status la_chunked_bwd(const void* q, const void* k, const void* v,
                          int G, int C, int D, int block, la_dtype dtype, float eps,
                          void* stream);
 
-/* Largest C la_chunked_bwd accepts for this shape on the current device; 0 if
- * the shape or dtype is unsupported or no device is available. */
+/* Largest C la_chunked_bwd accepts for this shape on the current device (2^30
+ * for bfloat16); 0 if the shape or dtype is unsupported, or, for float32, when no
+ * device is available. */
 int la_bwd_max_c(int D, int block, la_dtype dtype);
 
 /* Synchronises the current device, then reports whether any kernel of this library

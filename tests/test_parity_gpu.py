@@ -219,3 +219,11 @@ def test_backward_without_carry_gradient_outputs(C):
     assert got[3] is None and got[4] is None
     ref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
     check(got[:3], ref[:3], "bf16", BWD_NAMES[:3])
+
+
+@pytest.mark.parametrize("G,C,D", [(2, 5000, 128), (2, 17000, 64)])
+def test_long_chunk_backward(G, C, D):
+    """bf16 backward of chunks longer than any on-chip per-token buffer would allow
+    (the kernel parks 1/den and dd in the dk rows between its passes)."""
+    assert la.la_bwd_max_c(D, 64, la.LA_BF16) >= C
+    bwd_case(G, C, D, 64, "bf16", seed=C)
