@@ -32,8 +32,10 @@
 // dk row (dk is only written in pass 2, after they have been read back), so the chunk
 // length is not bounded by on-chip memory; pass 2 re-reads the tiles, mostly from L2.
 //
-// One CTA per group, warp-specialised: warps 0-3 own the 128 rows of a tile (thread t <->
-// TMEM lane t), warp 4 is the producer (TMA loads; one lane issues every tcgen05.mma).
+// One CTA per group, warp-specialised: warps 0-7 own the 128 rows of a tile, two warps per
+// 32-lane TMEM quarter splitting the columns (warp w: lanes 32 (w % 4) .., column half
+// w / 4; a row's two partial sums meet in shared memory); warp 8 is the producer (TMA
+// loads; one lane issues every tcgen05.mma).
 // The state S (pass 1) and R (pass 2) live in TMEM as D x D fp32 accumulators with rows p
 // in lanes (head size 64: the M=64 layout, rows in lanes 0-15 of each 32-lane quarter).
 //
@@ -65,9 +67,10 @@ struct BwdTcmLayout {
     static constexpr uint32_t SR_ATOM = D * 128;  // one D-row x 64-column atom of SR
     static constexpr uint32_t ZIN = SR + D * D * 2;
     static constexpr uint32_t RZ = ZIN + D * 4;
-    static constexpr uint32_t ZPART = RZ + D * 4;
-    static constexpr uint32_t BARS = ZPART + 4 * D * 4;
-    static constexpr uint32_t DDT = BARS + 128;   // float[128]
+    static constexpr uint32_t ZPART = RZ + D * 4;          // float[8][D]: per-warp column sums
+    static constexpr uint32_t XCH = ZPART + 8 * D * 4;     // float[2][2][128]: the two halves of a row
+    static constexpr uint32_t BARS = XCH + 2048;
+    static constexpr uint32_t DDT = BARS + 128;            // float[128]: dd of the tile's rows
     static constexpr uint32_t BYTES = DDT + 512;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns; pass 2 reuses pass 1's
@@ -77,10 +80,13 @@ struct BwdTcmLayout {
     static constexpr uint32_t T_AV = 128 + D;     // A V (pass 1) / dk (pass 2)
     static constexpr uint32_t T_DK = 128 + D;
     static constexpr uint32_t T_ST = 128 + 2 * D; // S (pass 1) / R (pass 2): D x D, rows p
-    static constexpr int THREADS = 160;
+    static constexpr int THREADS = 288;           // 8 epilogue warps + the producer
     static constexpr int BOX_ROWS = 128;
     static constexpr uint32_t HALF_BYTES = 2 * TILE;  // Q + K, or dO + V, of a tile
 };
+
+// Named barrier over the 256 epilogue threads (warps 0-7).
+__device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // 16-byte chunk `chunk` (8 bf16) of row `row` in a tile made of 64-column atoms of
 // `atom` bytes each
@@ -90,7 +96,7 @@ __device__ __forceinline__ uint32_t chunk_at(int row, int chunk, uint32_t atom)
 }
 
 template <int D>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(288, 1)
 la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
@@ -112,6 +118,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     float* zin = reinterpret_cast<float*>(sm + L::ZIN);
     float* rz = reinterpret_cast<float*>(sm + L::RZ);
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    float* xch = reinterpret_cast<float*>(sm + L::XCH);
     float* ddt = reinterpret_cast<float*>(sm + L::DDT);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* bar_qk = bars + 0;   // Q, K of the tile landed (TMA)
@@ -132,12 +139,12 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         mbar_init(bar_qk, 1);
         mbar_init(bar_vg, 1);
         mbar_init(bar_m1, 1);
-        mbar_init(bar_e1, 128);
+        mbar_init(bar_e1, 256);
         mbar_init(bar_m2, 1);
         mbar_init(bar_m2b, 1);
-        mbar_init(bar_e2, 128);
+        mbar_init(bar_e2, 256);
         mbar_init(bar_m3, 1);
-        mbar_init(bar_e3, 128);
+        mbar_init(bar_e3, 256);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -152,12 +159,12 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
     if (nsb == 0) {  // empty chunk: the carry gradients pass straight through
-        if (warp < 4) {
-            for (int i = tid; i < D * D; i += 128)
+        if (warp < 8) {
+            for (int i = tid; i < D * D; i += 256)
                 if (dS0) dS0[g * D * D + i] = dS_out ? dS_out[g * D * D + i] : 0.f;
             if (tid < D && dz0) dz0[g * D + tid] = dz_out ? dz_out[g * D + tid] : 0.f;
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // =================================================== producer (one lane)
         if (lane == 0) {
             prefetch_tmap(&tq);
@@ -185,12 +192,6 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // next atom 1024 units on (16 KB: 128-row tiles, and the SR tile at D = 128).
             // MN-major operands span their 64-wide atoms through LBO and advance 16 rows
             // (2048 B = 128 units) per K = 16 step.
-            const uint64_t dQ = smem_desc(sbase + L::QT, 16, 1024), dQm = smem_desc(sbase + L::QT, 16384, 1024);
-            const uint64_t dK = smem_desc(sbase + L::KT, 16, 1024), dKm = smem_desc(sbase + L::KT, 16384, 1024);
-            const uint64_t dV = smem_desc(sbase + L::VT, 16, 1024), dVm = smem_desc(sbase + L::VT, 16384, 1024);
-            const uint64_t dG = smem_desc(sbase + L::GN, 16, 1024), dGm = smem_desc(sbase + L::GN, 16384, 1024);
-            const uint64_t dAk = smem_desc(sbase + L::AD, 16, 1024), dAm = smem_desc(sbase + L::AD, 16384, 1024);
-            const uint64_t dS = smem_desc(sbase + L::SR, 16, 1024), dRm = smem_desc(sbase + L::SR, L::SR_ATOM, 1024);
             const uint32_t id_sq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
             const uint32_t id_kk = idesc_bf16(128, D, false, false);    // N = D, both K-major
             const uint32_t id_km = idesc_bf16(128, D, false, true);     // N = D, K-major A, MN-major B
@@ -202,6 +203,16 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             for (int it = 0; it < 2 * nsb && ok; ++it) {
                 const bool p1 = it < nsb;
                 const uint32_t par = it & 1;
+                // descriptors derived per tile from an opaque copy of the base address, so the
+                // compiler cannot hoist every unrolled instruction's operands out of the loop
+                uint32_t b0 = sbase;
+                asm volatile("" : "+r"(b0));
+                const uint64_t dQ = smem_desc(b0 + L::QT, 16, 1024), dQm = smem_desc(b0 + L::QT, 16384, 1024);
+                const uint64_t dK = smem_desc(b0 + L::KT, 16, 1024), dKm = smem_desc(b0 + L::KT, 16384, 1024);
+                const uint64_t dV = smem_desc(b0 + L::VT, 16, 1024), dVm = smem_desc(b0 + L::VT, 16384, 1024);
+                const uint64_t dG = smem_desc(b0 + L::GN, 16, 1024), dGm = smem_desc(b0 + L::GN, 16384, 1024);
+                const uint64_t dAk = smem_desc(b0 + L::AD, 16, 1024), dAm = smem_desc(b0 + L::AD, 16384, 1024);
+                const uint64_t dS = smem_desc(b0 + L::SR, 16, 1024), dRm = smem_desc(b0 + L::SR, L::SR_ATOM, 1024);
                 ok = mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
                 if (!ok) break;
                 tc_fence_after();
@@ -260,13 +271,16 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
         }
     } else {
-        // =================================================== epilogue (warps 0-3)
-        const int t = tid;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        // =================================================== epilogue (warps 0-7)
+        constexpr int HC = D / 2;    // columns of a D-wide accumulator row per half
+        constexpr int HCH = D / 16;  // 16-byte bf16 chunks of a D-wide row per half
+        const int q4 = warp & 3, hh = warp >> 2;
+        const int t = 32 * q4 + lane;  // the tile row (TMEM lane) this thread shares with its pair
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         // rows of the D x D accumulators (S, R): lane = row at D = 128; at D = 64 the M=64
-        // layout puts row 16w + l in lane l < 16 of warp w
+        // layout puts row 16 q + l in lane l < 16 of quarter q
         const bool srow = D == 128 || lane < 16;
-        const int prow = D == 128 ? t : 16 * warp + lane;
+        const int prow = D == 128 ? t : 16 * q4 + lane;
         for (int it = 0; it < 2 * nsb; ++it) {
             const bool p1 = it < nsb;
             const int b = p1 ? it : 2 * nsb - 1 - it;
@@ -275,14 +289,16 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const bool row_ok = row0 + t < C;
             if (it == 0 || it == nsb) {
                 // ---- a pass starts: S0 (pass 1) or dS_out (pass 2) -> the D x D TMEM accumulator
-                //      (fp32) and the bf16 operand SR; z0 -> z, or dz_out -> r
+                //      (fp32) and the bf16 operand SR, this thread's half of row prow; z0 -> z, or
+                //      dz_out -> r.  Every load is issued before the first use.
                 const float* src = it == 0 ? S0 : dS_out;
                 const float* srcv = it == 0 ? z0 : dz_out;
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {  // 32 columns at a time, all loads first
                     uint32_t r[32];
                     if (srow && src) {
-                        const float4* s4 = reinterpret_cast<const float4*>(src + g * D * D + (size_t)prow * D + 32 * h);
+                        const float4* s4 =
+                            reinterpret_cast<const float4*>(src + g * D * D + (size_t)prow * D + hh * HC + 32 * h2);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 f = s4[j];
@@ -295,40 +311,40 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = 0u;
                     }
-                    tmem_st32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    tmem_st32(tmem + lane_base + L::T_ST + hh * HC + 32 * h2, r);
                     if (srow)
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, hh * HCH + 4 * h2 + q, L::SR_ATOM)) =
                                 pack8(r + 8 * q, 1.f);
                 }
-                if (t < D) (it == 0 ? zin : rz)[t] = srcv ? srcv[g * D + t] : 0.f;
-                epi_sync();  // z / r complete before any thread reads them
+                if (tid < D) (it == 0 ? zin : rz)[tid] = srcv ? srcv[g * D + tid] : 0.f;
+                epi_sync256();  // z / r complete before any thread reads them
             }
             // the row's (1/den, dd), parked in its dk row between the passes
             float2* stash = reinterpret_cast<float2*>(dk + ((size_t)g * C + row0 + t) * D);
             float2 parked = make_float2(0.f, 0.f);
             if (!p1 && row_ok) parked = *stash;
-            // ---- E1: masked scores -> bf16 A (AD); den (pass 1) or the parked 1/den (pass 2)
+            // ---- E1: this half's masked scores -> bf16 A (AD atom hh); den (pass 1) or the
+            //      parked 1/den (pass 2); this half of dO -> dN
             mbar_wait(bar_m1, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             float rsum = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            {
                 uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * half, r);
+                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * hh, r);
 #pragma unroll
                 for (int chunk = 0; chunk < 8; ++chunk) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const int j = 64 * hh + 8 * chunk + 2 * e;
                         const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
                         const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
                         rsum += x0 + x1;
                         w[e] = pack_bf16(x0, x1);
                     }
-                    *reinterpret_cast<uint4*>(sm + L::AD + half * 16384 + sw_chunk(t, chunk)) =
+                    *reinterpret_cast<uint4*>(sm + L::AD + hh * 16384 + sw_chunk(t, chunk)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
@@ -337,7 +353,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
                 float qz = 0.f;
 #pragma unroll
-                for (int cq = 0; cq < D / 8; ++cq) {
+                for (int c8 = 0; c8 < HCH; ++c8) {
+                    const int cq = hh * HCH + c8;
                     const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + chunk_at(t, cq, 16384));
                     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -347,15 +364,17 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         qz = fmaf(f.y, zin[8 * cq + 2 * e + 1], qz);
                     }
                 }
-                den = rsum + qz + eps;
+                xch[hh * 128 + t] = rsum + qz;
+                epi_sync256();
+                den = xch[t] + xch[128 + t] + eps;
                 inv = row_ok ? 1.f / den : 0.f;
             } else {
                 inv = parked.x;
             }
             mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
 #pragma unroll
-            for (int chunk = 0; chunk < D / 8; ++chunk) {  // dO -> dN = dO / den in place
-                uint4* p4 = reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, chunk, 16384));
+            for (int c8 = 0; c8 < HCH; ++c8) {  // dO -> dN = dO / den in place
+                uint4* p4 = reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, hh * HCH + c8, 16384));
                 uint4 u = *p4;
                 __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
@@ -369,61 +388,65 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_before();
             mbar_arrive(bar_e1);
 
-            // ---- E2: dd (pass 1: -(dN . AV + q . U) / den; pass 2: stashed), dA -> AD (over A)
+            // ---- E2: dd (pass 1: -(dN . AV + q . U) / den; pass 2: parked), this half of
+            //      dA -> AD atom hh (over A)
             mbar_wait(bar_m2, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             float dd;
             if (p1) {
                 float dot = 0.f;
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_AV + 32 * h, r);  // AV . dN
+                    tmem_ld32(tmem + lane_base + L::T_AV + hh * HC + 32 * h2, r);  // AV . dN
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(sm + L::GN + chunk_at(t, 4 * h + q, 16384));
-                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+                        const uint4 u =
+                            *reinterpret_cast<const uint4*>(sm + L::GN + chunk_at(t, hh * HCH + 4 * h2 + q, 16384));
+                        const __nv_bfloat162* h2v = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(h2[e]);
+                            const float2 f = __bfloat1622float2(h2v[e]);
                             dot = fmaf(f.x, __uint_as_float(r[8 * q + 2 * e]), dot);
                             dot = fmaf(f.y, __uint_as_float(r[8 * q + 2 * e + 1]), dot);
                         }
                     }
-                    tmem_ld32(tmem + lane_base + L::T_DQ + 32 * h, r);  // U . q
+                    tmem_ld32(tmem + lane_base + L::T_DQ + hh * HC + 32 * h2, r);  // U . q
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(sm + L::QT + chunk_at(t, 4 * h + q, 16384));
-                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+                        const uint4 u =
+                            *reinterpret_cast<const uint4*>(sm + L::QT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384));
+                        const __nv_bfloat162* h2v = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(h2[e]);
+                            const float2 f = __bfloat1622float2(h2v[e]);
                             dot = fmaf(f.x, __uint_as_float(r[8 * q + 2 * e]), dot);
                             dot = fmaf(f.y, __uint_as_float(r[8 * q + 2 * e + 1]), dot);
                         }
                     }
                 }
-                dd = row_ok ? -dot / den : 0.f;
-                if (row_ok) *stash = make_float2(inv, dd);
+                xch[256 + hh * 128 + t] = dot;
+                epi_sync256();
+                dd = row_ok ? -(xch[256 + t] + xch[384 + t]) / den : 0.f;
+                if (hh == 0 && row_ok) *stash = make_float2(inv, dd);
             } else {
                 dd = parked.y;
             }
-            ddt[t] = dd;  // for the weighted column sums of pass 2 (read after the next barrier)
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {  // dA = masked (P + dd)
+            if (hh == 0) ddt[t] = dd;  // for the weighted column sums of pass 2 (read after a barrier)
+            {
                 uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * half, r);
+                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * hh, r);
 #pragma unroll
                 for (int chunk = 0; chunk < 8; ++chunk) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * half + 8 * chunk + 2 * e;
+                        const int j = 64 * hh + 8 * chunk + 2 * e;
                         const float x0 = (row_ok && j <= t) ? __uint_as_float(r[8 * chunk + 2 * e]) + dd : 0.f;
                         const float x1 = (row_ok && j + 1 <= t) ? __uint_as_float(r[8 * chunk + 2 * e + 1]) + dd : 0.f;
                         w[e] = pack_bf16(x0, x1);
                     }
-                    *reinterpret_cast<uint4*>(sm + L::AD + half * 16384 + sw_chunk(t, chunk)) =
+                    *reinterpret_cast<uint4*>(sm + L::AD + hh * 16384 + sw_chunk(t, chunk)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
@@ -432,16 +455,17 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_arrive(bar_e2);
             if (!p1) {  // dv -> staging in KT (its last reader, K R, is done) -> TMA store
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_DV + 32 * h, r);
+                    tmem_ld32(tmem + lane_base + L::T_DV + hh * HC + 32 * h2, r);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(sm + L::KT + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                        *reinterpret_cast<uint4*>(sm + L::KT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
+                            pack8(r + 8 * q, 1.f);
                 }
                 fence_async_smem();
-                epi_sync();
-                if (t == 0) {
+                epi_sync256();
+                if (tid == 0) {
 #pragma unroll
                     for (int a = 0; a < NA; ++a) tma_store_3d(&tdv, sm + L::KT + a * 16384, 64 * a, row0, (int)g);
                     tma_store_commit();
@@ -450,16 +474,16 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
             // ---- E3
             // per-warp sums over the tile's 128 rows of a bf16 tile's columns, optionally
-            // weighted per row: thread (cc, rg) sums D/8 rows x 8 columns, then the warp's rows
+            // weighted per row: thread (cc, rg) sums D/16 rows x 8 columns, then the warp's rows
             auto column_sums = [&](uint32_t tile, const float* wrow) {
-                constexpr int CH = D / 8;
-                const int cc = t % CH, rg = t / CH;
+                constexpr int CH = D / 8, RPG = CH / 2;
+                const int cc = tid % CH, rg = tid / CH;
                 float s[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) s[e] = 0.f;
-#pragma unroll 4
-                for (int rr = 0; rr < CH; ++rr) {
-                    const int row = rg * CH + rr;
+#pragma unroll
+                for (int rr = 0; rr < RPG; ++rr) {
+                    const int row = rg * RPG + rr;
                     const float w = wrow ? wrow[row] : 1.f;
                     const uint4 u = *reinterpret_cast<const uint4*>(sm + tile + chunk_at(row, cc, 16384));
                     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -479,69 +503,81 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 8; ++e) zpart[warp * D + 8 * cc + e] = s[e];
             };
+            auto warp_total = [&](int c) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) v += zpart[w * D + c];
+                return v;
+            };
             mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             if (p1) {
                 // dq = U + dA K + dd z -> staging in QT (Q's last readers, M1 and q . U, are done)
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_DQ + 32 * h, r);
+                    tmem_ld32(tmem + lane_base + L::T_DQ + hh * HC + 32 * h2, r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + dd * zin[32 * h + j]);
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) + dd * zin[hh * HC + 32 * h2 + j]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(sm + L::QT + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                        *reinterpret_cast<uint4*>(sm + L::QT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
+                            pack8(r + 8 * q, 1.f);
                 }
                 column_sums(L::KT, nullptr);  // z after the tile = z + sum_j k_j
                 // S after the tile -> bf16 operand for the next tile (the state update is its own group)
                 mbar_wait(bar_m2b, par, ERR_TIMEOUT_MMA);
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    tmem_ld32(tmem + lane_base + L::T_ST + hh * HC + 32 * h2, r);
                     if (srow)
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                            *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, hh * HCH + 4 * h2 + q, L::SR_ATOM)) =
                                 pack8(r + 8 * q, 1.f);
                 }
                 fence_async_smem();
                 tc_fence_before();
-                epi_sync();  // dq staging and column partials complete; every dq has read z
-                if (t == 0) {
+                epi_sync256();  // dq staging and column partials complete; every dq has read z
+                if (tid == 0) {
 #pragma unroll
                     for (int a = 0; a < NA; ++a) tma_store_3d(&tdq, sm + L::QT + a * 16384, 64 * a, row0, (int)g);
                     tma_store_commit();
                 }
-                if (t < D) zin[t] += zpart[t] + zpart[D + t] + zpart[2 * D + t] + zpart[3 * D + t];
+                if (tid < D) zin[tid] += warp_total(tid);
             } else {
                 // dk = dA^T Q + V R^T + r -> staging in GN (dN's last reader, R += Q^T dN, is done)
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_DK + 32 * h, r);
+                    tmem_ld32(tmem + lane_base + L::T_DK + hh * HC + 32 * h2, r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + rz[32 * h + j]);
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) + rz[hh * HC + 32 * h2 + j]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, 4 * h + q, 16384)) = pack8(r + 8 * q, 1.f);
+                        *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
+                            pack8(r + 8 * q, 1.f);
                 }
                 column_sums(L::QT, ddt);  // r before the tile = r + sum_i dd_i q_i
                 // R before the tile -> bf16 operand for the next (earlier) tile; after tile 0: dS0
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_ST + 32 * h, r);
+                    tmem_ld32(tmem + lane_base + L::T_ST + hh * HC + 32 * h2, r);
                     if (srow) {
                         if (b > 0) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, 4 * h + q, L::SR_ATOM)) =
+                                *reinterpret_cast<uint4*>(sm + L::SR +
+                                                          chunk_at(prow, hh * HCH + 4 * h2 + q, L::SR_ATOM)) =
                                     pack8(r + 8 * q, 1.f);
                         } else if (dS0) {
-                            float4* dst = reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)prow * D + 32 * h);
+                            float4* dst =
+                                reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)prow * D + hh * HC + 32 * h2);
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
@@ -552,19 +588,19 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 fence_async_smem();
                 fence_async_global();  // the parked values were read before the dk store overwrites them
                 tc_fence_before();
-                epi_sync();  // dk staging and column partials complete; every dk has read r
-                if (t == 0) {
+                epi_sync256();  // dk staging and column partials complete; every dk has read r
+                if (tid == 0) {
 #pragma unroll
                     for (int a = 0; a < NA; ++a) tma_store_3d(&tdk, sm + L::GN + a * 16384, 64 * a, row0, (int)g);
                     tma_store_commit();
                 }
-                if (t < D) {
-                    rz[t] += zpart[t] + zpart[D + t] + zpart[2 * D + t] + zpart[3 * D + t];
-                    if (b == 0 && dz0) dz0[g * D + t] = rz[t];
+                if (tid < D) {
+                    rz[tid] += warp_total(tid);
+                    if (b == 0 && dz0) dz0[g * D + tid] = rz[tid];
                 }
             }
-            epi_sync();                         // z / r updated before the next tile reads them
-            if (t == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
+            epi_sync256();                        // z / r updated before the next tile reads them
+            if (tid == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
             mbar_arrive(bar_e3);
         }
     }
