@@ -314,6 +314,7 @@ def run_ours(args, rank, world, local):
         kernels[k]["avg_us"] = round(kernels[k]["avg_us"], 3)
         kernels[k]["gbs"] = round(kernels[k]["gbs"], 1)
     fwd_only = job_value(world, G, C, 1, fwd_secs)
+    others = measure_other_configs(stream, eps, hbm) if rank == 0 else None
 
     out = None
     if rank == 0:
@@ -328,7 +329,7 @@ def run_ours(args, rank, world, local):
                              f"{l2 / 2**20:.0f} MiB)", "timing": "CUDA graphs, CUDA events, max over ranks"},
             "fwd_only": {"value": fwd_only, "unit": UNIT, "us_per_launch": kernels["la_fwd"]["avg_us"]},
             "roofline": roof, "kernels": kernels, "e2e": e2e, "gpu_launches": 2 * args.steps,
-            "clocks": clock_info, "cpu_baseline": cpu,
+            "clocks": clock_info, "cpu_baseline": cpu, "other_configs": others,
         }
     if world > 1:
         import torch.distributed as dist
@@ -368,6 +369,78 @@ def gpu_local_cpus(local):
         return None
     cpus &= os.sched_getaffinity(0)
     return cpus or None
+
+
+# The other workloads (parity cases in tests/), measured the same way as the headline's
+# per-kernel numbers, for context: (name, G, C, D, block, directions)
+OTHER_CONFIGS = (
+    ("batch16_fwdbwd: G=640, C=128, D=64, block=64, bf16", 640, 128, 64, 64, ("fwd", "bwd")),
+    ("long_stream_fwd: G=160, T=8192 as one C=8192 launch, D=64, bf16", 160, 8192, 64, 64, ("fwd",)),
+    ("wide_heads_fwdbwd: G=320, C=256, D=128, block=64, bf16", 320, 256, 128, 64, ("fwd", "bwd")),
+    ("wide_heads_ragged_fwdbwd: G=320, C=200, D=128, block=64, bf16", 320, 200, 128, 64, ("fwd", "bwd")),
+)
+
+
+def measure_other_configs(stream, eps, hbm):
+    """Per-launch device time of each direction on the other workloads: CUDA graphs of 20
+    launches over enough buffer sets that the working set exceeds 4x L2."""
+    import torch
+
+    import causal_linear_attention_gb300 as la
+    from causal_linear_attention_gb300.inputs import make_inputs
+    dev = stream.device
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for name, G, C, D, block, dirs in OTHER_CONFIGS:
+        x = make_inputs(G, C, D, dtype="bf16", seed=rank_seed(0), grads="bwd" in dirs).to(dev)
+        fb, bb = algorithmic_bytes(G, C, D, 2)
+        nsets = max(1, min(8, -(-4 * l2 // (fb + (bb if "bwd" in dirs else 0)))))
+        sets = []
+        for _ in range(nsets):
+            d = {k: (None if t is None else t.clone()) for k, t in x.__dict__.items()}
+            o = (torch.empty_like(x.q), torch.empty(G, D, D, device=dev), torch.empty(G, D, device=dev))
+            gr = (torch.empty_like(x.q), torch.empty_like(x.q), torch.empty_like(x.q), torch.empty(G, D, D, device=dev),
+                  torch.empty(G, D, device=dev)) if "bwd" in dirs else None
+            sets.append((d, o, gr))
+        entry = {"G": G, "C": C, "D": D, "block": block}
+        for direction in dirs:
+            def call(i, direction=direction):
+                d, o, gr = sets[i % nsets]
+                if direction == "fwd":
+                    la.chunked_fwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], block=block, eps=eps, o=o[0],
+                                   S_out=o[1], z_out=o[2])
+                else:
+                    la.chunked_bwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], d["dO"], d["dS_out"], d["dz_out"],
+                                   block=block, eps=eps, out=gr)
+            n = 20
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    call(i)
+            torch.cuda.synchronize()
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                for i in range(n):
+                    call(i)
+            gph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(3):
+                    gph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (3 * n)
+            byts = fb if direction == "fwd" else bb
+            entry[direction] = {"us": round(us, 2), "gbs": round(byts / us / 1e3, 1),
+                                "frac": round(byts / us / 1e3 / hbm, 4)}
+        secs = sum(entry[d]["us"] for d in dirs) * 1e-6
+        entry["value"] = G * C / secs
+        entry["unit"] = UNIT + (" (" + "+".join(dirs) + ")")
+        out[name] = entry
+        del sets, x
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
