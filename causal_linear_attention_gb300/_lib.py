@@ -87,6 +87,8 @@ def lib():
         L.la_step_workspace_bytes.restype = ctypes.c_size_t
         L.la_chunked_step_host.argtypes = [P] * 17 + [ctypes.c_size_t, I, I, I, I, I, F, P]
         L.la_chunked_step_host.restype = I
+        L.la_selftest_bounded_wait.argtypes = [I]
+        L.la_selftest_bounded_wait.restype = I
         L.la_bwd_max_c.argtypes = [I, I, I]
         L.la_bwd_max_c.restype = I
         L.la_status_string.argtypes = [I]
@@ -98,7 +100,7 @@ def lib():
 
 
 EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
-           "la_device_status", "la_status_string", "la_version")
+           "la_device_status", "la_selftest_bounded_wait", "la_status_string", "la_version")
 
 
 def _p(x) -> Optional[int]:
@@ -151,6 +153,11 @@ def la_device_status(clear: bool = True) -> int:
     """Synchronise the device; LA_ERR_TIMEOUT (4) if a kernel gave up a bounded wait,
     LA_ERR_DEVICE (5) if one found its shared memory misaligned and did nothing."""
     return int(lib().la_device_status(1 if clear else 0))
+
+
+def la_selftest_bounded_wait(wait_us: int = 1000) -> int:
+    """Status of the bounded-wait self-test: LA_ERR_TIMEOUT (4) is the expected result."""
+    return int(lib().la_selftest_bounded_wait(wait_us))
 
 
 def la_status_string(status: int) -> str:

@@ -507,6 +507,21 @@ extern "C" la_status la_device_status(int clear)
     return word ? LA_ERR_DEVICE : LA_OK;
 }
 
+extern "C" la_status la_selftest_bounded_wait(int wait_us)
+{
+    if (wait_us < 1 || wait_us > 1000000) return LA_ERR_INVALID;
+    uint32_t before = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&before, la::tc::g_status, sizeof(before)) != cudaSuccess) return LA_ERR_CUDA;
+    la::tc::la_selftest_wait_kernel<<<1, 32>>>((unsigned long long)wait_us * 1000ull);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
+    uint32_t after = 0;
+    if (cudaMemcpyFromSymbol(&after, la::tc::g_status, sizeof(after)) != cudaSuccess) return LA_ERR_CUDA;
+    // leave the device word as it was: the self-test's own timeout is not a fault of real work
+    if (cudaMemcpyToSymbol(la::tc::g_status, &before, sizeof(before)) != cudaSuccess) return LA_ERR_CUDA;
+    return (after & ~before & la::tc::ERR_TIMEOUT_MMA) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
 extern "C" const char* la_status_string(la_status status)
 {
     switch (status) {

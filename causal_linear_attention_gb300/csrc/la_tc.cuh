@@ -64,19 +64,32 @@ __device__ __forceinline__ unsigned long long global_ns()
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-// Bounded wait for phase `parity` to complete.  Gives up after kWaitLimitNs of wall
-// time, ORs `err_bit` into g_status and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t err_bit)
+// Bounded wait for phase `parity` to complete.  Gives up after `limit_ns` of wall time
+// (kWaitLimitNs unless stated), ORs `err_bit` into g_status and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t err_bit,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             atomicOr(&g_status, err_bit);
             return false;
         }
     }
     return true;
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever
+// arrives at; the wait must give up after `limit_ns` and the kernel return normally.
+__global__ void la_selftest_wait_kernel(unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0, ERR_TIMEOUT_MMA, limit_ns);
+    }
 }
 
 // ---------------------------------------------------------------- proxies / fences

@@ -156,6 +156,16 @@ la_status la_chunked_step_host(const void* q, const void* k, const void* v,
                                int G, int C, int D, int block, la_dtype dtype, float eps,
                                void* stream);
 
+/* Self-test of the bounded on-device waits (the failure-detection path): synchronises
+ * the current device, launches one kernel whose single wait is on an mbarrier nothing
+ * ever arrives at, bounded by wait_us microseconds (1 .. 10^6), and synchronises
+ * again.  Returns LA_ERR_TIMEOUT when the wait gave up as it must (the expected
+ * result; the device stays usable and la_device_status is left as it was), LA_OK if
+ * it somehow did not, LA_ERR_INVALID for a wait_us out of range, LA_ERR_CUDA if a
+ * CUDA call failed.  No counterpart on the page: it tests this library's own safety
+ * net. */
+la_status la_selftest_bounded_wait(int wait_us);
+
 /* Static, NUL-terminated description of a status code. */
 const char* la_status_string(la_status status);
 

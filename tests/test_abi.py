@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
-                                           "la_status_string", "la_version"])
+                                           "la_selftest_bounded_wait", "la_status_string", "la_version"])
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -159,6 +159,11 @@ def step(**kw):
 ])
 def test_host_step_argument_checks(L, kw, status):
     assert step(**kw) == status
+
+
+def test_selftest_rejects_out_of_range_waits_before_any_cuda_call(L):
+    assert la.la_selftest_bounded_wait(0) == INVALID
+    assert la.la_selftest_bounded_wait(2_000_000) == INVALID
 
 
 def test_host_step_empty_problem_is_accepted_without_copies(L):

@@ -227,3 +227,13 @@ def test_long_chunk_backward(G, C, D):
     (the kernel parks 1/den and dd in the dk rows between its passes)."""
     assert la.la_bwd_max_c(D, 64, la.LA_BF16) >= C
     bwd_case(G, C, D, 64, "bf16", seed=C)
+
+
+def test_bounded_wait_gives_up_and_the_device_stays_usable():
+    """Failure detection without a fault: a wait nothing satisfies gives up after its
+    bound (1 ms here), the library reports it, and the next calls run normally."""
+    assert la.la_device_status() == 0
+    assert la.la_selftest_bounded_wait(1000) == 4  # LA_ERR_TIMEOUT, as it must
+    assert la.la_device_status() == 0              # the self-test leaves the device word alone
+    fwd_case(4, 128, 64, 64, "bf16", seed=21)
+    assert la.la_device_status() == 0
