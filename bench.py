@@ -443,7 +443,7 @@ def measure_other_configs(stream, eps, hbm):
     return out
 
 
-def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
+def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=3):
     """End to end through the C ABI with HOST buffers: every step copies its inputs from
     pinned host memory into a device workspace, runs forward + backward and copies every
     output back (la_chunked_step_host).  Two streams with a workspace and an output set
@@ -465,12 +465,13 @@ def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
             return (torch.empty_like(q, pin_memory=True), f(G, D, D), f(G, D), torch.empty_like(q, pin_memory=True),
                     torch.empty_like(q, pin_memory=True), torch.empty_like(q, pin_memory=True), f(G, D, D), f(G, D))
 
-        sets = [(outs(), la.step_workspace(G, C, D, q.dtype, dev), torch.cuda.Stream(device=dev)) for _ in range(2)]
+        sets = [(outs(), la.step_workspace(G, C, D, q.dtype, dev), torch.cuda.Stream(device=dev))
+                for _ in range(nstreams)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
         d2h = sum(t.numel() * t.element_size() for t in sets[0][0])
 
         def step(i):
-            out, ws, s = sets[i % 2]
+            out, ws, s = sets[i % nstreams]
             la.chunked_step_host(pin["q"], pin["k"], pin["v"], pin["S0"], pin["z0"], pin["dO"], pin["dS_out"],
                                  pin["dz_out"], out=out, workspace=ws, block=block, eps=eps, stream=s)
 
@@ -508,7 +509,7 @@ def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": job_value(world, G, C, n, secs), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "steps": n, "api": "la_chunked_step_host (C ABI, pinned host buffers), two streams",
+            "steps": n, "api": f"la_chunked_step_host (C ABI, pinned host buffers), {nstreams} streams",
             "host_cpus": f"{len(near)} cpus of the GPU's NUMA node" if near else "unrestricted",
             "copy_gbs": gbs}
 
