@@ -446,8 +446,9 @@ def measure_other_configs(stream, eps, hbm):
 def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=3):
     """End to end through the C ABI with HOST buffers: every step copies its inputs from
     pinned host memory into a device workspace, runs forward + backward and copies every
-    output back (la_chunked_step_host).  Two streams with a workspace and an output set
-    each let one step's copies overlap the next step's, as a pipelined caller would."""
+    output back (la_chunked_step_host).  Three streams with a workspace and an output set
+    each let one step's copies overlap the next steps', as a pipelined caller would (two
+    streams measured 5 % slower, four no faster)."""
     import torch
 
     import causal_linear_attention_gb300 as la
