@@ -20,10 +20,11 @@ from typing import Optional
 
 from . import _lib
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
-                   la_chunked_step_host, la_device_status, la_selftest_bounded_wait, la_status_string,
-                   la_step_workspace_bytes, la_version, lib)
+                   la_chunked_fwd_split, la_chunked_step_host, la_device_status, la_fwd_split_workspace_bytes,
+                   la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
-__all__ = ["chunked_fwd", "chunked_bwd", "chunked_step_host", "step_workspace", "la_chunked_fwd", "la_chunked_bwd",
+__all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_step_host", "step_workspace", "la_chunked_fwd",
+           "la_chunked_fwd_split", "la_fwd_split_workspace_bytes", "la_chunked_bwd",
            "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
@@ -69,6 +70,33 @@ def chunked_fwd(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float = 1e-6
     S_out = torch.empty(G, D, D, device=q.device, dtype=torch.float32) if S_out is None else S_out
     z_out = torch.empty(G, D, device=q.device, dtype=torch.float32) if z_out is None else z_out
     la_chunked_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, _dtype_code(q), eps, _stream(stream))
+    return o, S_out, z_out
+
+
+def chunked_fwd_split(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float = 1e-6, o=None, S_out=None,
+                      z_out=None, workspace=None, stream=None):
+    """chunked_fwd cut along the tokens for few groups of long chunks (bf16, D = 64): the
+    pieces of every group run on separate CTAs from carries computed by a prefix over the
+    pieces' own sums.  `workspace` (a CUDA tensor of at least la_fwd_split_workspace_bytes
+    bytes) is allocated here when not given.  Returns (o, S_out, z_out)."""
+    import torch
+    G, C, D = q.shape
+    dt = q.dtype
+    for n, t in (("k", k), ("v", v)):
+        _check_tensor(n, t, q.shape, dt, q.device)
+    _check_tensor("q", q, q.shape, dt, q.device)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, q.device)
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(G, D, D, device=q.device, dtype=torch.float32) if S_out is None else S_out
+    z_out = torch.empty(G, D, device=q.device, dtype=torch.float32) if z_out is None else z_out
+    need = la_fwd_split_workspace_bytes(G, C, D, _dtype_code(q))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    la_chunked_fwd_split(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, _dtype_code(q), eps, workspace, wbytes,
+                         _stream(stream))
     return o, S_out, z_out
 
 

@@ -20,6 +20,7 @@
 #include "la_bwd_tc.cuh"
 #include "la_fwd_tc128.cuh"
 #include "la_bwd_tcm.cuh"
+#include "la_fwd_split.cuh"
 
 namespace {
 
@@ -174,8 +175,11 @@ bool tmap_state_f32(CUtensorMap* map, const float* base, int G, int D)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The bf16 head-size-64 forward; with piece_carry != nullptr, the G * P pieces of the
+// chunk-parallel forward (la_chunked_fwd_split).
 la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
-                        float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+                        float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream, int P = 1,
+                        int PL = 0, const float* piece_carry = nullptr)
 {
     static OptIn flag;
     auto kern = la::la_fwd_tc_kernel;
@@ -188,8 +192,8 @@ la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float
             !tmap_bf16(&to, o, G, C, 64, R))
             return LA_ERR_CUDA;
     }
-    return launch_pdl(kern, G, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, to, S0, z0,
-                      S_out, z_out, C, eps);
+    return launch_pdl(kern, G * P, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, to, S0, z0,
+                      S_out, z_out, C, eps, P, PL, piece_carry);
 }
 
 la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
@@ -323,9 +327,12 @@ bool ptrs_ok(const void* const* ps, int n, const bool* required)
 
 }  // namespace
 
-extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
-                                    void* o, float* S_out, float* z_out, int G, int C, int D, int block,
-                                    la_dtype dtype, float eps, void* stream)
+namespace {
+
+// Argument checks shared by the forward entry points.
+la_status check_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* o,
+                    const float* S_out, const float* z_out, int G, int C, int D, int block, la_dtype dtype,
+                    float eps)
 {
     size_t esz = 0;
     la_status st = check_common(G, C, D, block, dtype, eps, &esz);
@@ -339,6 +346,17 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
     const Buf outs[] = {{o, n_x}, {S_out, n_S}, {z_out, n_z}};
     const int inplace[] = {-1, 3, 4};
     if (!disjoint(outs, 3, ins, 5, inplace)) return LA_ERR_INVALID;
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                    void* o, float* S_out, float* z_out, int G, int C, int D, int block,
+                                    la_dtype dtype, float eps, void* stream)
+{
+    la_status st = check_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps);
+    if (st != LA_OK) return st;
     if (G == 0) return LA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -353,6 +371,104 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
     LA_FWD_TABLE(LA_FWD_CASE)
 #undef LA_FWD_CASE
     return LA_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- chunk-parallel forward
+namespace {
+
+int sm_count()
+{
+    static std::atomic<int> cached[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// How a chunk is cut: P pieces of PL tokens (the last one ragged) so that G * P CTAs
+// about fill the GPU at two per SM; P = 1 when that does not help or does not apply.
+struct SplitPlan {
+    int P = 1, PL = 0;
+    size_t bytes = 0;  // workspace: one cell per piece
+};
+
+bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
+{
+    *plan = SplitPlan{};
+    plan->PL = C;
+    if (dtype != LA_BF16 || D != 64 || G <= 0 || C <= 128) return true;
+    const int sms = sm_count();
+    if (sms == 0) return false;
+    const int nsb = (C + 127) / 128;
+    const int want = std::min(nsb, std::max(1, 2 * sms / G));
+    if (want <= 1) return true;
+    const int bpp = (nsb + want - 1) / want;  // 128-token blocks per piece
+    plan->P = (nsb + bpp - 1) / bpp;
+    plan->PL = bpp * 128;
+    plan->bytes = plan->P > 1 ? (size_t)G * plan->P * la::DeltaLayout::CELL * 4 : 0;
+    if (plan->P == 1) plan->PL = C;
+    return true;
+}
+
+la_status fwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                           float* S_out, float* z_out, int G, int C, float eps, const SplitPlan& plan, float* ws,
+                           cudaStream_t stream)
+{
+    static OptIn dflag;
+    auto dkern = la::la_state_delta_kernel;
+    la_status st = prepare(dkern, dflag, la::DeltaLayout::BYTES);
+    if (st != LA_OK) return st;
+    CUtensorMap tk{}, tv{};
+    if (!tmap_bf16(&tk, k, G, C, 64, 128) || !tmap_bf16(&tv, v, G, C, 64, 128)) return LA_ERR_CUDA;
+    st = launch_pdl(dkern, G * plan.P, la::DeltaLayout::THREADS, la::DeltaLayout::BYTES, stream, tk, tv, C, plan.P,
+                    plan.PL, ws);
+    if (st != LA_OK) return st;
+    st = launch_pdl(la::la_state_scan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, S0, z0, ws, plan.P);
+    if (st != LA_OK) return st;
+    return fwd_tc_launch(q, k, v, nullptr, nullptr, o, S_out, z_out, G, C, eps, stream, plan.P, plan.PL, ws);
+}
+
+}  // namespace
+
+extern "C" size_t la_fwd_split_workspace_bytes(int G, int C, int D, la_dtype dtype)
+{
+    size_t esz = 0;
+    if (check_common(G, C, D, 64, dtype, 0.f, &esz) != LA_OK) return 0;
+    SplitPlan plan;
+    if (!split_plan(G, C, D, dtype, &plan)) return 0;
+    return plan.bytes;
+}
+
+extern "C" la_status la_chunked_fwd_split(const void* q, const void* k, const void* v, const float* S0,
+                                          const float* z0, void* o, float* S_out, float* z_out, int G, int C, int D,
+                                          int block, la_dtype dtype, float eps, void* workspace,
+                                          size_t workspace_bytes, void* stream)
+{
+    la_status st = check_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps);
+    if (st != LA_OK) return st;
+    if (G == 0) return LA_OK;
+    SplitPlan plan;
+    if (!split_plan(G, C, D, dtype, &plan)) return LA_ERR_CUDA;
+    if (plan.P == 1) return la_chunked_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps, stream);
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < plan.bytes)
+        return LA_ERR_INVALID;
+    const size_t n_x = (size_t)G * C * D * 2, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    const Buf wsb = {workspace, plan.bytes};
+    const Buf all[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}, {o, n_x}, {S_out, n_S}, {z_out, n_z}};
+    for (const Buf& b : all)
+        if (overlaps(wsb, b)) return LA_ERR_INVALID;
+    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, plan, static_cast<float*>(workspace),
+                            static_cast<cudaStream_t>(stream));
 }
 
 extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,

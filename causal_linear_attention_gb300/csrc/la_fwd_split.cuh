@@ -1,0 +1,197 @@
+// la_fwd_split.cuh -- the chunk-parallel forward's helper kernels (few groups, long chunks).
+//
+// "Fractus-1B training optimization -- 2026-08-22", section 2, "Opt 2": the state after a
+// run of tokens is the state before it plus the run's own sum of outer products,
+//     S_after = S_before + sum_j k_j v_j^T,   z_after = z_before + sum_j k_j,
+// so a chunk cut into P pieces can be processed in parallel: every piece first sums its
+// own keys and values (la_state_delta_kernel), an exclusive prefix over the pieces turns
+// those sums into each piece's carry (la_state_scan_kernel), and then every piece runs the
+// ordinary chunked forward from its carry (la_fwd_tc_kernel in piece mode).  With one
+// group per CTA, a few groups of long chunks would leave most SMs idle; cut this way they
+// fill the GPU.  The result equals the sequential one up to the order of the fp32 sums.
+//
+// The per-piece sums live in a caller-provided device workspace: for piece p of group g,
+// the D x D fp32 sum [p][c] followed by the D fp32 key sums (4160 floats at D = 64).
+#pragma once
+#include <cuda_bf16.h>
+
+#include "la_fwd_tc.cuh"
+#include "la_tc.cuh"
+
+namespace la {
+
+struct DeltaLayout {
+    static constexpr int D = 64;
+    static constexpr uint32_t KT0 = 0, KT1 = 16384;   // K tiles, two stages
+    static constexpr uint32_t VT0 = 32768, VT1 = 49152;
+    static constexpr uint32_t F = 65536;              // fp32 sum staging [p][c]
+    static constexpr uint32_t ZPART = 81920;          // float[4][64]
+    static constexpr uint32_t BARS = 82944;
+    static constexpr uint32_t END = 83072;
+    static constexpr uint32_t BYTES = END;
+    static constexpr uint32_t TMEM_COLS = 64;
+    static constexpr int THREADS = 160;
+    static constexpr uint32_t CELL = D * D + D;       // floats per piece in the workspace
+};
+
+// One CTA per piece (grid G * P): sum_j k_j v_j^T over the piece's tokens on the tensor
+// core (the transposed sum accumulates in TMEM, M = 64), sum_j k_j on the CUDA cores, the
+// tiles streamed through two TMA stages.
+__global__ void __launch_bounds__(160, 2)
+la_state_delta_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, int C, int P,
+                      int PL, float* delta)
+{
+    using L = DeltaLayout;
+    using namespace tc;
+    constexpr int D = L::D;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t sbase = smem_addr(sm);
+    float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* full = bars + 0;   // [2] K, V of a stage landed (TMA)
+    uint64_t* empty = bars + 2;  // [2] a stage's MMA and column sums are done (MMA commit + 128)
+    uint64_t* done = bars + 4;   // every MMA of the piece is done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 40);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = (int)blockIdx.x / P, piece = (int)blockIdx.x % P;
+    const int rbase = piece * PL;
+    const int nblk = (min(PL, C - rbase) + 127) / 128;
+
+    if (tid == 0) {
+        mbar_init(full + 0, 1);
+        mbar_init(full + 1, 1);
+        mbar_init(empty + 0, 129);
+        mbar_init(empty + 1, 129);
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            auto load = [&](int blk) {
+                const int s = blk & 1;
+                mbar_expect_tx(full + s, 32768);
+                tma_load_3d(sm + (s ? L::KT1 : L::KT0), &tk, full + s, 0, rbase + blk * 128, g);
+                tma_load_3d(sm + (s ? L::VT1 : L::VT0), &tv, full + s, 0, rbase + blk * 128, g);
+            };
+            for (int blk = 0; blk < min(2, nblk); ++blk) load(blk);
+            pdl_launch_dependents();
+            const uint32_t id_state = idesc_bf16(64, 64, true, true);
+            bool ok = true;
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int s = blk & 1;
+                const uint32_t ph = (blk >> 1) & 1;
+                ok = mbar_wait(full + s, ph, ERR_TIMEOUT_TMA);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dK = smem_desc(sbase + (s ? L::KT1 : L::KT0), 16, 1024);
+                const uint64_t dV = smem_desc(sbase + (s ? L::VT1 : L::VT0), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // sum^T += V^T K  (M = c, N = p, K = j; both read MN-major)
+                    umma_bf16(tmem, dV + kk * 128, dK + kk * 128, id_state, blk > 0 || kk > 0);
+                umma_commit(empty + s);
+                if (blk + 2 < nblk) {
+                    ok = mbar_wait(empty + s, ph, ERR_TIMEOUT_MMA);
+                    if (ok) load(blk + 2);
+                }
+            }
+            umma_commit(done);
+        }
+    } else {
+        // ---- column sums of K: thread (cc, rg) sums 8 rows x 8 columns of every block
+        const int t = tid, cc = t & 7, rg = t >> 3;
+        float zs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zs[e] = 0.f;
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int s = blk & 1;
+            mbar_wait(full + s, (blk >> 1) & 1, ERR_TIMEOUT_TMA);
+            const uint32_t kt = s ? L::KT1 : L::KT0;
+#pragma unroll
+            for (int r8 = 0; r8 < 8; ++r8) {
+                const uint4 u = *reinterpret_cast<const uint4*>(sm + kt + sw_chunk(rg * 8 + r8, cc));
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    zs[2 * e] += f.x;
+                    zs[2 * e + 1] += f.y;
+                }
+            }
+            mbar_arrive(empty + s);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            zs[e] += __shfl_xor_sync(0xffffffffu, zs[e], 8);
+            zs[e] += __shfl_xor_sync(0xffffffffu, zs[e], 16);
+        }
+        if (lane < 8)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zpart[warp * 64 + 8 * cc + e] = zs[e];
+        // ---- the sum of outer products: TMEM lane c (M = 64 layout) holds row c of the
+        //      transposed sum; staged as [p][c] and bulk-stored
+        mbar_wait(done, 0, ERR_TIMEOUT_MMA);
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32x64(tmem + ((uint32_t)(32 * warp) << 16), r);
+        if (lane < 16) {
+            float* f = reinterpret_cast<float*>(sm + L::F);
+            const int c = 16 * warp + lane;
+#pragma unroll
+            for (int p = 0; p < 64; ++p) f[p * D + c] = __uint_as_float(r[p]);
+        }
+        fence_async_smem();
+        epi_sync();
+        float* cell = delta + (size_t)blockIdx.x * L::CELL;
+        if (t == 0) {
+            bulk_store(cell, sm + L::F, D * D * 4);
+            tma_store_commit();
+            tma_store_wait_read();
+        }
+        if (t < D) cell[D * D + t] = zpart[t] + zpart[64 + t] + zpart[128 + t] + zpart[192 + t];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+// Exclusive prefix over each group's pieces, in place: piece p's cell becomes the state
+// before it (S0 plus the sums of pieces 0..p-1).  SCAN_BLOCKS blocks of 256 threads per
+// group, one element of the cell per thread.
+constexpr int SCAN_BLOCKS = (DeltaLayout::CELL + 255) / 256;
+
+__global__ void __launch_bounds__(256)
+la_state_scan_kernel(const float* S0, const float* z0, float* delta, int P)
+{
+    constexpr int D = DeltaLayout::D;
+    constexpr uint32_t CELL = DeltaLayout::CELL;
+    pdl_wait();
+    const int e = ((int)blockIdx.x % SCAN_BLOCKS) * 256 + threadIdx.x;
+    const size_t g = blockIdx.x / SCAN_BLOCKS;
+    if (e >= (int)CELL) return;
+    float run = e < D * D ? (S0 ? S0[g * D * D + e] : 0.f) : (z0 ? z0[g * D + (e - D * D)] : 0.f);
+    float* cell = delta + g * P * CELL + e;
+    for (int p = 0; p < P; ++p, cell += CELL) {
+        const float d = *cell;
+        *cell = run;
+        run += d;
+    }
+}
+
+}  // namespace la

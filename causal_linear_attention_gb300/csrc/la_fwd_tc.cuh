@@ -93,8 +93,13 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 __global__ void __launch_bounds__(160, 2)
 la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                 const float* S0, const float* z0, float* S_out, float* z_out, int C, float eps)
+                 const float* S0, const float* z0, float* S_out, float* z_out, int C, float eps,
+                 int P = 1, int PL = 0, const float* piece_carry = nullptr)
 {
+    // Piece mode (piece_carry != nullptr): the chunk of each group is cut into P pieces of PL
+    // tokens (the last one ragged); CTA b runs piece b % P of group b / P with the carry
+    // piece_carry[b] (S [D][D] then z [D], fp32) and writes S_out, z_out only for the last
+    // piece, whose final state is the group's.
     using L = FwdTcLayout;
     using namespace tc;
     constexpr int D = 64;
@@ -119,8 +124,18 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 96);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x;
-    const int nsb = (C + 127) / 128;
+    const int g = piece_carry ? (int)blockIdx.x / P : (int)blockIdx.x;  // group
+    const int piece = piece_carry ? (int)blockIdx.x % P : 0;
+    const int rbase = piece * PL;                                          // first token of the piece
+    const int nsb = ((piece_carry ? min(PL, C - rbase) : C) + 127) / 128;
+    // this CTA's incoming carry: the group's S0 / z0, or the piece's cell
+    const float* S0g = S0 ? S0 + (size_t)g * D * D : nullptr;
+    const float* z0g = z0 ? z0 + (size_t)g * D : nullptr;
+    if (piece_carry) {
+        S0g = piece_carry + (size_t)blockIdx.x * (D * D + D);
+        z0g = S0g + D * D;
+        if (piece + 1 < P) S_out = z_out = nullptr;
+    }
 
     if (tid == 0) {
         mbar_init(bar_s0, 1);
@@ -139,9 +154,9 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         tmem_relinquish();
     }
     if (warp < 4) {  // S0 / z0 absent: zero carry
-        if (!S0)
+        if (!S0g)
             for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::S0F)[i] = make_uint4(0, 0, 0, 0);
-        if (!z0 && tid < D) zin[tid] = 0.f;
+        if (!z0g && tid < D) zin[tid] = 0.f;
     }
     fence_async_smem();
     tc_fence_before();
@@ -159,18 +174,18 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             prefetch_tmap(&to);
             auto issue_qk = [&](int sb) {
                 mbar_expect_tx(bar_qk, L::LOAD_BYTES / 3 * 2);
-                tma_load_3d(sm + L::QT, &tq, bar_qk, 0, sb * 128, g);
-                tma_load_3d(sm + L::KS, &tk, bar_qk, 0, sb * 128, g);
+                tma_load_3d(sm + L::QT, &tq, bar_qk, 0, rbase + sb * 128, g);
+                tma_load_3d(sm + L::KS, &tk, bar_qk, 0, rbase + sb * 128, g);
             };
             auto issue_v = [&](int sb) {
                 mbar_expect_tx(bar_v, L::LOAD_BYTES / 3);
-                tma_load_3d(sm + L::VT, &tv, bar_v, 0, sb * 128, g);
+                tma_load_3d(sm + L::VT, &tv, bar_v, 0, rbase + sb * 128, g);
             };
             if (nsb > 0) {  // the carry first (its conversion runs while Q, K land), then Q, K, V
                 // (with neither S0 nor z0 this arrival alone completes the phase)
-                mbar_expect_tx(bar_s0, (S0 ? 16384u : 0u) + (z0 ? 256u : 0u));
-                if (S0) bulk_load(sm + L::S0F, S0 + (size_t)g * D * D, 16384, bar_s0);
-                if (z0) bulk_load(sm + L::ZIN, z0 + (size_t)g * D, 256, bar_s0);
+                mbar_expect_tx(bar_s0, (S0g ? 16384u : 0u) + (z0g ? 256u : 0u));
+                if (S0g) bulk_load(sm + L::S0F, S0g, 16384, bar_s0);
+                if (z0g) bulk_load(sm + L::ZIN, z0g, 256, bar_s0);
                 issue_qk(0);
                 issue_v(0);
             }
@@ -229,7 +244,7 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         for (int sb = 0; sb < nsb; ++sb) {
             const uint32_t par = sb & 1;
-            const int row0 = sb * 128;
+            const int row0 = rbase + sb * 128;
             const bool last = sb + 1 == nsb;
             if (sb == 0) {  // carry in: S^T operand rows <- bf16(S0)^T.  Thread t converts column
                             // c = t % 64, rows p in [32h, 32h+32) with h = t / 64 (conflict-free reads)

@@ -118,6 +118,33 @@ int la_bwd_max_c(int D, int block, la_dtype dtype);
 la_status la_device_status(int clear);
 
 /*
+ * Chunk-parallel forward for few groups of long chunks (bf16, head size 64).
+ * The state after a run of tokens is the state before it plus the run's own sums
+ * (section 2, "Opt 2", read run by run), so each group's chunk is cut into P pieces
+ * that run on P CTAs: the pieces' sums of k v^T and k, an exclusive prefix over them
+ * (each piece's carry), then the ordinary chunked forward of every piece from its carry.
+ * Results equal la_chunked_fwd's up to the order of the fp32 state sums.
+ *
+ * la_fwd_split_workspace_bytes: device workspace the call needs on the current device
+ * (one 16,640-byte cell per piece); 0 when no split applies (other dtypes or head
+ * sizes, C <= 128, or G already large enough to fill the GPU) -- then la_chunked_fwd_split
+ * simply runs la_chunked_fwd and needs no workspace.
+ *
+ * la_chunked_fwd_split: arguments, layouts, in-place carries and errors as
+ * la_chunked_fwd; workspace is caller-owned DEVICE memory, 256-byte aligned, at least
+ * la_fwd_split_workspace_bytes(G, C, D, dtype) bytes, disjoint from every tensor and not
+ * used by anything else until the stream has completed (LA_ERR_INVALID otherwise).  The
+ * library allocates nothing.  Three kernels are enqueued on `stream`.
+ */
+size_t la_fwd_split_workspace_bytes(int G, int C, int D, la_dtype dtype);
+
+la_status la_chunked_fwd_split(const void* q, const void* k, const void* v,
+                               const float* S0, const float* z0,
+                               void* o, float* S_out, float* z_out,
+                               int G, int C, int D, int block, la_dtype dtype, float eps,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Host-buffer form of one training step of a chunk (forward, then the backward of
  * section 1 on the same inputs), for callers whose tensors start and end in host
  * memory.  The page has no counterpart: its chunked form runs on device tensors.

@@ -29,7 +29,8 @@ def declared_functions():
 
 
 def test_header_declares_the_boundary():
-    assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_step_workspace_bytes",
+    assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes",
+                                           "la_chunked_fwd_split", "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
 
