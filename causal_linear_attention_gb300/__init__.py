@@ -20,11 +20,12 @@ from typing import Optional
 
 from . import _lib
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
-                   la_chunked_fwd_split, la_chunked_step_host, la_device_status, la_fwd_split_workspace_bytes,
+                   la_chunked_fwd_split, la_chunked_fwd_split_static, la_chunked_step_host, la_device_status,
+                   la_fwd_split_workspace_bytes,
                    la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
 __all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_step_host", "step_workspace", "la_chunked_fwd",
-           "la_chunked_fwd_split", "la_fwd_split_workspace_bytes", "la_chunked_bwd",
+           "la_chunked_fwd_split", "la_chunked_fwd_split_static", "la_fwd_split_workspace_bytes", "la_chunked_bwd",
            "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]

@@ -91,6 +91,8 @@ def lib():
         L.la_fwd_split_workspace_bytes.restype = ctypes.c_size_t
         L.la_chunked_fwd_split.argtypes = [P] * 8 + [I, I, I, I, I, F, P, ctypes.c_size_t, P]
         L.la_chunked_fwd_split.restype = I
+        L.la_chunked_fwd_split_static.argtypes = [P] * 8 + [I, I, I, I, I, F, P]
+        L.la_chunked_fwd_split_static.restype = I
         L.la_selftest_bounded_wait.argtypes = [I]
         L.la_selftest_bounded_wait.restype = I
         L.la_bwd_max_c.argtypes = [I, I, I]
@@ -104,6 +106,7 @@ def lib():
 
 
 EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes", "la_chunked_fwd_split",
+           "la_chunked_fwd_split_static",
            "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
            "la_device_status", "la_selftest_bounded_wait", "la_status_string", "la_version")
 
@@ -146,6 +149,14 @@ def la_chunked_fwd_split(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: in
     """Raw C-ABI call (device pointers or tensors).  Raises LAError on a non-OK status."""
     _check(lib().la_chunked_fwd_split(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(o), _p(S_out), _p(z_out), G, C, D,
                                       block, dtype, eps, _p(workspace), workspace_bytes, _p(stream)))
+
+
+def la_chunked_fwd_split_static(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: int, block: int, dtype: int,
+                                eps: float, stream=None) -> None:
+    """Raw C-ABI call of the chunk-parallel forward that needs no workspace (module-level
+    device scratch; calls on one device must not overlap in time)."""
+    _check(lib().la_chunked_fwd_split_static(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(o), _p(S_out), _p(z_out), G, C,
+                                             D, block, dtype, eps, _p(stream)))
 
 
 def la_step_workspace_bytes(G: int, C: int, D: int, dtype: int) -> int:

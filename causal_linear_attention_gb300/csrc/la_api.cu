@@ -471,6 +471,59 @@ extern "C" la_status la_chunked_fwd_split(const void* q, const void* k, const vo
                             static_cast<cudaStream_t>(stream));
 }
 
+// ---------------------------------------------------------------- chunk-parallel forward, no workspace
+namespace {
+
+// The chunk-parallel forward needs a little device memory between its kernels (one 16,640-
+// byte cell per piece).  For callers that cannot allocate any, la_chunked_fwd_split_static
+// takes it from this module-level array instead of a workspace argument: 8 MiB, room for
+// 504 cells, while a plan never asks for more than two pieces per SM (304 cells on a
+// 152-SM GPU; a larger request is rejected).  Nothing in it has to start at zero: the sum
+// kernel writes every cell before the scan reads it.  Every call on a device shares it,
+// so calls that overlap in time (several streams or host threads) would race.
+constexpr size_t kStaticScratchBytes = (size_t)8 << 20;
+static __device__ __align__(256) unsigned char g_split_scratch[kStaticScratchBytes];
+
+// Device address of the array on the current device, looked up once per device (with
+// that device current) and cached; nullptr if the lookup fails.
+void* static_split_scratch()
+{
+    static std::atomic<void*> addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_split_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+}  // namespace
+
+extern "C" la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* v, const float* S0,
+                                                 const float* z0, void* o, float* S_out, float* z_out, int G, int C,
+                                                 int D, int block, la_dtype dtype, float eps, void* stream)
+{
+    la_status st = check_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps);
+    if (st != LA_OK) return st;
+    if (G == 0) return LA_OK;
+    SplitPlan plan;
+    if (!split_plan(G, C, D, dtype, &plan)) return LA_ERR_CUDA;
+    if (plan.P == 1) return la_chunked_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps, stream);
+    if (plan.bytes > kStaticScratchBytes) return LA_ERR_UNSUPPORTED;
+    void* ws = static_split_scratch();
+    if (!ws) return LA_ERR_CUDA;
+    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, plan, static_cast<float*>(ws),
+                            static_cast<cudaStream_t>(stream));
+}
+
 extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
                                     const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk,
                                     void* dv, float* dS0, float* dz0, int G, int C, int D, int block,

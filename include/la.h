@@ -145,6 +145,26 @@ la_status la_chunked_fwd_split(const void* q, const void* k, const void* v,
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * la_chunked_fwd_split without a workspace argument, for callers that cannot allocate
+ * device memory.  The page has no counterpart: it is this library's way of running the
+ * chunk-parallel forward above from a fixed, module-level device array of 8 MiB (room for
+ * 504 piece cells; a plan asking for more -- more than about 250 SMs' worth of pieces --
+ * returns LA_ERR_UNSUPPORTED).  Arguments, results and errors otherwise as
+ * la_chunked_fwd_split; with no split to make it runs la_chunked_fwd.
+ *   - Every call on a device uses the same array: calls that may overlap in time (on
+ *     different streams, or from different host threads) race and must be ordered by the
+ *     caller (one stream, or events).
+ *   - The first call on each device looks the array up and sets the kernels' shared-memory
+ *     limits (CUDA runtime calls that do not belong in a stream capture): make one call
+ *     outside any capture before capturing calls into a CUDA graph.
+ */
+la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* v,
+                                      const float* S0, const float* z0,
+                                      void* o, float* S_out, float* z_out,
+                                      int G, int C, int D, int block, la_dtype dtype, float eps,
+                                      void* stream);
+
+/*
  * Host-buffer form of one training step of a chunk (forward, then the backward of
  * section 1 on the same inputs), for callers whose tensors start and end in host
  * memory.  The page has no counterpart: its chunked form runs on device tensors.

@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes",
-                                           "la_chunked_fwd_split", "la_step_workspace_bytes",
+                                           "la_chunked_fwd_split", "la_chunked_fwd_split_static",
+                                           "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
 
@@ -169,6 +170,21 @@ def test_selftest_rejects_out_of_range_waits_before_any_cuda_call(L):
 
 def test_host_step_empty_problem_is_accepted_without_copies(L):
     assert step(G=0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(q=None), INVALID), (dict(o=None), INVALID), (dict(q=A + 4), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(o=A), INVALID),
+])
+def test_split_forward_entry_points_check_arguments_first(L, kw, status):
+    """Both chunk-parallel entry points run the forward's checks before any CUDA call."""
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, S0=None, z0=None, o=A + 0x300000, S_out=None,
+                z_out=None, G=2, C=8, D=64, block=64, dtype=la.LA_BF16, eps=1e-6)
+    args.update(kw)
+    head = [args[n] for n in ("q", "k", "v", "S0", "z0", "o", "S_out", "z_out")]
+    tail = [args[n] for n in ("G", "C", "D", "block", "dtype", "eps")]
+    assert L.la_chunked_fwd_split(*head, *tail, None, 0, None) == status
+    assert L.la_chunked_fwd_split_static(*head, *tail, None) == status
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

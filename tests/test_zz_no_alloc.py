@@ -1,0 +1,46 @@
+"""The chunk-parallel forward without a workspace (la_chunked_fwd_split_static).
+
+It runs the same kernels as la_chunked_fwd_split on a module-level device array, so on
+the same inputs its results must equal the workspace form bit for bit, call after call.
+(The file name puts it after the other GPU tests; it also passes on its own.)"""
+import pytest
+import torch
+
+import causal_linear_attention_gb300 as la
+from causal_linear_attention_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+EPS = 1e-6
+
+
+def test_static_scratch_forward_equals_the_workspace_form_on_consecutive_calls():
+    la.build()
+    for G, C, seed in ((2, 4096, 31), (8, 1000, 32)):  # two calls in a row, different plans
+        assert la.la_fwd_split_workspace_bytes(G, C, 64, la.LA_BF16) > 0
+        x = make_inputs(G, C, 64, dtype="bf16", seed=seed, carry=True).to(DEV)
+        ref = la.chunked_fwd_split(x.q, x.k, x.v, x.S0, x.z0, block=64, eps=EPS)
+        o = torch.empty_like(x.q)
+        S = torch.empty(G, 64, 64, device=DEV)
+        z = torch.empty(G, 64, device=DEV)
+        la.la_chunked_fwd_split_static(x.q, x.k, x.v, x.S0, x.z0, o, S, z, G, C, 64, 64, la.LA_BF16, EPS,
+                                       torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("o", "S_out", "z_out"), (o, S, z), ref):
+            assert torch.equal(a, b), name
+    assert la.la_device_status() == 0
+
+
+def test_static_scratch_forward_without_a_split_is_the_plain_forward():
+    x = make_inputs(200, 256, 64, dtype="bf16", seed=33, carry=True).to(DEV)
+    assert la.la_fwd_split_workspace_bytes(200, 256, 64, la.LA_BF16) == 0
+    ref = la.chunked_fwd(x.q, x.k, x.v, x.S0, x.z0, block=64, eps=EPS)
+    o = torch.empty_like(x.q)
+    S = torch.empty(200, 64, 64, device=DEV)
+    z = torch.empty(200, 64, device=DEV)
+    la.la_chunked_fwd_split_static(x.q, x.k, x.v, x.S0, x.z0, o, S, z, 200, 256, 64, 64, la.LA_BF16, EPS,
+                                   torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    for a, b in zip((o, S, z), ref):
+        assert torch.equal(a, b)
