@@ -295,7 +295,6 @@ def run_ours(args, rank, world, local):
     # end to end through the public API: pinned host inputs -> device -> fwd + bwd -> host outputs
     e2e = run_e2e(args, host, G, C, D, block, eps, local, bar, mor)
 
-    tokens = G * C
     value = job_value(world, G, C, args.steps, secs)
     hbm, peak_src = measured_peaks()
     kernels = {

@@ -18,7 +18,6 @@ from __future__ import annotations
 
 from typing import Optional
 
-from . import _lib
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
                    la_chunked_fwd_split, la_chunked_fwd_split_static, la_chunked_step_host, la_device_status,
                    la_fwd_split_workspace_bytes,

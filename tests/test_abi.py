@@ -1,6 +1,5 @@
 """The C-ABI library builds, loads and exports every symbol include/la.h declares;
 host-side argument checks reject bad calls before anything touches a GPU."""
-import ctypes
 import os
 import re
 import shutil

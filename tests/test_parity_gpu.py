@@ -5,7 +5,6 @@ C = 128 tokens, head size 64, carry active) plus wide heads and ragged chunks;
 inputs are seeded and synthetic (causal_linear_attention_gb300.inputs), the same
 bits go to both sides.  Metric and tolerances: tests/parity_util.py.
 """
-import numpy as np
 import pytest
 import torch
 
