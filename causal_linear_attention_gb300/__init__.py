@@ -18,13 +18,14 @@ from __future__ import annotations
 
 from typing import Optional
 
-from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_chunked_bwd, la_chunked_fwd,
-                   la_chunked_fwd_split, la_chunked_fwd_split_static, la_chunked_step_host, la_device_status,
-                   la_fwd_split_workspace_bytes,
+from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_bwd_split_workspace_bytes, la_chunked_bwd,
+                   la_chunked_bwd_split, la_chunked_fwd, la_chunked_fwd_split, la_chunked_fwd_split_static,
+                   la_chunked_step_host, la_device_status, la_fwd_split_workspace_bytes,
                    la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
-__all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_step_host", "step_workspace", "la_chunked_fwd",
-           "la_chunked_fwd_split", "la_chunked_fwd_split_static", "la_fwd_split_workspace_bytes", "la_chunked_bwd",
+__all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_bwd_split", "chunked_step_host",
+           "step_workspace", "la_chunked_fwd", "la_chunked_fwd_split", "la_chunked_fwd_split_static",
+           "la_fwd_split_workspace_bytes", "la_chunked_bwd", "la_chunked_bwd_split", "la_bwd_split_workspace_bytes",
            "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
@@ -98,6 +99,41 @@ def chunked_fwd_split(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float 
     la_chunked_fwd_split(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, _dtype_code(q), eps, workspace, wbytes,
                          _stream(stream))
     return o, S_out, z_out
+
+
+def _bwd_args(q, k, v, S0, z0, dO, dS_out, dz_out, out):
+    import torch
+    G, C, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _check_tensor(n, t, q.shape, q.dtype, q.device)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D)), ("dS_out", dS_out, (G, D, D)),
+                      ("dz_out", dz_out, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q),
+               torch.empty(G, D, D, device=q.device, dtype=torch.float32),
+               torch.empty(G, D, device=q.device, dtype=torch.float32))
+    return out
+
+
+def chunked_bwd_split(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 64, eps: float = 1e-6,
+                      out: Optional[tuple] = None, workspace=None, stream=None):
+    """chunked_bwd cut along the tokens for few groups of long chunks (bf16, D = 64): the
+    pieces of every group run on separate CTAs, between prefix sums over the pieces in
+    token order (the forward carries) and in reverse (the carry gradients).  `workspace`
+    (a CUDA tensor of at least la_bwd_split_workspace_bytes bytes) is allocated here when
+    not given.  Returns (dq, dk, dv, dS0, dz0)."""
+    import torch
+    G, C, D = q.shape
+    dq, dk, dv, dS0, dz0 = _bwd_args(q, k, v, S0, z0, dO, dS_out, dz_out, out)
+    need = la_bwd_split_workspace_bytes(G, C, D, _dtype_code(q))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    la_chunked_bwd_split(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block, _dtype_code(q),
+                         eps, workspace, wbytes, _stream(stream))
+    return dq, dk, dv, dS0, dz0
 
 
 def chunked_bwd(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 64, eps: float = 1e-6,

@@ -234,11 +234,14 @@ la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float
                       tds, S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
 }
 
-// Multi-tile tensor-core backward (bf16, head size 64 or 128, any C).
+// Multi-tile tensor-core backward (bf16, head size 64 or 128, any C).  mode 0: both passes
+// over whole chunks (P = 1); modes 1 / 2: one pass over P pieces of PL tokens per group,
+// carries in fcell / rcell (the chunk-parallel backward, head size 64).
 template <int D>
 la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
                          const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0,
-                         float* dz0, int G, int C, float eps, cudaStream_t stream)
+                         float* dz0, int G, int C, float eps, cudaStream_t stream, int P = 1, int PL = 0, int mode = 0,
+                         const float* fcell = nullptr, float* rcell = nullptr)
 {
     using L = la::BwdTcmLayout<D>;
     static OptIn flag;
@@ -256,8 +259,8 @@ la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const floa
             !tmap_bf16(&tdv, dv, G, C, D, R))
             return LA_ERR_CUDA;
     }
-    return launch_pdl(kern, G, L::THREADS, smem, stream, tq, tk, tv, tg, tdq, tdk, tdv, S0, z0, dS_out, dz_out, dS0,
-                      dz0, static_cast<__nv_bfloat16*>(dk), C, eps);
+    return launch_pdl(kern, G * P, L::THREADS, smem, stream, tq, tk, tv, tg, tdq, tdk, tdv, S0, z0, dS_out, dz_out,
+                      dS0, dz0, static_cast<__nv_bfloat16*>(dk), C, eps, P, PL, mode, fcell, rcell);
 }
 
 // ---------------------------------------------------------------- kernel table
@@ -349,6 +352,26 @@ la_status check_fwd(const void* q, const void* k, const void* v, const float* S0
     return LA_OK;
 }
 
+// Argument checks shared by the backward entry points.
+la_status check_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
+                    const float* dS_out, const float* dz_out, const void* dq, const void* dk, const void* dv,
+                    const float* dS0, const float* dz0, int G, int C, int D, int block, la_dtype dtype, float eps)
+{
+    size_t esz = 0;
+    la_status st = check_common(G, C, D, block, dtype, eps, &esz);
+    if (st != LA_OK) return st;
+    const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    const bool t = n_x > 0;
+    const void* ps[] = {q, k, v, dO, dq, dk, dv, S0, z0, dS_out, dz_out, dS0, dz0};
+    const bool req[] = {t, t, t, t, t, t, t, false, false, false, false, false, false};
+    if (!ptrs_ok(ps, 13, req)) return LA_ERR_INVALID;
+    const Buf ins[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}, {dO, n_x}, {dS_out, n_S}, {dz_out, n_z}};
+    const Buf outs[] = {{dq, n_x}, {dk, n_x}, {dv, n_x}, {dS0, n_S}, {dz0, n_z}};
+    const int inplace[] = {-1, -1, -1, 6, 7};
+    if (!disjoint(outs, 5, ins, 8, inplace)) return LA_ERR_INVALID;
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
@@ -395,14 +418,15 @@ int sm_count()
     return n;
 }
 
-// How a chunk is cut: P pieces of PL tokens (the last one ragged) so that G * P CTAs
-// about fill the GPU at two per SM; P = 1 when that does not help or does not apply.
+// How a chunk is cut: P pieces of PL tokens (the last one ragged, none empty) so that
+// G * P CTAs about fill the GPU at `per_sm` per SM (the forward's kernel fits two on an
+// SM, the backward's one); P = 1 when that does not help or does not apply.
 struct SplitPlan {
     int P = 1, PL = 0;
-    size_t bytes = 0;  // workspace: one cell per piece
+    size_t bytes = 0;  // workspace: `cells` cells per piece
 };
 
-bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
+bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan, int per_sm = 2, int cells = 1)
 {
     *plan = SplitPlan{};
     plan->PL = C;
@@ -410,19 +434,25 @@ bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
     const int sms = sm_count();
     if (sms == 0) return false;
     const int nsb = (C + 127) / 128;
-    const int want = std::min(nsb, std::max(1, 2 * sms / G));
+    const int want = std::min(nsb, std::max(1, per_sm * sms / G));
     if (want <= 1) return true;
     const int bpp = (nsb + want - 1) / want;  // 128-token blocks per piece
     plan->P = (nsb + bpp - 1) / bpp;
     plan->PL = bpp * 128;
-    plan->bytes = plan->P > 1 ? (size_t)G * plan->P * la::DeltaLayout::CELL * 4 : 0;
+    plan->bytes = plan->P > 1 ? (size_t)cells * G * plan->P * la::DeltaLayout::CELL * 4 : 0;
     if (plan->P == 1) plan->PL = C;
     return true;
 }
 
-la_status fwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
-                           float* S_out, float* z_out, int G, int C, float eps, const SplitPlan& plan, float* ws,
-                           cudaStream_t stream)
+bool bwd_split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
+{
+    return split_plan(G, C, D, dtype, plan, 1, 2);
+}
+
+// Every piece's forward carry into ws: the pieces' sums of k v^T and k, then their
+// exclusive prefix from S0, z0.
+la_status piece_carries(const void* k, const void* v, const float* S0, const float* z0, int G, int C,
+                        const SplitPlan& plan, float* ws, cudaStream_t stream)
 {
     static OptIn dflag;
     auto dkern = la::la_state_delta_kernel;
@@ -433,9 +463,38 @@ la_status fwd_split_launch(const void* q, const void* k, const void* v, const fl
     st = launch_pdl(dkern, G * plan.P, la::DeltaLayout::THREADS, la::DeltaLayout::BYTES, stream, tk, tv, C, plan.P,
                     plan.PL, ws);
     if (st != LA_OK) return st;
-    st = launch_pdl(la::la_state_scan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, S0, z0, ws, plan.P);
+    return launch_pdl(la::la_state_scan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, S0, z0, ws, plan.P);
+}
+
+la_status fwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                           float* S_out, float* z_out, int G, int C, float eps, const SplitPlan& plan, float* ws,
+                           cudaStream_t stream)
+{
+    const la_status st = piece_carries(k, v, S0, z0, G, C, plan, ws, stream);
     if (st != LA_OK) return st;
     return fwd_tc_launch(q, k, v, nullptr, nullptr, o, S_out, z_out, G, C, eps, stream, plan.P, plan.PL, ws);
+}
+
+// The chunk-parallel backward: forward carries, pass 1 of every piece (dq, the parked
+// 1/den and dd, each piece's own reverse sums), their reverse prefix (and dS0, dz0), pass 2
+// of every piece (dk, dv).  ws holds the forward cells, then the reverse cells.
+la_status bwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                           const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv,
+                           float* dS0, float* dz0, int G, int C, float eps, const SplitPlan& plan, float* ws,
+                           cudaStream_t stream)
+{
+    float* fcell = ws;
+    float* rcell = ws + (size_t)G * plan.P * la::DeltaLayout::CELL;
+    la_status st = piece_carries(k, v, S0, z0, G, C, plan, fcell, stream);
+    if (st != LA_OK) return st;
+    st = bwd_tcm_launch<64>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
+                            stream, plan.P, plan.PL, 1, fcell, rcell);
+    if (st != LA_OK) return st;
+    st = launch_pdl(la::la_state_rscan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, dS_out, dz_out, rcell, dS0, dz0,
+                    plan.P);
+    if (st != LA_OK) return st;
+    return bwd_tcm_launch<64>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
+                              stream, plan.P, plan.PL, 2, fcell, rcell);
 }
 
 }  // namespace
@@ -529,18 +588,8 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
                                     void* dv, float* dS0, float* dz0, int G, int C, int D, int block,
                                     la_dtype dtype, float eps, void* stream)
 {
-    size_t esz = 0;
-    la_status st = check_common(G, C, D, block, dtype, eps, &esz);
+    la_status st = check_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block, dtype, eps);
     if (st != LA_OK) return st;
-    const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
-    const bool t = n_x > 0;
-    const void* ps[] = {q, k, v, dO, dq, dk, dv, S0, z0, dS_out, dz_out, dS0, dz0};
-    const bool req[] = {t, t, t, t, t, t, t, false, false, false, false, false, false};
-    if (!ptrs_ok(ps, 13, req)) return LA_ERR_INVALID;
-    const Buf ins[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}, {dO, n_x}, {dS_out, n_S}, {dz_out, n_z}};
-    const Buf outs[] = {{dq, n_x}, {dk, n_x}, {dv, n_x}, {dS0, n_S}, {dz0, n_z}};
-    const int inplace[] = {-1, -1, -1, 6, 7};
-    if (!disjoint(outs, 5, ins, 8, inplace)) return LA_ERR_INVALID;
     if (G == 0) return LA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // bf16, head size 64, one 128-token tile: the tensor-core (tcgen05 / TMEM / TMA) kernel
@@ -561,6 +610,42 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
     LA_BWD_TABLE(LA_BWD_CASE)
 #undef LA_BWD_CASE
     return LA_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- chunk-parallel backward
+extern "C" size_t la_bwd_split_workspace_bytes(int G, int C, int D, la_dtype dtype)
+{
+    size_t esz = 0;
+    if (check_common(G, C, D, 64, dtype, 0.f, &esz) != LA_OK) return 0;
+    SplitPlan plan;
+    if (!bwd_split_plan(G, C, D, dtype, &plan)) return 0;
+    return plan.bytes;
+}
+
+extern "C" la_status la_chunked_bwd_split(const void* q, const void* k, const void* v, const float* S0,
+                                          const float* z0, const void* dO, const float* dS_out, const float* dz_out,
+                                          void* dq, void* dk, void* dv, float* dS0, float* dz0, int G, int C, int D,
+                                          int block, la_dtype dtype, float eps, void* workspace,
+                                          size_t workspace_bytes, void* stream)
+{
+    la_status st = check_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block, dtype, eps);
+    if (st != LA_OK) return st;
+    if (G == 0) return LA_OK;
+    SplitPlan plan;
+    if (!bwd_split_plan(G, C, D, dtype, &plan)) return LA_ERR_CUDA;
+    if (plan.P == 1)
+        return la_chunked_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, block, dtype, eps,
+                              stream);
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < plan.bytes)
+        return LA_ERR_INVALID;
+    const size_t n_x = (size_t)G * C * D * 2, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+    const Buf wsb = {workspace, plan.bytes};
+    const Buf all[] = {{q, n_x},      {k, n_x},      {v, n_x},   {S0, n_S},  {z0, n_z},  {dO, n_x},  {dS_out, n_S},
+                       {dz_out, n_z}, {dq, n_x},     {dk, n_x},  {dv, n_x},  {dS0, n_S}, {dz0, n_z}};
+    for (const Buf& b : all)
+        if (overlaps(wsb, b)) return LA_ERR_INVALID;
+    return bwd_split_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, plan,
+                            static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- host-buffer step

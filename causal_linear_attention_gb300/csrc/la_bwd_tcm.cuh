@@ -32,6 +32,17 @@
 // dk row (dk is only written in pass 2, after they have been read back), so the chunk
 // length is not bounded by on-chip memory; pass 2 re-reads the tiles, mostly from L2.
 //
+// Piece mode (head size 64; the chunk-parallel backward): the grid has P CTAs per group,
+// CTA (g, p) owning tokens [p PL, (p+1) PL) of group g, and each launch runs ONE pass:
+//   mode 1 runs pass 1 over the piece from its forward carry (S, z before the piece: a
+//          cell of D*D + D floats, S as [p][c] then z) and also sums the piece's own
+//          Q^T dN (a fourth TMEM accumulator) and Q^T dd, written to the piece's cell of
+//          `rcell` -- what pass 2 adds to R and r over the piece;
+//   mode 2 runs pass 2 over the piece from its reverse carry (R, r after the piece, read
+//          from the same cell once a reverse scan has turned the sums into carries).
+// Between them the parked (1/den, dd) wait in dk as usual.  Mode 0 is the whole chunk,
+// both passes, P = 1.
+//
 // One CTA per group, warp-specialised: warps 0-7 own the 128 rows of a tile, two warps per
 // 32-lane TMEM quarter splitting the columns (warp w: lanes 32 (w % 4) .., column half
 // w / 4; a row's two partial sums meet in shared memory); warp 8 is the producer (TMA
@@ -71,7 +82,9 @@ struct BwdTcmLayout {
     static constexpr uint32_t XCH = ZPART + 8 * D * 4;     // float[2][2][128]: the two halves of a row
     static constexpr uint32_t BARS = XCH + 2048;
     static constexpr uint32_t DDT = BARS + 128;            // float[128]: dd of the tile's rows
-    static constexpr uint32_t BYTES = DDT + 512;
+    static constexpr uint32_t ZPART2 = DDT + 512;          // float[8][D]: per-warp sums of dd q (mode 1)
+    static constexpr uint32_t RZL = ZPART2 + 8 * D * 4;    // float[D]: the piece's sum of dd q (mode 1)
+    static constexpr uint32_t BYTES = RZL + D * 4;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns; pass 2 reuses pass 1's
     static constexpr uint32_t T_SC = 0;           // scores, then P = dN V^T (128)
@@ -80,6 +93,8 @@ struct BwdTcmLayout {
     static constexpr uint32_t T_AV = 128 + D;     // A V (pass 1) / dk (pass 2)
     static constexpr uint32_t T_DK = 128 + D;
     static constexpr uint32_t T_ST = 128 + 2 * D; // S (pass 1) / R (pass 2): D x D, rows p
+    static constexpr uint32_t T_RL = 128 + 3 * D; // mode 1, head size 64: the piece's Q^T dN
+    static constexpr uint32_t CELL = D * D + D;   // floats per piece carry cell
     static constexpr int THREADS = 288;           // 8 epilogue warps + the producer
     static constexpr int BOX_ROWS = 128;
     static constexpr uint32_t HALF_BYTES = 2 * TILE;  // Q + K, or dO + V, of a tile
@@ -102,7 +117,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
                   const __grid_constant__ CUtensorMap tdv,
                   const float* S0, const float* z0, const float* dS_out, const float* dz_out,
-                  float* dS0, float* dz0, __nv_bfloat16* dk, int C, float eps)
+                  float* dS0, float* dz0, __nv_bfloat16* dk, int C, float eps, int P, int PL, int mode,
+                  const float* fcell, float* rcell)
 {
     using L = BwdTcmLayout<D>;
     using namespace tc;
@@ -113,11 +129,24 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
         return;
     }
+    static_assert(D == 64 || L::T_RL + D > L::TMEM_COLS, "T_RL is used at head size 64 only");
     const uint32_t sbase = smem_addr(sm);
-    const int nsb = (C + 127) / 128;
+    const size_t g = blockIdx.x / P;
+    const int rbase = (int)(blockIdx.x % P) * PL;
+    const int nsb = ((P == 1 ? C : min(PL, C - rbase)) + 127) / 128;  // 128-token tiles of this CTA
+    const int it0 = mode == 2 ? nsb : 0, it1 = mode == 1 ? nsb : 2 * nsb;
+    // where the two D x D accumulators start from
+    const float* cellF = mode == 1 ? fcell + (size_t)blockIdx.x * L::CELL : nullptr;
+    float* cellR = mode != 0 ? rcell + (size_t)blockIdx.x * L::CELL : nullptr;
+    const float* Ssrc = mode == 1 ? cellF : S0 ? S0 + g * D * D : nullptr;
+    const float* zsrc = mode == 1 ? cellF + D * D : z0 ? z0 + g * D : nullptr;
+    const float* Rsrc = mode == 2 ? cellR : dS_out ? dS_out + g * D * D : nullptr;
+    const float* rsrc = mode == 2 ? cellR + D * D : dz_out ? dz_out + g * D : nullptr;
     float* zin = reinterpret_cast<float*>(sm + L::ZIN);
     float* rz = reinterpret_cast<float*>(sm + L::RZ);
     float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    float* zpart2 = reinterpret_cast<float*>(sm + L::ZPART2);
+    float* rzl = reinterpret_cast<float*>(sm + L::RZL);
     float* xch = reinterpret_cast<float*>(sm + L::XCH);
     float* ddt = reinterpret_cast<float*>(sm + L::DDT);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
@@ -133,7 +162,6 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 72);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t g = blockIdx.x;
 
     if (tid == 0) {
         mbar_init(bar_qk, 1);
@@ -175,17 +203,18 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 mbar_expect_tx(bar_qk, L::HALF_BYTES);
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
-                    tma_load_3d(sm + L::QT + a * 16384, &tq, bar_qk, 64 * a, b * 128, (int)g);
-                    tma_load_3d(sm + L::KT + a * 16384, &tk, bar_qk, 64 * a, b * 128, (int)g);
+                    tma_load_3d(sm + L::QT + a * 16384, &tq, bar_qk, 64 * a, rbase + b * 128, (int)g);
+                    tma_load_3d(sm + L::KT + a * 16384, &tk, bar_qk, 64 * a, rbase + b * 128, (int)g);
                 }
                 mbar_expect_tx(bar_vg, L::HALF_BYTES);
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
-                    tma_load_3d(sm + L::GN + a * 16384, &tg, bar_vg, 64 * a, b * 128, (int)g);
-                    tma_load_3d(sm + L::VT + a * 16384, &tv, bar_vg, 64 * a, b * 128, (int)g);
+                    tma_load_3d(sm + L::GN + a * 16384, &tg, bar_vg, 64 * a, rbase + b * 128, (int)g);
+                    tma_load_3d(sm + L::VT + a * 16384, &tv, bar_vg, 64 * a, rbase + b * 128, (int)g);
                 }
             };
-            load(0);
+            auto tile_of = [&](int it) { return it < nsb ? it : 2 * nsb - 1 - it; };
+            load(tile_of(it0));
             pdl_launch_dependents();
 
             // K-major operands: +32 B (2 units) per K = 16 step inside a 64-column atom, the
@@ -200,9 +229,9 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             auto kstep = [](uint64_t d, int kk) { return d + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2); };
 
             bool ok = true;
-            for (int it = 0; it < 2 * nsb && ok; ++it) {
+            for (int it = it0; it < it1 && ok; ++it) {
                 const bool p1 = it < nsb;
-                const uint32_t par = it & 1;
+                const uint32_t par = (it - it0) & 1;
                 // descriptors derived per tile from an opaque copy of the base address, so the
                 // compiler cannot hoist every unrolled instruction's operands out of the loop
                 uint32_t b0 = sbase;
@@ -238,6 +267,12 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     for (int kk = 0; kk < 8; ++kk)  // S += K^T V  (M = p, N = c, K = j)
                         umma_bf16(tmem + L::T_ST, dKm + kk * 128, dVm + kk * 128, id_dd, true);
                     umma_commit(bar_m2b);
+                    if constexpr (D == 64) {
+                        if (mode == 1)  // the piece's Q^T dN (M = p, N = c, K = i); done by bar_m3's commit
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                umma_bf16(tmem + L::T_RL, dQm + kk * 128, dGm + kk * 128, id_dd, it > 0 || kk > 0);
+                    }
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // dv = A^T dN  (M = j, K = i)
@@ -267,7 +302,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 umma_commit(bar_m3);
                 ok = mbar_wait(bar_e3, par, ERR_TIMEOUT_MMA);
-                if (ok && it + 1 < 2 * nsb) load(it + 1 < nsb ? it + 1 : 2 * nsb - 2 - it);
+                if (ok && it + 1 < it1) load(tile_of(it + 1));
             }
         }
     } else {
@@ -281,24 +316,24 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // layout puts row 16 q + l in lane l < 16 of quarter q
         const bool srow = D == 128 || lane < 16;
         const int prow = D == 128 ? t : 16 * q4 + lane;
-        for (int it = 0; it < 2 * nsb; ++it) {
+        for (int it = it0; it < it1; ++it) {
             const bool p1 = it < nsb;
             const int b = p1 ? it : 2 * nsb - 1 - it;
-            const uint32_t par = it & 1;
-            const int row0 = b * 128;
+            const uint32_t par = (it - it0) & 1;
+            const int row0 = rbase + b * 128;
             const bool row_ok = row0 + t < C;
-            if (it == 0 || it == nsb) {
-                // ---- a pass starts: S0 (pass 1) or dS_out (pass 2) -> the D x D TMEM accumulator
-                //      (fp32) and the bf16 operand SR, this thread's half of row prow; z0 -> z, or
-                //      dz_out -> r.  Every load is issued before the first use.
-                const float* src = it == 0 ? S0 : dS_out;
-                const float* srcv = it == 0 ? z0 : dz_out;
+            if (it == it0 || it == nsb) {
+                // ---- a pass starts: S (pass 1) or R (pass 2) -> the D x D TMEM accumulator
+                //      (fp32) and the bf16 operand SR, this thread's half of row prow; z or r.
+                //      Every load is issued before the first use.
+                const float* src = p1 ? Ssrc : Rsrc;
+                const float* srcv = p1 ? zsrc : rsrc;
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {  // 32 columns at a time, all loads first
                     uint32_t r[32];
                     if (srow && src) {
                         const float4* s4 =
-                            reinterpret_cast<const float4*>(src + g * D * D + (size_t)prow * D + hh * HC + 32 * h2);
+                            reinterpret_cast<const float4*>(src + (size_t)prow * D + hh * HC + 32 * h2);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 f = s4[j];
@@ -318,7 +353,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             *reinterpret_cast<uint4*>(sm + L::SR + chunk_at(prow, hh * HCH + 4 * h2 + q, L::SR_ATOM)) =
                                 pack8(r + 8 * q, 1.f);
                 }
-                if (tid < D) (it == 0 ? zin : rz)[tid] = srcv ? srcv[g * D + tid] : 0.f;
+                if (tid < D) (p1 ? zin : rz)[tid] = srcv ? srcv[tid] : 0.f;
+                if (mode == 1 && tid < D) rzl[tid] = 0.f;
                 epi_sync256();  // z / r complete before any thread reads them
             }
             // the row's (1/den, dd), parked in its dk row between the passes
@@ -475,7 +511,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // ---- E3
             // per-warp sums over the tile's 128 rows of a bf16 tile's columns, optionally
             // weighted per row: thread (cc, rg) sums D/16 rows x 8 columns, then the warp's rows
-            auto column_sums = [&](uint32_t tile, const float* wrow) {
+            auto column_sums = [&](uint32_t tile, const float* wrow, float* part) {
                 constexpr int CH = D / 8, RPG = CH / 2;
                 const int cc = tid % CH, rg = tid / CH;
                 float s[8];
@@ -501,17 +537,22 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 if (lane < CH)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) zpart[warp * D + 8 * cc + e] = s[e];
+                    for (int e = 0; e < 8; ++e) part[warp * D + 8 * cc + e] = s[e];
             };
-            auto warp_total = [&](int c) {
+            auto warp_total = [&](const float* part, int c) {
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) v += zpart[w * D + c];
+                for (int w = 0; w < 8; ++w) v += part[w * D + c];
                 return v;
             };
             mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             if (p1) {
+                if (mode == 1) {  // the piece's sum of dd_i q_i, before dq overwrites Q
+                    epi_sync256();  // every row's dd is in ddt
+                    column_sums(L::QT, ddt, zpart2);
+                    epi_sync256();  // Q read
+                }
                 // dq = U + dA K + dd z -> staging in QT (Q's last readers, M1 and q . U, are done)
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {
@@ -525,7 +566,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         *reinterpret_cast<uint4*>(sm + L::QT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
                             pack8(r + 8 * q, 1.f);
                 }
-                column_sums(L::KT, nullptr);  // z after the tile = z + sum_j k_j
+                column_sums(L::KT, nullptr, zpart);  // z after the tile = z + sum_j k_j
                 // S after the tile -> bf16 operand for the next tile (the state update is its own group)
                 mbar_wait(bar_m2b, par, ERR_TIMEOUT_MMA);
                 tc_fence_after();
@@ -547,7 +588,10 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     for (int a = 0; a < NA; ++a) tma_store_3d(&tdq, sm + L::QT + a * 16384, 64 * a, row0, (int)g);
                     tma_store_commit();
                 }
-                if (tid < D) zin[tid] += warp_total(tid);
+                if (tid < D) {
+                    zin[tid] += warp_total(zpart, tid);
+                    if (mode == 1) rzl[tid] += warp_total(zpart2, tid);
+                }
             } else {
                 // dk = dA^T Q + V R^T + r -> staging in GN (dN's last reader, R += Q^T dN, is done)
 #pragma unroll
@@ -562,7 +606,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
                             pack8(r + 8 * q, 1.f);
                 }
-                column_sums(L::QT, ddt);  // r before the tile = r + sum_i dd_i q_i
+                column_sums(L::QT, ddt, zpart);  // r before the tile = r + sum_i dd_i q_i
                 // R before the tile -> bf16 operand for the next (earlier) tile; after tile 0: dS0
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {
@@ -595,13 +639,29 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     tma_store_commit();
                 }
                 if (tid < D) {
-                    rz[tid] += warp_total(tid);
+                    rz[tid] += warp_total(zpart, tid);
                     if (b == 0 && dz0) dz0[g * D + tid] = rz[tid];
                 }
             }
             epi_sync256();                        // z / r updated before the next tile reads them
             if (tid == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
             mbar_arrive(bar_e3);
+        }
+        if constexpr (D == 64) {
+            if (mode == 1) {
+                // the piece's sums -> its cell: Q^T dN from TMEM (its last MMA completed before the
+                // last bar_m3), then Q^T dd
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + L::T_RL + hh * HC, r);
+                if (srow) {
+                    float4* dst = reinterpret_cast<float4*>(cellR + (size_t)prow * D + hh * HC);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                }
+                if (tid < D) cellR[D * D + tid] = rzl[tid];
+            }
         }
     }
     if (tid == 0) tma_store_wait_read();  // shared memory stays valid until the stores have read it

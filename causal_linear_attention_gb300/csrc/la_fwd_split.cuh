@@ -1,4 +1,5 @@
-// la_fwd_split.cuh -- the chunk-parallel forward's helper kernels (few groups, long chunks).
+// la_fwd_split.cuh -- the chunk-parallel forward's and backward's helper kernels (few
+// groups, long chunks).
 //
 // "Fractus-1B training optimization -- 2026-08-22", section 2, "Opt 2": the state after a
 // run of tokens is the state before it plus the run's own sum of outer products,
@@ -12,6 +13,13 @@
 //
 // The per-piece sums live in a caller-provided device workspace: for piece p of group g,
 // the D x D fp32 sum [p][c] followed by the D fp32 key sums (4160 floats at D = 64).
+//
+// The backward runs the same way in reverse ("the derivative of a cumsum is a reverse
+// cumsum", section 1): with every piece's forward carry known, the pass-1 launch of the
+// multi-tile backward (la_bwd_tcm_kernel, mode 1) also leaves each piece's own sums of
+// q dN^T and dd q in a second set of cells; a reverse exclusive prefix
+// (la_state_rscan_kernel) turns them into the gradient reaching each piece's end, and the
+// pass-2 launch (mode 2) finishes every piece from there.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -191,6 +199,36 @@ la_state_scan_kernel(const float* S0, const float* z0, float* delta, int P)
         const float d = *cell;
         *cell = run;
         run += d;
+    }
+}
+
+// Reverse exclusive prefix over each group's pieces, in place: piece p's cell (its own sums
+// of q dN^T [p][c] and of dd q) becomes the gradient reaching the state after the piece,
+// dS_out (dz_out) plus the sums of pieces p+1 .. P-1; the total over all pieces is the
+// gradient of the incoming carry, written to dS0 (dz0).  dS0 may be dS_out (dz0 dz_out):
+// each element is read and then written by the same thread.  NULL dS_out / dz_out = zero;
+// NULL dS0 / dz0 are skipped.  Launch as la_state_scan_kernel.
+__global__ void __launch_bounds__(256)
+la_state_rscan_kernel(const float* dS_out, const float* dz_out, float* delta, float* dS0, float* dz0, int P)
+{
+    constexpr int D = DeltaLayout::D;
+    constexpr uint32_t CELL = DeltaLayout::CELL;
+    pdl_wait();
+    const int e = ((int)blockIdx.x % SCAN_BLOCKS) * 256 + threadIdx.x;
+    const size_t g = blockIdx.x / SCAN_BLOCKS;
+    if (e >= (int)CELL) return;
+    const bool is_S = e < D * D;
+    float run = is_S ? (dS_out ? dS_out[g * D * D + e] : 0.f) : (dz_out ? dz_out[g * D + (e - D * D)] : 0.f);
+    float* cells = delta + g * P * CELL + e;
+    for (int p = P - 1; p >= 0; --p) {
+        const float d = cells[(size_t)p * CELL];
+        cells[(size_t)p * CELL] = run;
+        run += d;
+    }
+    if (is_S) {
+        if (dS0) dS0[g * D * D + e] = run;
+    } else if (dz0) {
+        dz0[g * D + (e - D * D)] = run;
     }
 }
 

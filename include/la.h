@@ -165,6 +165,36 @@ la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* 
                                       void* stream);
 
 /*
+ * Chunk-parallel backward for few groups of long chunks (bf16, head size 64): the
+ * reverse cumsum of section 1 cut into pieces like la_chunked_fwd_split's forward.
+ * Every piece's forward carry comes from the pieces' sums and their exclusive prefix; a
+ * first pass over every piece (token order) writes dq and each piece's own sums of
+ * q dN^T and dd q; their reverse exclusive prefix, started from dS_out / dz_out, is the
+ * gradient reaching each piece's end (and, over all pieces, dS0 / dz0); a second pass over
+ * every piece (reverse order) writes dk and dv.  Results equal la_chunked_bwd's up to
+ * the order of the fp32 sums.
+ *
+ * la_bwd_split_workspace_bytes: device workspace the call needs on the current device
+ * (two 16,640-byte cells per piece); 0 when no split applies (other dtypes or head sizes,
+ * C <= 128, or G already large enough to fill the GPU at one group per SM) -- then
+ * la_chunked_bwd_split simply runs la_chunked_bwd and needs no workspace.
+ *
+ * la_chunked_bwd_split: arguments, layouts, in-place carry gradients and errors as
+ * la_chunked_bwd; workspace is caller-owned DEVICE memory, 256-byte aligned, at least
+ * la_bwd_split_workspace_bytes(G, C, D, dtype) bytes, disjoint from every tensor and not
+ * used by anything else until the stream has completed (LA_ERR_INVALID otherwise).  The
+ * library allocates nothing.  Five kernels are enqueued on `stream`.
+ */
+size_t la_bwd_split_workspace_bytes(int G, int C, int D, la_dtype dtype);
+
+la_status la_chunked_bwd_split(const void* q, const void* k, const void* v,
+                               const float* S0, const float* z0,
+                               const void* dO, const float* dS_out, const float* dz_out,
+                               void* dq, void* dk, void* dv, float* dS0, float* dz0,
+                               int G, int C, int D, int block, la_dtype dtype, float eps,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Host-buffer form of one training step of a chunk (forward, then the backward of
  * section 1 on the same inputs), for callers whose tensors start and end in host
  * memory.  The page has no counterpart: its chunked form runs on device tensors.

@@ -30,6 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes",
                                            "la_chunked_fwd_split", "la_chunked_fwd_split_static",
+                                           "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
                                            "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
@@ -184,6 +185,31 @@ def test_split_forward_entry_points_check_arguments_first(L, kw, status):
     tail = [args[n] for n in ("G", "C", "D", "block", "dtype", "eps")]
     assert L.la_chunked_fwd_split(*head, *tail, None, 0, None) == status
     assert L.la_chunked_fwd_split_static(*head, *tail, None) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(dq=None), INVALID), (dict(dO=None), INVALID), (dict(dk=A + 8), INVALID),
+    (dict(D=48), UNSUPPORTED), (dict(dq=A), INVALID), (dict(dk=A + 0x400000, dv=A + 0x400000), INVALID),
+])
+def test_split_backward_checks_arguments_first(L, kw, status):
+    """The chunk-parallel backward runs the backward's checks before any CUDA call."""
+    base = {n: A + i * 0x100000 for i, n in enumerate(("q", "k", "v", "dO", "dq", "dk", "dv"))}
+    args = dict(base, S0=None, z0=None, dS_out=None, dz_out=None, dS0=None, dz0=None, G=2, C=8, D=64,
+                block=64, dtype=la.LA_BF16, eps=1e-6)
+    args.update(kw)
+    names = ("q", "k", "v", "S0", "z0", "dO", "dS_out", "dz_out", "dq", "dk", "dv", "dS0", "dz0", "G", "C", "D",
+             "block", "dtype", "eps")
+    assert L.la_chunked_bwd_split(*(args[n] for n in names), None, 0, None) == status
+
+
+def test_split_workspace_is_zero_where_no_split_applies(L):
+    """No split (so no workspace) for fp32, head size 128, or chunks of one tile; the
+    calls make no kernel launch to decide that."""
+    for f in (la.la_fwd_split_workspace_bytes, la.la_bwd_split_workspace_bytes):
+        assert f(2, 4096, 64, la.LA_F32) == 0
+        assert f(2, 4096, 128, la.LA_BF16) == 0
+        assert f(2, 128, 64, la.LA_BF16) == 0
+        assert f(-1, 4096, 64, la.LA_BF16) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

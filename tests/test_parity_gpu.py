@@ -270,3 +270,58 @@ def test_chunk_parallel_forward_falls_back_and_threads_carry_in_place():
     got = la.chunked_fwd_split(d.q, d.k, d.v, S, z, block=64, eps=EPS, S_out=S, z_out=z)
     torch.cuda.synchronize()
     check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
+
+
+@pytest.mark.parametrize("G,C", [(2, 4096), (8, 1000), (1, 300), (3, 2048), (1, 16384)])
+def test_chunk_parallel_backward(G, C):
+    """la_chunked_bwd_split (forward carries from a prefix over the pieces, carry gradients
+    from a reverse prefix) matches the oracle, and the sequential kernel within the bf16
+    bounds."""
+    x = make_inputs(G, C, 64, dtype="bf16", seed=G * C + 1, carry=True, grads=True)
+    assert la.la_bwd_split_workspace_bytes(G, C, 64, la.LA_BF16) > 0
+    d = x.to(DEV)
+    got = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
+    seq = la.chunked_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
+    torch.cuda.synchronize()
+    assert la.la_device_status() == 0
+    ref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
+    check(got, ref, "bf16", BWD_NAMES)
+    for a, b, n in zip(got, seq, BWD_NAMES):
+        assert max_rel(a, b.cpu().double().numpy()) < (2e-2 if n in ("dq", "dk", "dv") else 1e-4), n
+
+
+def test_chunk_parallel_backward_carry_cases():
+    # no upstream carry gradient, no carry
+    x = make_inputs(2, 1500, 64, dtype="bf16", seed=31, carry=False, grads=True)
+    x.dS_out = x.dz_out = None
+    d = x.to(DEV)
+    got = la.chunked_bwd_split(d.q, d.k, d.v, None, None, d.dO, None, None, block=64, eps=EPS)
+    torch.cuda.synchronize()
+    check(got, oracle.bwd(x.q, x.k, x.v, None, None, x.dO, None, None, eps=EPS), "bf16", BWD_NAMES)
+    # in place: dS0 over dS_out and dz0 over dz_out (the reverse scan reads each element
+    # before it writes it)
+    x = make_inputs(2, 2000, 64, dtype="bf16", seed=32, carry=True, grads=True)
+    d = x.to(DEV)
+    dS, dz = d.dS_out.clone(), d.dz_out.clone()
+    out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), dS, dz)
+    got = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, dS, dz, block=64, eps=EPS, out=out)
+    torch.cuda.synchronize()
+    check(got, oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS), "bf16", BWD_NAMES)
+    # dS0 = dz0 = NULL: skipped
+    out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), None, None)
+    got = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS, out=out)
+    torch.cuda.synchronize()
+    ref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
+    check(got[:3], ref[:3], "bf16", BWD_NAMES[:3])
+
+
+def test_chunk_parallel_backward_falls_back():
+    """Enough groups to fill the GPU (or one tile per chunk): no split, no workspace, the
+    ordinary backward."""
+    for G, C in ((300, 256), (4, 128)):
+        assert la.la_bwd_split_workspace_bytes(G, C, 64, la.LA_BF16) == 0
+        x = make_inputs(G, C, 64, dtype="bf16", seed=G + C, carry=True, grads=True)
+        d = x.to(DEV)
+        got = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
+        torch.cuda.synchronize()
+        check(got, oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS), "bf16", BWD_NAMES)
