@@ -61,6 +61,8 @@
 #pragma once
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "la_fwd_tc.cuh"
 #include "la_tc.cuh"
 
@@ -99,6 +101,53 @@ struct BwdTcmLayout {
     static constexpr int BOX_ROWS = 128;
     static constexpr uint32_t HALF_BYTES = 2 * TILE;  // Q + K, or dO + V, of a tile
 };
+
+// The causal mask j <= t over the 8 keys [j0, j0 + 8) for a warp whose 32 rows are
+// [r0, r0 + 32): the whole chunk is kept, dropped, or depends on the row.  The class is
+// the same for every lane of the warp, so branching on it does not diverge, and only the
+// chunks that straddle the warp's diagonal pay for a per-key compare.  (This pays here,
+// where two epilogue warps share a scheduler; the single-tile kernels, one epilogue warp
+// per scheduler, measured faster with a straight-line loop.)
+enum ChunkMask { kDrop = 0, kMixed = 1, kKeep = 2 };
+__device__ __forceinline__ int chunk_mask(int j0, int r0)
+{
+    return j0 > r0 + 31 ? kDrop : (j0 + 7 <= r0 ? kKeep : kMixed);
+}
+
+// Keys j0 .. j0+7 of row t, masked (j <= t) and plus `add` (ADD) where kept -> four bf16
+// pairs; the kept fp32 values are added to `sum` (SUM).
+template <bool ADD, bool SUM>
+__device__ __forceinline__ uint4 masked_chunk8(const uint32_t* r, int j0, int t, int cls, float add, float& sum)
+{
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (cls == kKeep) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+            if (ADD) {
+                x0 += add;
+                x1 += add;
+            }
+            if (SUM) sum += x0 + x1;
+            w[e] = pack_bf16(x0, x1);
+        }
+    } else if (cls == kMixed) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = j0 + 2 * e;
+            float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+            if (ADD) {
+                x0 += add;
+                x1 += add;
+            }
+            x0 = j <= t ? x0 : 0.f;
+            x1 = j + 1 <= t ? x1 : 0.f;
+            if (SUM) sum += x0 + x1;
+            w[e] = pack_bf16(x0, x1);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // Named barrier over the 256 epilogue threads (warps 0-7).
 __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -249,6 +298,17 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int kk = 0; kk < KD; ++kk)  // M1: A = Q K^T
                     umma_bf16(tmem + L::T_SC, kstep(dQ, kk), kstep(dK, kk), id_sq, kk > 0);
                 umma_commit(bar_m1);
+                if constexpr (D == 64) {
+                    // the next tile's boxes -> L2 while this one computes (measured: a gain at
+                    // head size 64, a loss at 128, where the tile loads are twice as large)
+                    if (it + 1 < it1) {
+                        const int nb = tile_of(it + 1);
+                        tma_prefetch_3d(&tq, 0, rbase + nb * 128, (int)g);
+                        tma_prefetch_3d(&tk, 0, rbase + nb * 128, (int)g);
+                        tma_prefetch_3d(&tg, 0, rbase + nb * 128, (int)g);
+                        tma_prefetch_3d(&tv, 0, rbase + nb * 128, (int)g);
+                    }
+                }
                 ok = mbar_wait(bar_e1, par, ERR_TIMEOUT_MMA) && mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
                 if (!ok) break;
                 tc_fence_after();
@@ -366,24 +426,28 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_wait(bar_m1, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             float rsum = 0.f;
-            {
+            // this warp's rows are [32 q4, 32 q4 + 32): chunks of keys wholly above them are
+            // zero, wholly below them unmasked (chunk_mask)
+            auto stage_masked = [&](auto add_dd, float dd) {  // add_dd: std::true_type or std::false_type
+                constexpr bool ADD = decltype(add_dd)::value;
+                if (chunk_mask(64 * hh, 32 * q4) == kDrop) {
+#pragma unroll
+                    for (int chunk = 0; chunk < 8; ++chunk)
+                        *reinterpret_cast<uint4*>(sm + L::AD + hh * 16384 + sw_chunk(t, chunk)) =
+                            make_uint4(0, 0, 0, 0);
+                    return;
+                }
                 uint32_t r[64];
                 tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * hh, r);
 #pragma unroll
                 for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * hh + 8 * chunk + 2 * e;
-                        const float x0 = j <= t ? __uint_as_float(r[8 * chunk + 2 * e]) : 0.f;
-                        const float x1 = j + 1 <= t ? __uint_as_float(r[8 * chunk + 2 * e + 1]) : 0.f;
-                        rsum += x0 + x1;
-                        w[e] = pack_bf16(x0, x1);
-                    }
+                    const int j0 = 64 * hh + 8 * chunk;
+                    const int cls = chunk_mask(j0, 32 * q4);
                     *reinterpret_cast<uint4*>(sm + L::AD + hh * 16384 + sw_chunk(t, chunk)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                        masked_chunk8<ADD, !ADD>(r + 8 * chunk, j0, t, cls, dd, rsum);
                 }
-            }
+            };
+            stage_masked(std::false_type{}, 0.f);
             float den = 1.f, inv;
             if (p1) {
                 mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
@@ -469,23 +533,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 dd = parked.y;
             }
             if (hh == 0) ddt[t] = dd;  // for the weighted column sums of pass 2 (read after a barrier)
-            {
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + L::T_SC + 64 * hh, r);
-#pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 64 * hh + 8 * chunk + 2 * e;
-                        const float x0 = (row_ok && j <= t) ? __uint_as_float(r[8 * chunk + 2 * e]) + dd : 0.f;
-                        const float x1 = (row_ok && j + 1 <= t) ? __uint_as_float(r[8 * chunk + 2 * e + 1]) + dd : 0.f;
-                        w[e] = pack_bf16(x0, x1);
-                    }
-                    *reinterpret_cast<uint4*>(sm + L::AD + hh * 16384 + sw_chunk(t, chunk)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
+            // a row past the chunk's end has dN = 0 (so P = 0) and dd = 0: zero unmasked
+            stage_masked(std::true_type{}, dd);
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_e2);
