@@ -380,11 +380,27 @@ def gpu_local_cpus(local):
 # The other workloads (parity cases in tests/), measured the same way as the headline's
 # per-kernel numbers, for context: (name, G, C, D, block, directions)
 OTHER_CONFIGS = (
-    ("batch16_fwdbwd: G=640, C=128, D=64, block=64, bf16", 640, 128, 64, 64, ("fwd", "bwd")),
-    ("long_stream_fwd: G=160, T=8192 as one C=8192 launch, D=64, bf16", 160, 8192, 64, 64, ("fwd",)),
-    ("wide_heads_fwdbwd: G=320, C=256, D=128, block=64, bf16", 320, 256, 128, 64, ("fwd", "bwd")),
-    ("wide_heads_ragged_fwdbwd: G=320, C=200, D=128, block=64, bf16", 320, 200, 128, 64, ("fwd", "bwd")),
+    ("batch16_fwdbwd: G=640, C=128, D=64, block=64, bf16", 640, 128, 64, 64, ("fwd", "bwd"), "chunked"),
+    ("long_stream_fwd: G=160, T=8192 as one C=8192 launch, D=64, bf16", 160, 8192, 64, 64, ("fwd",), "chunked"),
+    ("wide_heads_fwdbwd: G=320, C=256, D=128, block=64, bf16", 320, 256, 128, 64, ("fwd", "bwd"), "chunked"),
+    ("wide_heads_ragged_fwdbwd: G=320, C=200, D=128, block=64, bf16", 320, 200, 128, 64, ("fwd", "bwd"), "chunked"),
+    ("cumsum_form_fwdbwd: G=160, C=128, D=64, bf16, token-by-token scan", 160, 128, 64, 64, ("fwd", "bwd"),
+     "cumsum"),
 )
+
+# The cumsum form runs on the CUDA cores: its bound is fp32 FMA issue, 128 FMA lanes per
+# SM at the maximum SM clock (2 FLOP per FMA).
+FP32_LANES_PER_SM = 128
+MAX_SM_MHZ = 2070.0
+
+
+def cumsum_flop(G, C, D):
+    """Algorithmic FLOP of the cumsum form per launch: each token updates the D x D state
+    and reads it out once per sweep (2 D^2 FMA); the forward makes one sweep, the backward
+    four (n and den; R with dv; S with dq; R with dk).  The length-D sums (z, q.z, r) are
+    left out."""
+    per_sweep = 2 * D * D * 2
+    return G * C * per_sweep, G * C * 4 * per_sweep
 
 
 def measure_other_configs(stream, eps, hbm):
@@ -397,7 +413,9 @@ def measure_other_configs(stream, eps, hbm):
     dev = stream.device
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     out = {}
-    for name, G, C, D, block, dirs in OTHER_CONFIGS:
+    props = torch.cuda.get_device_properties(dev)
+    alu_peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * MAX_SM_MHZ * 1e6 / 1e12  # TFLOP/s
+    for name, G, C, D, block, dirs, impl in OTHER_CONFIGS:
         x = make_inputs(G, C, D, dtype="bf16", seed=rank_seed(0), grads="bwd" in dirs).to(dev)
         fb, bb = algorithmic_bytes(G, C, D, 2)
         nsets = max(1, min(8, -(-4 * l2 // (fb + (bb if "bwd" in dirs else 0)))))
@@ -407,12 +425,20 @@ def measure_other_configs(stream, eps, hbm):
             o = (torch.empty_like(x.q), torch.empty(G, D, D, device=dev), torch.empty(G, D, device=dev))
             gr = (torch.empty_like(x.q), torch.empty_like(x.q), torch.empty_like(x.q), torch.empty(G, D, D, device=dev),
                   torch.empty(G, D, device=dev)) if "bwd" in dirs else None
-            sets.append((d, o, gr))
-        entry = {"G": G, "C": C, "D": D, "block": block}
+            ws = None
+            if impl == "cumsum" and "bwd" in dirs:
+                ws = torch.empty(la.la_cumsum_bwd_workspace_bytes(G, C, D, la.LA_BF16), dtype=torch.uint8, device=dev)
+            sets.append((d, o, gr, ws))
+        entry = {"G": G, "C": C, "D": D, "block": block, "impl": impl}
         for direction in dirs:
             def call(i, direction=direction):
-                d, o, gr = sets[i % nsets]
-                if direction == "fwd":
+                d, o, gr, ws = sets[i % nsets]
+                if impl == "cumsum" and direction == "fwd":
+                    la.cumsum_fwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], eps=eps, o=o[0], S_out=o[1], z_out=o[2])
+                elif impl == "cumsum":
+                    la.cumsum_bwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], d["dO"], d["dS_out"], d["dz_out"],
+                                  eps=eps, out=gr, workspace=ws)
+                elif direction == "fwd":
                     la.chunked_fwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], block=block, eps=eps, o=o[0],
                                    S_out=o[1], z_out=o[2])
                 else:
@@ -440,6 +466,12 @@ def measure_other_configs(stream, eps, hbm):
             byts = fb if direction == "fwd" else bb
             entry[direction] = {"us": round(us, 2), "gbs": round(byts / us / 1e3, 1),
                                 "frac": round(byts / us / 1e3 / hbm, 4)}
+            if impl == "cumsum":
+                flop = cumsum_flop(G, C, D)[0 if direction == "fwd" else 1]
+                tf = flop / us / 1e6
+                entry[direction]["alu"] = {"bound": "alu", "alg_flop": flop, "achieved_tflops": round(tf, 2),
+                                           "peak_tflops": round(alu_peak, 1), "frac": round(tf / alu_peak, 4),
+                                           "peak_source": "SMs x 128 fp32 lanes x 2 x 2070 MHz"}
         secs = sum(entry[d]["us"] for d in dirs) * 1e-6
         entry["value"] = G * C / secs
         entry["unit"] = UNIT + (" (" + "+".join(dirs) + ")")

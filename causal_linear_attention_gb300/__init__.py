@@ -20,12 +20,14 @@ from typing import Optional
 
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_bwd_split_workspace_bytes, la_chunked_bwd,
                    la_chunked_bwd_split, la_chunked_fwd, la_chunked_fwd_split, la_chunked_fwd_split_static,
-                   la_chunked_step_host, la_device_status, la_fwd_split_workspace_bytes,
+                   la_chunked_step_host, la_cumsum_bwd, la_cumsum_bwd_workspace_bytes, la_cumsum_fwd,
+                   la_device_status, la_fwd_split_workspace_bytes,
                    la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
 __all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_bwd_split", "chunked_step_host",
            "step_workspace", "la_chunked_fwd", "la_chunked_fwd_split", "la_chunked_fwd_split_static",
            "la_fwd_split_workspace_bytes", "la_chunked_bwd", "la_chunked_bwd_split", "la_bwd_split_workspace_bytes",
+           "cumsum_fwd", "cumsum_bwd", "la_cumsum_fwd", "la_cumsum_bwd", "la_cumsum_bwd_workspace_bytes",
            "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
@@ -115,6 +117,40 @@ def _bwd_args(q, k, v, S0, z0, dO, dS_out, dz_out, out):
                torch.empty(G, D, D, device=q.device, dtype=torch.float32),
                torch.empty(G, D, device=q.device, dtype=torch.float32))
     return out
+
+
+def cumsum_fwd(q, k, v, S0=None, z0=None, *, eps: float = 1e-6, o=None, S_out=None, z_out=None, stream=None):
+    """The cumsum form of chunked_fwd (token-by-token scan, fp32 state on chip, CUDA
+    cores).  Returns (o, S_out, z_out)."""
+    import torch
+    G, C, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(n, t, q.shape, q.dtype, q.device)
+    for n, t, shp in (("S0", S0, (G, D, D)), ("z0", z0, (G, D))):
+        if t is not None:
+            _check_tensor(n, t, torch.Size(shp), torch.float32, q.device)
+    o = torch.empty_like(q) if o is None else o
+    S_out = torch.empty(G, D, D, device=q.device, dtype=torch.float32) if S_out is None else S_out
+    z_out = torch.empty(G, D, device=q.device, dtype=torch.float32) if z_out is None else z_out
+    la_cumsum_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, _dtype_code(q), eps, _stream(stream))
+    return o, S_out, z_out
+
+
+def cumsum_bwd(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, eps: float = 1e-6, out: Optional[tuple] = None,
+               workspace=None, stream=None):
+    """The cumsum form of chunked_bwd.  `workspace` (a CUDA tensor of at least
+    la_cumsum_bwd_workspace_bytes bytes) is allocated here when not given.  Returns
+    (dq, dk, dv, dS0, dz0)."""
+    import torch
+    G, C, D = q.shape
+    dq, dk, dv, dS0, dz0 = _bwd_args(q, k, v, S0, z0, dO, dS_out, dz_out, out)
+    need = la_cumsum_bwd_workspace_bytes(G, C, D, _dtype_code(q))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    la_cumsum_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, _dtype_code(q), eps, workspace,
+                  wbytes, _stream(stream))
+    return dq, dk, dv, dS0, dz0
 
 
 def chunked_bwd_split(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 64, eps: float = 1e-6,

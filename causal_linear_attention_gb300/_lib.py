@@ -93,6 +93,12 @@ def lib():
         L.la_chunked_fwd_split.restype = I
         L.la_chunked_fwd_split_static.argtypes = [P] * 8 + [I, I, I, I, I, F, P]
         L.la_chunked_fwd_split_static.restype = I
+        L.la_cumsum_fwd.argtypes = [P] * 8 + [I, I, I, I, F, P]
+        L.la_cumsum_fwd.restype = I
+        L.la_cumsum_bwd_workspace_bytes.argtypes = [I, I, I, I]
+        L.la_cumsum_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.la_cumsum_bwd.argtypes = [P] * 13 + [I, I, I, I, F, P, ctypes.c_size_t, P]
+        L.la_cumsum_bwd.restype = I
         L.la_bwd_split_workspace_bytes.argtypes = [I, I, I, I]
         L.la_bwd_split_workspace_bytes.restype = ctypes.c_size_t
         L.la_chunked_bwd_split.argtypes = [P] * 13 + [I, I, I, I, I, F, P, ctypes.c_size_t, P]
@@ -111,6 +117,7 @@ def lib():
 
 EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes", "la_chunked_fwd_split",
            "la_chunked_fwd_split_static", "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
+           "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
            "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
            "la_device_status", "la_selftest_bounded_wait", "la_status_string", "la_version")
 
@@ -153,6 +160,25 @@ def la_chunked_fwd_split(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: in
     """Raw C-ABI call (device pointers or tensors).  Raises LAError on a non-OK status."""
     _check(lib().la_chunked_fwd_split(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(o), _p(S_out), _p(z_out), G, C, D,
                                       block, dtype, eps, _p(workspace), workspace_bytes, _p(stream)))
+
+
+def la_cumsum_fwd(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: int, dtype: int, eps: float,
+                  stream=None) -> None:
+    """Raw C-ABI call of the cumsum form (device pointers or tensors)."""
+    _check(lib().la_cumsum_fwd(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(o), _p(S_out), _p(z_out), G, C, D, dtype, eps,
+                               _p(stream)))
+
+
+def la_cumsum_bwd_workspace_bytes(G: int, C: int, D: int, dtype: int) -> int:
+    return int(lib().la_cumsum_bwd_workspace_bytes(G, C, D, dtype))
+
+
+def la_cumsum_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G: int, C: int, D: int, dtype: int,
+                  eps: float, workspace, workspace_bytes: int, stream=None) -> None:
+    """Raw C-ABI call of the cumsum form's backward."""
+    _check(lib().la_cumsum_bwd(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(dO), _p(dS_out), _p(dz_out), _p(dq), _p(dk),
+                               _p(dv), _p(dS0), _p(dz0), G, C, D, dtype, eps, _p(workspace), workspace_bytes,
+                               _p(stream)))
 
 
 def la_bwd_split_workspace_bytes(G: int, C: int, D: int, dtype: int) -> int:

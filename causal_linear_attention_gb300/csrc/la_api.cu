@@ -21,6 +21,7 @@
 #include "la_fwd_tc128.cuh"
 #include "la_bwd_tcm.cuh"
 #include "la_fwd_split.cuh"
+#include "la_cumsum.cuh"
 
 namespace {
 
@@ -646,6 +647,106 @@ extern "C" la_status la_chunked_bwd_split(const void* q, const void* k, const vo
         if (overlaps(wsb, b)) return LA_ERR_INVALID;
     return bwd_split_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, plan,
                             static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- cumsum form
+namespace {
+
+template <int D, typename T>
+la_status cumsum_fwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                            float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    using Cf = la::CumsumCfg<D>;
+    static OptIn flag;
+    auto kern = la::la_cumsum_fwd_kernel<D, T>;
+    const la_status st = prepare(kern, flag, Cf::SMEM);
+    if (st != LA_OK) return st;
+    return launch_pdl(kern, G, Cf::THREADS, Cf::SMEM, stream, static_cast<const T*>(q), static_cast<const T*>(k),
+                      static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out, z_out, C, eps);
+}
+
+template <int D, typename T>
+la_status cumsum_bwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                            const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv,
+                            float* dS0, float* dz0, int G, int C, float eps, float* ws, cudaStream_t stream)
+{
+    using Cf = la::CumsumCfg<D>;
+    static OptIn fc, fr;
+    auto kc = la::la_cumsum_bwd_col_kernel<D, T>;
+    auto kr = la::la_cumsum_bwd_row_kernel<D, T>;
+    la_status st = prepare(kc, fc, Cf::SMEM);
+    if (st == LA_OK) st = prepare(kr, fr, Cf::SMEM);
+    if (st != LA_OK) return st;
+    float* ws_inv = ws;
+    float* ws_dd = ws + (size_t)G * C;
+    const T* tq = static_cast<const T*>(q);
+    const T* tk = static_cast<const T*>(k);
+    const T* tv = static_cast<const T*>(v);
+    const T* tg = static_cast<const T*>(dO);
+    st = launch_pdl(kc, G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, static_cast<T*>(dv),
+                    ws_inv, ws_dd, C, eps);
+    if (st != LA_OK) return st;
+    // both kernels start R from dS_out; only the second writes dS0 (which may be dS_out)
+    return launch_pdl(kr, G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, dz_out,
+                      static_cast<T*>(dq), static_cast<T*>(dk), dS0, dz0, static_cast<const float*>(ws_inv),
+                      static_cast<const float*>(ws_dd), C);
+}
+
+}  // namespace
+
+extern "C" la_status la_cumsum_fwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                   void* o, float* S_out, float* z_out, int G, int C, int D, la_dtype dtype, float eps,
+                                   void* stream)
+{
+    const la_status st = check_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, 64, dtype, eps);
+    if (st != LA_OK) return st;
+    if (G == 0) return LA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == LA_BF16)
+        return D == 64 ? cumsum_fwd_launch<64, __nv_bfloat16>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s)
+                       : cumsum_fwd_launch<128, __nv_bfloat16>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+    return D == 64 ? cumsum_fwd_launch<64, float>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s)
+                   : cumsum_fwd_launch<128, float>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+}
+
+extern "C" size_t la_cumsum_bwd_workspace_bytes(int G, int C, int D, la_dtype dtype)
+{
+    size_t esz = 0;
+    if (check_common(G, C, D, 64, dtype, 0.f, &esz) != LA_OK) return 0;
+    return (size_t)2 * G * C * 4;
+}
+
+extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                   const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk,
+                                   void* dv, float* dS0, float* dz0, int G, int C, int D, la_dtype dtype, float eps,
+                                   void* workspace, size_t workspace_bytes, void* stream)
+{
+    la_status st = check_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, 64, dtype, eps);
+    if (st != LA_OK) return st;
+    if (G == 0) return LA_OK;
+    const size_t need = (size_t)2 * G * C * 4;
+    if (need > 0) {
+        if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0 || workspace_bytes < need)
+            return LA_ERR_INVALID;
+        const size_t esz = dtype == LA_BF16 ? 2 : 4;
+        const size_t n_x = (size_t)G * C * D * esz, n_S = (size_t)G * D * D * 4, n_z = (size_t)G * D * 4;
+        const Buf wsb = {workspace, need};
+        const Buf all[] = {{q, n_x},      {k, n_x},  {v, n_x},  {S0, n_S},  {z0, n_z},  {dO, n_x},  {dS_out, n_S},
+                           {dz_out, n_z}, {dq, n_x}, {dk, n_x}, {dv, n_x}, {dS0, n_S}, {dz0, n_z}};
+        for (const Buf& b : all)
+            if (overlaps(wsb, b)) return LA_ERR_INVALID;
+    }
+    float* ws = static_cast<float*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == LA_BF16)
+        return D == 64 ? cumsum_bwd_launch<64, __nv_bfloat16>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0,
+                                                              dz0, G, C, eps, ws, s)
+                       : cumsum_bwd_launch<128, __nv_bfloat16>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0,
+                                                               dz0, G, C, eps, ws, s);
+    return D == 64 ? cumsum_bwd_launch<64, float>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C,
+                                                  eps, ws, s)
+                   : cumsum_bwd_launch<128, float>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C,
+                                                   eps, ws, s);
 }
 
 // ---------------------------------------------------------------- host-buffer step

@@ -195,6 +195,41 @@ la_status la_chunked_bwd_split(const void* q, const void* k, const void* v,
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The cumsum form (section 1, "Bottleneck #1"; section 2, "Opt 1"): the same forward and
+ * backward as la_chunked_fwd / la_chunked_bwd, computed as a token-by-token causal cumsum
+ * of the outer products k_t v_t^T (and of k_t) with the state on chip, in fp32 on the CUDA
+ * cores, one CTA per group.  The page materialises that cumsum as a (G, C, D, D) tensor;
+ * this form stores nothing but the carry.  A second implementation beside the chunked
+ * tensor-core kernels (which are faster on this GPU, as the page found on its own).
+ *
+ * la_cumsum_fwd: arguments, layouts, in-place carry and errors as la_chunked_fwd, without
+ * the block size (there are no blocks).  D 64 or 128; float32 or bfloat16; any C >= 0.
+ *
+ * la_cumsum_bwd_workspace_bytes: the device workspace la_cumsum_bwd needs: two float32
+ * values per token (1/den and dd, passed from the first kernel to the second); 0 for an
+ * invalid shape.  No CUDA call.
+ *
+ * la_cumsum_bwd: arguments, layouts, in-place carry gradients and errors as
+ * la_chunked_bwd, without the block size; workspace is caller-owned DEVICE memory,
+ * 16-byte aligned, at least la_cumsum_bwd_workspace_bytes(G, C, D, dtype) bytes and
+ * disjoint from every tensor (LA_ERR_INVALID otherwise; NULL is fine when C = 0).  Two
+ * kernels are enqueued on `stream`; the library allocates nothing.
+ */
+la_status la_cumsum_fwd(const void* q, const void* k, const void* v,
+                        const float* S0, const float* z0,
+                        void* o, float* S_out, float* z_out,
+                        int G, int C, int D, la_dtype dtype, float eps, void* stream);
+
+size_t la_cumsum_bwd_workspace_bytes(int G, int C, int D, la_dtype dtype);
+
+la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
+                        const float* S0, const float* z0,
+                        const void* dO, const float* dS_out, const float* dz_out,
+                        void* dq, void* dk, void* dv, float* dS0, float* dz0,
+                        int G, int C, int D, la_dtype dtype, float eps,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Host-buffer form of one training step of a chunk (forward, then the backward of
  * section 1 on the same inputs), for callers whose tensors start and end in host
  * memory.  The page has no counterpart: its chunked form runs on device tensors.

@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes",
                                            "la_chunked_fwd_split", "la_chunked_fwd_split_static",
                                            "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
+                                           "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
                                            "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
@@ -210,6 +211,40 @@ def test_split_workspace_is_zero_where_no_split_applies(L):
         assert f(2, 4096, 128, la.LA_BF16) == 0
         assert f(2, 128, 64, la.LA_BF16) == 0
         assert f(-1, 4096, 64, la.LA_BF16) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(q=None), INVALID), (dict(o=None), INVALID), (dict(q=A + 4), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED), (dict(o=A), INVALID), (dict(eps=float("nan")), INVALID),
+])
+def test_cumsum_forward_checks_arguments_first(L, kw, status):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, S0=None, z0=None, o=A + 0x300000, S_out=None,
+                z_out=None, G=2, C=8, D=64, dtype=la.LA_BF16, eps=1e-6)
+    args.update(kw)
+    names = ("q", "k", "v", "S0", "z0", "o", "S_out", "z_out", "G", "C", "D", "dtype", "eps")
+    assert L.la_cumsum_fwd(*(args[n] for n in names), None) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(G=-1), INVALID), (dict(dq=None), INVALID), (dict(dk=A + 8), INVALID), (dict(D=48), UNSUPPORTED),
+    (dict(dq=A), INVALID), (dict(workspace=None), INVALID), (dict(workspace_bytes=64), INVALID),
+    (dict(workspace=0x20000008), INVALID), (dict(workspace=A), INVALID),  # misaligned; overlaps q
+])
+def test_cumsum_backward_checks_arguments_first(L, kw, status):
+    base = {n: A + i * 0x100000 for i, n in enumerate(("q", "k", "v", "dO", "dq", "dk", "dv"))}
+    args = dict(base, S0=None, z0=None, dS_out=None, dz_out=None, dS0=None, dz0=None, G=2, C=8, D=64,
+                dtype=la.LA_BF16, eps=1e-6, workspace=0x20000000, workspace_bytes=1 << 20)
+    args.update(kw)
+    names = ("q", "k", "v", "S0", "z0", "dO", "dS_out", "dz_out", "dq", "dk", "dv", "dS0", "dz0", "G", "C", "D",
+             "dtype", "eps", "workspace", "workspace_bytes")
+    assert L.la_cumsum_bwd(*(args[n] for n in names), None) == status
+
+
+def test_cumsum_workspace_bytes_closed_form(L):
+    """Two fp32 values per token: 1/den and dd."""
+    for G, C, D, dt in ((160, 128, 64, 1), (3, 200, 128, 0), (0, 5, 64, 1), (4, 0, 64, 1)):
+        assert la.la_cumsum_bwd_workspace_bytes(G, C, D, dt) == 2 * G * C * 4
+    assert la.la_cumsum_bwd_workspace_bytes(2, 8, 96, 1) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
