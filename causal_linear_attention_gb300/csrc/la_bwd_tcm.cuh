@@ -19,7 +19,7 @@
 //                             M2  P = dN V^T, U = dN S^T (dq accumulator), AV = A V | S += K^T V
 //                             E2  dd -> stash, dA -> shared memory (over A)
 //                             M3  dq += dA K
-//                             E3  dq + dd z -> staging -> TMA store, z += column sums of K,
+//                             E3  dq + dd z -> staging (AD) -> TMA store, z += column sums of K,
 //                                 S -> bf16 operand for the next tile
 //   pass 2 (b = last, ..., 0): M1  A = Q K^T (again)
 //                             E1  mask, dN = dO * stash
@@ -30,7 +30,9 @@
 //                                 operand (dS0, dz0 after tile 0)
 // 1/den and dd of every token wait between the passes in the first 8 bytes of the token's
 // dk row (dk is only written in pass 2, after they have been read back), so the chunk
-// length is not bounded by on-chip memory; pass 2 re-reads the tiles, mostly from L2.
+// length is not bounded by on-chip memory; pass 2 re-reads the tiles, mostly from L2 --
+// except the first, which is the tile pass 1 ended with: pass 1 leaves Q, K, V and dN in
+// place (dq is staged over dA), so it is not loaded again.
 //
 // Piece mode (head size 64; the chunk-parallel backward): the grid has P CTAs per group,
 // CTA (g, p) owning tokens [p PL, (p+1) PL) of group g, and each launch runs ONE pass:
@@ -52,9 +54,8 @@
 //
 // Shared memory (128-byte swizzle; a 128-row tile of D bf16 columns is D/64 atoms of
 // 16 KB; the dynamic base must be 1024-aligned, which is checked):
-//   QT, KT, VT, GN   Q, K, V, dO -> dN (D*256 bytes each); QT stages dq (pass 1) and the
-//                    dS0 tile (after pass 2), KT stages dv, GN stages dk (pass 2)
-//   AD   32768       bf16 A -> dA [i][j] (two 64-key atoms)
+//   QT, KT, VT, GN   Q, K, V, dO -> dN (D*256 bytes each); KT stages dv, GN stages dk (pass 2)
+//   AD   32768       bf16 A -> dA [i][j] (two 64-key atoms); then stages dq (pass 1)
 //   SR   D*D*2       bf16 S (pass 1) / R (pass 2) [p][c]
 //   ZIN, RZ, ZPART   z (pass 1), r (pass 2), per-warp column partial sums
 //   BARS, DDT        mbarriers; dd of the tile's rows
@@ -362,7 +363,14 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 umma_commit(bar_m3);
                 ok = mbar_wait(bar_e3, par, ERR_TIMEOUT_MMA);
-                if (ok && it + 1 < it1) load(tile_of(it + 1));
+                if (ok && it + 1 < it1) {
+                    if (it + 1 == nsb && it0 == 0) {  // pass 2 starts on the tile pass 1 ended with:
+                        mbar_arrive(bar_qk);          // its Q, K, V and dN are still in place
+                        mbar_arrive(bar_vg);
+                    } else {
+                        load(tile_of(it + 1));
+                    }
+                }
             }
         }
     } else {
@@ -472,6 +480,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 inv = parked.x;
             }
             mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
+            if (!(it == nsb && it0 == 0))  // (a tile kept from pass 1 already holds dN)
 #pragma unroll
             for (int c8 = 0; c8 < HCH; ++c8) {  // dO -> dN = dO / den in place
                 uint4* p4 = reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, hh * HCH + c8, 16384));
@@ -597,12 +606,11 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             if (p1) {
-                if (mode == 1) {  // the piece's sum of dd_i q_i, before dq overwrites Q
+                if (mode == 1) {  // the piece's sum of dd_i q_i
                     epi_sync256();  // every row's dd is in ddt
                     column_sums(L::QT, ddt, zpart2);
-                    epi_sync256();  // Q read
                 }
-                // dq = U + dA K + dd z -> staging in QT (Q's last readers, M1 and q . U, are done)
+                // dq = U + dA K + dd z -> staging in AD (dA's last reader, dq += dA K, is done)
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {
                     uint32_t r[32];
@@ -612,7 +620,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         r[j] = __float_as_uint(__uint_as_float(r[j]) + dd * zin[hh * HC + 32 * h2 + j]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(sm + L::QT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
+                        *reinterpret_cast<uint4*>(sm + L::AD + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
                             pack8(r + 8 * q, 1.f);
                 }
                 column_sums(L::KT, nullptr, zpart);  // z after the tile = z + sum_j k_j
@@ -634,7 +642,7 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 epi_sync256();  // dq staging and column partials complete; every dq has read z
                 if (tid == 0) {
 #pragma unroll
-                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdq, sm + L::QT + a * 16384, 64 * a, row0, (int)g);
+                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdq, sm + L::AD + a * 16384, 64 * a, row0, (int)g);
                     tma_store_commit();
                 }
                 if (tid < D) {
