@@ -82,6 +82,70 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """The dense bf16 GEMM rate of MEASURED_PEAKS.json (burst), TFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def measure_chunked_ce(stream):
+    """The chunked cross-entropy of the tied head (N = 512 tokens, V = 50257, d = 1280,
+    bf16; one chunk of 512 and chunks of 128): device time per call of la_ce_fwd and
+    la_ce_bwd, CUDA graphs of 10 calls.  Its binding roofline is the tensor pipe: the GEMM
+    FLOPs (2 N V d forward; the recomputed logits plus dh and dW, 6 N V d, backward)
+    against the measured bf16 dense rate."""
+    import torch
+
+    import causal_linear_attention_gb300 as la
+    from causal_linear_attention_gb300.inputs import CE_SHAPE, make_ce_inputs
+    dev = stream.device
+    N, V, d = CE_SHAPE["N"], CE_SHAPE["V"], CE_SHAPE["d"]
+    h, W, y = (t.to(dev) for t in make_ce_inputs(N, V, d, seed=rank_seed(0)))
+    peak, src = measured_bf16_peak()
+    out = {"N": N, "V": V, "d": d, "dtype": "bf16", "api": "la_ce_fwd / la_ce_bwd (GEMMs on cuBLAS)"}
+    for chunk in (512, 128):
+        ws = la.ce_workspace(N, V, d, chunk, dev)
+        loss = torch.empty((), dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        dh = torch.empty_like(h)
+        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+        calls = {
+            "fwd": lambda: la.la_ce_fwd(h, W, y, N, V, d, chunk, loss, lse, ws, ws.numel(), stream.cuda_stream),
+            "bwd": lambda: la.la_ce_bwd(h, W, y, lse, 1.0, N, V, d, chunk, dh, dW, ws, ws.numel(), stream.cuda_stream),
+        }
+        entry = {}
+        for name, fn in calls.items():
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    fn()
+            torch.cuda.synchronize()
+            n = 10
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                for _ in range(n):
+                    fn()
+            gph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                gph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / n
+            flop = (2 if name == "fwd" else 6) * N * V * d
+            tf = flop / us / 1e6
+            entry[name] = {"us": round(us, 2), "tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+        out[f"ce_chunk={chunk}"] = entry
+        del ws, dW
+    out["roofline"] = {"bound": "tensor", "peak_tflops": peak, "peak_source": src}
+    torch.cuda.empty_cache()
+    return out
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -321,6 +385,8 @@ def run_ours(args, rank, world, local):
         kernels[k]["gbs"] = round(kernels[k]["gbs"], 1)
     fwd_only = job_value(world, G, C, 1, fwd_secs)
     others = measure_other_configs(stream, eps, hbm) if rank == 0 else None
+    if others is not None:
+        others["chunked_ce_fwdbwd: N=512 tokens, V=50257, d=1280, bf16 (tied head)"] = measure_chunked_ce(stream)
 
     out = None
     if rank == 0:

@@ -20,7 +20,8 @@ from typing import Optional
 
 from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_bwd_split_workspace_bytes, la_chunked_bwd,
                    la_chunked_bwd_split, la_chunked_fwd, la_chunked_fwd_split, la_chunked_fwd_split_static,
-                   la_chunked_step_host, la_cumsum_bwd, la_cumsum_bwd_workspace_bytes, la_cumsum_fwd,
+                   la_ce_bwd, la_ce_fwd, la_ce_workspace_bytes, la_chunked_step_host, la_cumsum_bwd,
+                   la_cumsum_bwd_workspace_bytes, la_cumsum_fwd,
                    la_device_status, la_fwd_split_workspace_bytes,
                    la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
@@ -28,6 +29,7 @@ __all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_bwd_split
            "step_workspace", "la_chunked_fwd", "la_chunked_fwd_split", "la_chunked_fwd_split_static",
            "la_fwd_split_workspace_bytes", "la_chunked_bwd", "la_chunked_bwd_split", "la_bwd_split_workspace_bytes",
            "cumsum_fwd", "cumsum_bwd", "la_cumsum_fwd", "la_cumsum_bwd", "la_cumsum_bwd_workspace_bytes",
+           "ce_workspace", "ce_fwd", "ce_bwd", "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
            "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
@@ -117,6 +119,52 @@ def _bwd_args(q, k, v, S0, z0, dO, dS_out, dz_out, out):
                torch.empty(G, D, D, device=q.device, dtype=torch.float32),
                torch.empty(G, D, device=q.device, dtype=torch.float32))
     return out
+
+
+def ce_workspace(N: int, V: int, d: int, ce_chunk: int, device=None):
+    """Device workspace (uint8 CUDA tensor) for ce_fwd / ce_bwd on this shape."""
+    import torch
+    n = la_ce_workspace_bytes(N, V, d, ce_chunk)
+    if n == 0:
+        raise ValueError(f"invalid shape N={N} V={V} d={d} ce_chunk={ce_chunk}")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ce_args(h, W, targets):
+    import torch
+    if h.dim() != 2 or W.dim() != 2 or h.shape[1] != W.shape[1]:
+        raise ValueError(f"h [N, d] and W [V, d] expected, got {tuple(h.shape)} and {tuple(W.shape)}")
+    N, d = h.shape
+    _check_tensor("h", h, h.shape, torch.bfloat16, h.device)
+    _check_tensor("W", W, W.shape, torch.bfloat16, h.device)
+    _check_tensor("targets", targets, torch.Size((N,)), torch.int32, h.device)
+    return N, W.shape[0], d
+
+
+def ce_fwd(h, W, targets, *, ce_chunk: int = 512, workspace=None, stream=None):
+    """Chunked cross-entropy of the tied head: returns (loss (0-d float32 tensor), lse [N])."""
+    import torch
+    N, V, d = _ce_args(h, W, targets)
+    if workspace is None:
+        workspace = ce_workspace(N, V, d, ce_chunk, h.device)
+    loss = torch.empty((), dtype=torch.float32, device=h.device)
+    lse = torch.empty(N, dtype=torch.float32, device=h.device)
+    la_ce_fwd(h, W, targets, N, V, d, ce_chunk, loss, lse, workspace, workspace.numel(), _stream(stream))
+    return loss, lse
+
+
+def ce_bwd(h, W, targets, lse, dloss: float = 1.0, *, ce_chunk: int = 512, workspace=None, stream=None):
+    """Gradients of dloss * ce_fwd's loss: returns (dh bf16 [N, d], dW float32 [V, d])."""
+    import torch
+    N, V, d = _ce_args(h, W, targets)
+    _check_tensor("lse", lse, torch.Size((N,)), torch.float32, h.device)
+    if workspace is None:
+        workspace = ce_workspace(N, V, d, ce_chunk, h.device)
+    dh = torch.empty_like(h)
+    dW = torch.empty(V, d, dtype=torch.float32, device=h.device)
+    la_ce_bwd(h, W, targets, lse, float(dloss), N, V, d, ce_chunk, dh, dW, workspace, workspace.numel(),
+              _stream(stream))
+    return dh, dW
 
 
 def cumsum_fwd(q, k, v, S0=None, z0=None, *, eps: float = 1e-6, o=None, S_out=None, z_out=None, stream=None):

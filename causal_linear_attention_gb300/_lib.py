@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(["nvcc", ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
-                    *objs, "-o", tmp], check=True)
+                    *objs, "-lcublas", "-o", tmp], check=True)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 
@@ -93,6 +93,12 @@ def lib():
         L.la_chunked_fwd_split.restype = I
         L.la_chunked_fwd_split_static.argtypes = [P] * 8 + [I, I, I, I, I, F, P]
         L.la_chunked_fwd_split_static.restype = I
+        L.la_ce_workspace_bytes.argtypes = [I, I, I, I]
+        L.la_ce_workspace_bytes.restype = ctypes.c_size_t
+        L.la_ce_fwd.argtypes = [P, P, P, I, I, I, I, P, P, P, ctypes.c_size_t, P]
+        L.la_ce_fwd.restype = I
+        L.la_ce_bwd.argtypes = [P, P, P, P, F, I, I, I, I, P, P, P, ctypes.c_size_t, P]
+        L.la_ce_bwd.restype = I
         L.la_cumsum_fwd.argtypes = [P] * 8 + [I, I, I, I, F, P]
         L.la_cumsum_fwd.restype = I
         L.la_cumsum_bwd_workspace_bytes.argtypes = [I, I, I, I]
@@ -118,6 +124,7 @@ def lib():
 EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes", "la_chunked_fwd_split",
            "la_chunked_fwd_split_static", "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
            "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
+           "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
            "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
            "la_device_status", "la_selftest_bounded_wait", "la_status_string", "la_version")
 
@@ -160,6 +167,24 @@ def la_chunked_fwd_split(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: in
     """Raw C-ABI call (device pointers or tensors).  Raises LAError on a non-OK status."""
     _check(lib().la_chunked_fwd_split(_p(q), _p(k), _p(v), _p(S0), _p(z0), _p(o), _p(S_out), _p(z_out), G, C, D,
                                       block, dtype, eps, _p(workspace), workspace_bytes, _p(stream)))
+
+
+def la_ce_workspace_bytes(N: int, V: int, d: int, ce_chunk: int) -> int:
+    return int(lib().la_ce_workspace_bytes(N, V, d, ce_chunk))
+
+
+def la_ce_fwd(h, W, targets, N: int, V: int, d: int, ce_chunk: int, loss, lse, workspace, workspace_bytes: int,
+              stream=None) -> None:
+    """Raw C-ABI call of the chunked cross-entropy forward (device pointers or tensors)."""
+    _check(lib().la_ce_fwd(_p(h), _p(W), _p(targets), N, V, d, ce_chunk, _p(loss), _p(lse), _p(workspace),
+                           workspace_bytes, _p(stream)))
+
+
+def la_ce_bwd(h, W, targets, lse, dloss: float, N: int, V: int, d: int, ce_chunk: int, dh, dW, workspace,
+              workspace_bytes: int, stream=None) -> None:
+    """Raw C-ABI call of the chunked cross-entropy backward."""
+    _check(lib().la_ce_bwd(_p(h), _p(W), _p(targets), _p(lse), dloss, N, V, d, ce_chunk, _p(dh), _p(dW),
+                           _p(workspace), workspace_bytes, _p(stream)))
 
 
 def la_cumsum_fwd(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int, D: int, dtype: int, eps: float,

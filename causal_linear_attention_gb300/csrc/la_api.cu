@@ -4,6 +4,7 @@
 // two CTAs ever touch the same output element and results are bitwise reproducible.
 #include "la.h"
 
+#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -12,6 +13,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <utility>
 
 #include "la_bwd.cuh"
@@ -22,6 +24,7 @@
 #include "la_bwd_tcm.cuh"
 #include "la_fwd_split.cuh"
 #include "la_cumsum.cuh"
+#include "la_ce.cuh"
 
 namespace {
 
@@ -71,11 +74,11 @@ la_status launched()
 // the previous kernel in the stream drains, runs its set-up (barriers, TMEM, constant
 // tiles), and waits in griddepcontrol.wait before it reads any input.
 template <class... KArgs, class... Args>
-la_status launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem, cudaStream_t stream,
+la_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t stream,
                      Args&&... args)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -747,6 +750,197 @@ extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, 
                                                   eps, ws, s)
                    : cumsum_bwd_launch<128, float>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C,
                                                    eps, ws, s);
+}
+
+// ---------------------------------------------------------------- chunked cross-entropy
+namespace {
+
+constexpr size_t kCeAlign = 256;
+constexpr size_t kCublasWsBytes = (size_t)32 << 20;  // cuBLAS's workspace, carved from the caller's
+
+size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
+
+// Token stride of the chunk's vocabulary-major logits and gradient: the chunk rounded up
+// to 32 tokens (one warp's lanes in the row kernels; 128-byte rows for the GEMMs).
+int ce_tstride(int cc) { return (cc + 31) / 32 * 32; }
+int ce_slices(int V) { return (V + la::CE_SLICE - 1) / la::CE_SLICE; }
+
+// Workspace slots: the chunk's fp32 logits LT [V][cs], its bf16 gradient GT [V][cs], the
+// per-token loss terms [N], the log-sum-exp partials pm, ps [slices][cs] and the target
+// logits [cs], cuBLAS's workspace.
+size_t ce_layout(int N, int V, int cc, size_t off[7])
+{
+    const size_t cs = (size_t)ce_tstride(cc), ns = (size_t)ce_slices(V);
+    const size_t sizes[7] = {(size_t)V * cs * 4, (size_t)V * cs * 2, (size_t)N * 4, ns * cs * 4, ns * cs * 4,
+                             cs * 4, kCublasWsBytes};
+    size_t o = 0;
+    for (int i = 0; i < 7; ++i) {
+        off[i] = o;
+        o += ce_round(sizes[i]);
+    }
+    return o;
+}
+
+// One cuBLAS handle per device, made on first use (cuBLAS keeps a little device state of
+// its own for it); calls that use it hold its lock while they enqueue, so the stream and
+// workspace it is given are theirs.
+struct CublasSlot {
+    std::mutex mu;
+    cublasHandle_t h = nullptr;
+};
+CublasSlot g_cublas[kMaxDevices];
+
+la_status ce_check(const void* h, const void* W, const int* targets, int N, int V, int d, int ce_chunk,
+                   const void* workspace, size_t workspace_bytes, size_t* need)
+{
+    if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0) return LA_ERR_INVALID;
+    if (N == 0) return LA_OK;
+    if (!h || !W || !targets) return LA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(h) % 16 || reinterpret_cast<uintptr_t>(W) % 16 ||
+        reinterpret_cast<uintptr_t>(targets) % 4)
+        return LA_ERR_INVALID;
+    size_t off[7];
+    *need = ce_layout(N, V, std::min(ce_chunk, N), off);
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kCeAlign || workspace_bytes < *need)
+        return LA_ERR_INVALID;
+    const Buf wsb = {workspace, *need};
+    const Buf ins[] = {{h, (size_t)N * d * 2}, {W, (size_t)V * d * 2}, {targets, (size_t)N * 4}};
+    for (const Buf& b : ins)
+        if (overlaps(wsb, b)) return LA_ERR_INVALID;
+    return LA_OK;
+}
+
+// A locked cuBLAS handle on `stream` with the caller's workspace slot
+struct CublasUse {
+    std::unique_lock<std::mutex> lock;
+    cublasHandle_t h = nullptr;
+    bool ok = false;
+    CublasUse(cudaStream_t stream, void* ws)
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) {
+            cudaGetLastError();
+            return;
+        }
+        lock = std::unique_lock<std::mutex>(g_cublas[dev].mu);
+        if (!g_cublas[dev].h && cublasCreate(&g_cublas[dev].h) != CUBLAS_STATUS_SUCCESS) {
+            g_cublas[dev].h = nullptr;
+            return;
+        }
+        h = g_cublas[dev].h;
+        ok = cublasSetStream(h, stream) == CUBLAS_STATUS_SUCCESS &&
+             cublasSetWorkspace(h, ws, kCublasWsBytes) == CUBLAS_STATUS_SUCCESS &&
+             cublasSetMathMode(h, CUBLAS_DEFAULT_MATH) == CUBLAS_STATUS_SUCCESS;
+    }
+};
+
+// LT[V][cs] (fp32, vocabulary-major: LT[j][i] = logits[i][j]) = W h_c^T for the chunk's nc
+// tokens (column-major: op_T(h_c) . W -> nc x V, ld cs)
+bool ce_logits(cublasHandle_t hb, const void* hc, const void* W, float* LT, int nc, int cs, int V, int d)
+{
+    const float one = 1.f, zero = 0.f;
+    return cublasGemmEx(hb, CUBLAS_OP_T, CUBLAS_OP_N, nc, V, d, &one, hc, CUDA_R_16BF, d, W, CUDA_R_16BF, d, &zero,
+                        LT, CUDA_R_32F, cs, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk)
+{
+    if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0) return 0;
+    size_t off[7];
+    return ce_layout(N, V, std::min(ce_chunk, std::max(N, 1)), off);
+}
+
+extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets, int N, int V, int d, int ce_chunk,
+                               float* loss, float* lse, void* workspace, size_t workspace_bytes, void* stream)
+{
+    size_t need = 0;
+    la_status st = ce_check(h, W, targets, N, V, d, ce_chunk, workspace, workspace_bytes, &need);
+    if (st != LA_OK) return st;
+    if (!loss || (N > 0 && !lse)) return LA_ERR_INVALID;
+    {
+        const Buf outs[] = {{loss, 4}, {lse, (size_t)N * 4}};
+        const Buf ins[] = {{h, (size_t)N * d * 2}, {W, (size_t)V * d * 2}, {targets, (size_t)N * 4}, {workspace, need}};
+        const int inplace[] = {-1, -1};
+        if (!disjoint(outs, 2, ins, 4, inplace)) return LA_ERR_INVALID;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) return cudaMemsetAsync(loss, 0, sizeof(float), s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc), ns = ce_slices(V);
+    size_t off[7];
+    ce_layout(N, V, cc, off);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    float* LT = reinterpret_cast<float*>(ws + off[0]);
+    float* row_loss = reinterpret_cast<float*>(ws + off[2]);
+    float* pm = reinterpret_cast<float*>(ws + off[3]);
+    float* ps = reinterpret_cast<float*>(ws + off[4]);
+    float* tl = reinterpret_cast<float*>(ws + off[5]);
+    {
+        CublasUse cb(s, ws + off[6]);
+        if (!cb.ok) return LA_ERR_CUDA;
+        for (int c0 = 0; c0 < N; c0 += cc) {
+            const int nc = std::min(cc, N - c0);
+            if (!ce_logits(cb.h, static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d, W, LT, nc, cs, V, d))
+                return LA_ERR_CUDA;
+            st = launch_pdl(la::la_ce_lse_part_kernel, dim3((nc + la::CE_TOK - 1) / la::CE_TOK, ns),
+                            la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0, pm,
+                            ps, tl);
+            if (st != LA_OK) return st;
+            st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
+                            static_cast<const float*>(ps), static_cast<const float*>(tl), ns, nc, cs, V, targets + c0,
+                            lse + c0, row_loss + c0);
+            if (st != LA_OK) return st;
+        }
+    }
+    return launch_pdl(la::la_ce_mean_kernel, 1, 1024, 0, s, static_cast<const float*>(row_loss), N, loss);
+}
+
+extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets, const float* lse, float dloss,
+                               int N, int V, int d, int ce_chunk, void* dh, float* dW, void* workspace,
+                               size_t workspace_bytes, void* stream)
+{
+    size_t need = 0;
+    la_status st = ce_check(h, W, targets, N, V, d, ce_chunk, workspace, workspace_bytes, &need);
+    if (st != LA_OK) return st;
+    if (!dW || !std::isfinite(dloss) || (N > 0 && (!lse || !dh))) return LA_ERR_INVALID;
+    const Buf outs[] = {{dh, (size_t)N * d * 2}, {dW, (size_t)V * d * 4}};
+    const Buf ins[] = {{h, (size_t)N * d * 2}, {W, (size_t)V * d * 2}, {targets, (size_t)N * 4},
+                       {lse, (size_t)N * 4}, {workspace, need}};
+    const int inplace[] = {-1, -1};
+    if (!disjoint(outs, 2, ins, 5, inplace)) return LA_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) return cudaMemsetAsync(dW, 0, (size_t)V * d * 4, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc);
+    size_t off[7];
+    ce_layout(N, V, cc, off);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    float* LT = reinterpret_cast<float*>(ws + off[0]);
+    __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[1]);
+    CublasUse cb(s, ws + off[6]);
+    if (!cb.ok) return LA_ERR_CUDA;
+    const float one = 1.f, zero = 0.f, scale = dloss / (float)N;
+    for (int c0 = 0; c0 < N; c0 += cc) {
+        const int nc = std::min(cc, N - c0);
+        const __nv_bfloat16* hc = static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d;
+        if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed
+        constexpr int rows_per_cta = la::CE_ROWS * la::CE_GRAD_ROWS;
+        st = launch_pdl(la::la_ce_grad_kernel, dim3(cs / la::CE_TOK, (V + rows_per_cta - 1) / rows_per_cta),
+                        la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0,
+                        lse + c0, scale, GT);
+        if (st != LA_OK) return st;
+        // dh_c[nc][d] = G W  (column-major: W (d x V) . op_T(GT) (V x nc))
+        if (cublasGemmEx(cb.h, CUBLAS_OP_N, CUBLAS_OP_T, d, nc, V, &one, W, CUDA_R_16BF, d, GT, CUDA_R_16BF, cs, &zero,
+                         static_cast<__nv_bfloat16*>(dh) + (size_t)c0 * d, CUDA_R_16BF, d, CUBLAS_COMPUTE_32F,
+                         CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+            return LA_ERR_CUDA;
+        // dW[V][d] (+)= G^T h_c  (column-major: h_c (d x nc) . GT (nc x V))
+        if (cublasGemmEx(cb.h, CUBLAS_OP_N, CUBLAS_OP_N, d, V, nc, &one, hc, CUDA_R_16BF, d, GT, CUDA_R_16BF, cs,
+                         c0 == 0 ? &zero : &one, dW, CUDA_R_32F, d, CUBLAS_COMPUTE_32F,
+                         CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+            return LA_ERR_CUDA;
+    }
+    return LA_OK;
 }
 
 // ---------------------------------------------------------------- host-buffer step

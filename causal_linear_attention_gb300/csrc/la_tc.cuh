@@ -16,7 +16,8 @@ enum : uint32_t {
     ERR_TIMEOUT_TMA = 1u,   // an mbarrier wait for a TMA load gave up
     ERR_TIMEOUT_MMA = 2u,   // an mbarrier wait for tcgen05.commit gave up
     ERR_TIMEOUT_STORE = 4u, // waiting for TMA stores to drain gave up
-    ERR_SMEM_ALIGN = 8u     // dynamic shared memory was not 1024-byte aligned: the kernel did nothing
+    ERR_SMEM_ALIGN = 8u,    // dynamic shared memory was not 1024-byte aligned: the kernel did nothing
+    ERR_BAD_TARGET = 16u    // a cross-entropy target outside [0, V): its row's loss is NaN
 };
 constexpr uint32_t kTimeoutBits = ERR_TIMEOUT_TMA | ERR_TIMEOUT_MMA | ERR_TIMEOUT_STORE;
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms of %globaltimer per wait

@@ -86,3 +86,19 @@ CONFIGS = {
     "long_stream": dict(G=160, C=128, D=64, block=64, dtype="bf16", eps=1e-6, chunks=64),
     "wide_d128": dict(G=320, C=256, D=128, block=64, dtype="bf16", eps=1e-6),
 }
+
+
+# The tied head of the Fractus-1B model: d_model 1280 (64.3M MACs per token over a
+# 50257-token vocabulary), 512 tokens per training tick (B = 4 sequences of 128).
+CE_SHAPE = dict(N=512, V=50257, d=1280)
+
+
+def make_ce_inputs(N: int, V: int, d: int, seed: int = 0):
+    """Hidden rows h ~ N(0, 1) and a head W ~ N(0, 0.02^2), both rounded to bfloat16,
+    and targets uniform in [0, V) (int32).  Logits h . W_j then have a standard deviation
+    near 0.02 sqrt(d) (0.7 at d = 1280).  Returns (h, W, targets) on the CPU."""
+    gen = torch.Generator().manual_seed(int(seed))
+    h = torch.randn(N, d, generator=gen).to(torch.bfloat16).contiguous()
+    W = (0.02 * torch.randn(V, d, generator=gen)).to(torch.bfloat16).contiguous()
+    y = torch.randint(0, V, (N,), generator=gen, dtype=torch.int64).to(torch.int32).contiguous()
+    return h, W, y

@@ -66,8 +66,9 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,  /* a valid but unsupported D, block, dtype or C */
     LA_ERR_CUDA = 3,         /* the CUDA launch failed */
     LA_ERR_TIMEOUT = 4,      /* a bounded on-device wait gave up (from la_device_status) */
-    LA_ERR_DEVICE = 5        /* a kernel found its launch unusable and wrote nothing
-                                (from la_device_status) */
+    LA_ERR_DEVICE = 5        /* a kernel found its launch unusable and wrote nothing, or
+                                found an invalid input value (a cross-entropy target
+                                outside [0, V)) (from la_device_status) */
 } la_status;
 
 /*
@@ -228,6 +229,45 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
                         void* dq, void* dk, void* dv, float* dS0, float* dz0,
                         int G, int C, int D, la_dtype dtype, float eps,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Chunked cross-entropy over a tied vocabulary head (section 1, "Bottleneck #3"; section
+ * 2, "Opt 3"): for N tokens with hidden rows h_i (bfloat16 [N][d]), the head W (bfloat16
+ * [V][d], V = 50257 on the page) and integer targets y_i in [0, V):
+ *     logits[i][j] = h_i . W_j,  lse_i = log sum_j exp(logits[i][j]),
+ *     loss = (1/N) sum_i (lse_i - logits[i][y_i]),
+ * computed ce_chunk tokens at a time so that only one chunk's logits (fp32) exist at once;
+ * the backward recomputes them.  The contractions run on cuBLAS (bf16 in, fp32
+ * accumulate; a plain library GEMM), the row work (log-sum-exp, target logit, the softmax
+ * gradient) on this library's kernels.
+ *
+ * la_ce_workspace_bytes: the device workspace both calls need: the chunk's fp32 logits and
+ * bf16 gradient, vocabulary-major with the chunk padded to 32 tokens (6 bytes per logit),
+ * N floats, the log-sum-exp partials (2 floats per token and 1024-row vocabulary slice)
+ * and a 32 MiB GEMM workspace, each at a 256-byte boundary; 0 for a negative or zero
+ * size.  No CUDA call.
+ *
+ * la_ce_fwd: loss (one float, device) and lse ([N] float32, device; the backward's input).
+ * la_ce_bwd: dloss is the gradient reaching the loss (1 for a plain mean loss); writes dh
+ * (bfloat16 [N][d]) and dW (float32 [V][d], overwritten: the gradient of this call alone).
+ *
+ * All pointers are device memory: h, W 16-byte aligned, targets 4-byte aligned, the
+ * workspace 256-byte aligned, at least la_ce_workspace_bytes(N, V, d, ce_chunk) bytes and
+ * disjoint from every tensor; outputs disjoint from inputs (LA_ERR_INVALID otherwise).
+ * N = 0 writes loss = 0 (forward) or dW = 0 (backward).  A target outside [0, V) gives its
+ * row a NaN loss and makes la_device_status report LA_ERR_DEVICE.  Asynchronous on
+ * `stream`; the library allocates nothing itself, but cuBLAS keeps one handle per device,
+ * made on the first call (make that call outside any stream capture), which calls share
+ * under a lock while they enqueue.
+ */
+size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk);
+
+la_status la_ce_fwd(const void* h, const void* W, const int* targets, int N, int V, int d, int ce_chunk,
+                    float* loss, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+la_status la_ce_bwd(const void* h, const void* W, const int* targets, const float* lse, float dloss,
+                    int N, int V, int d, int ce_chunk, void* dh, float* dW,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Host-buffer form of one training step of a chunk (forward, then the backward of

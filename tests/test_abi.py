@@ -32,6 +32,7 @@ def test_header_declares_the_boundary():
                                            "la_chunked_fwd_split", "la_chunked_fwd_split_static",
                                            "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
                                            "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
+                                           "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
                                            "la_step_workspace_bytes",
                                            "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
@@ -245,6 +246,49 @@ def test_cumsum_workspace_bytes_closed_form(L):
     for G, C, D, dt in ((160, 128, 64, 1), (3, 200, 128, 0), (0, 5, 64, 1), (4, 0, 64, 1)):
         assert la.la_cumsum_bwd_workspace_bytes(G, C, D, dt) == 2 * G * C * 4
     assert la.la_cumsum_bwd_workspace_bytes(2, 8, 96, 1) == 0
+
+
+def test_ce_workspace_bytes_closed_form(L):
+    """One chunk's vocabulary-major fp32 logits and bf16 gradient (the chunk padded to 32
+    tokens), N floats, two [slices][chunk] partial arrays (slices of 1024 vocabulary rows),
+    the chunk's target logits and a 32 MiB GEMM workspace, each rounded up to 256 bytes;
+    the chunk is at most N tokens."""
+    r = lambda n: (n + 255) // 256 * 256
+    for N, V, d, cc in ((512, 50257, 1280, 512), (512, 50257, 1280, 128), (300, 1000, 128, 1000), (1, 7, 8, 4)):
+        cs, ns = (min(cc, N) + 31) // 32 * 32, (V + 1023) // 1024
+        want = r(V * cs * 4) + r(V * cs * 2) + r(N * 4) + 2 * r(ns * cs * 4) + r(cs * 4) + (32 << 20)
+        assert la.la_ce_workspace_bytes(N, V, d, cc) == want
+    assert la.la_ce_workspace_bytes(-1, 5, 5, 5) == 0
+    assert la.la_ce_workspace_bytes(5, 0, 5, 5) == 0
+    assert la.la_ce_workspace_bytes(5, 5, 5, 0) == 0
+
+
+def ce_call(fwd=True, **kw):
+    WS = 0x40000000
+    args = dict(h=A, W=A + 0x100000, targets=A + 0x200000, lse=A + 0x300000, loss=A + 0x400000,
+                dh=A + 0x500000, dW=A + 0x600000, N=4, V=16, d=8, ce_chunk=4, workspace=WS, workspace_bytes=1 << 30)
+    args.update(kw)
+    L = la.lib()
+    if fwd:
+        return L.la_ce_fwd(args["h"], args["W"], args["targets"], args["N"], args["V"], args["d"], args["ce_chunk"],
+                           args["loss"], args["lse"], args["workspace"], args["workspace_bytes"], None)
+    return L.la_ce_bwd(args["h"], args["W"], args["targets"], args["lse"], 1.0, args["N"], args["V"], args["d"],
+                       args["ce_chunk"], args["dh"], args["dW"], args["workspace"], args["workspace_bytes"], None)
+
+
+@pytest.mark.parametrize("fwd", [True, False])
+@pytest.mark.parametrize("kw", [dict(N=-1), dict(V=0), dict(d=0), dict(ce_chunk=0), dict(h=None), dict(W=None),
+                                dict(targets=None), dict(h=A + 8), dict(targets=A + 0x200002), dict(workspace=None),
+                                dict(workspace=0x40000010), dict(workspace_bytes=1000), dict(workspace=A)])
+def test_ce_checks_arguments_first(L, fwd, kw):
+    assert ce_call(fwd, **kw) == INVALID
+
+
+def test_ce_output_checks(L):
+    assert ce_call(True, loss=None) == INVALID
+    assert ce_call(True, lse=A) == INVALID          # lse over h
+    assert ce_call(False, dh=None) == INVALID
+    assert ce_call(False, dW=A + 0x100000) == INVALID  # dW over W
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
