@@ -763,7 +763,16 @@ size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 // Token stride of the chunk's vocabulary-major logits and gradient: the chunk rounded up
 // to 32 tokens (one warp's lanes in the row kernels; 128-byte rows for the GEMMs).
 int ce_tstride(int cc) { return (cc + 31) / 32 * 32; }
-int ce_slices(int V) { return (V + la::CE_SLICE - 1) / la::CE_SLICE; }
+// log-sum-exp partial slots per token: one per 128-row vocabulary tile of the fused GEMM
+// (the row-kernel path, 1024-row slices, uses the first eighth of them)
+int ce_slices(int V) { return (V + la::CeGemmLayout::BN - 1) / la::CeGemmLayout::BN; }
+bool ce_fused(int d) { return d % la::CeGemmLayout::BK == 0; }
+
+// Maps for the fused GEMM: h [N][d] and W [V][d] in 128-row boxes.
+bool ce_maps(const void* h, const void* W, int N, int V, int d, CUtensorMap* th, CUtensorMap* tw)
+{
+    return tmap_bf16(th, h, 1, N, d, la::CeGemmLayout::BM) && tmap_bf16(tw, W, 1, V, d, la::CeGemmLayout::BN);
+}
 
 // Workspace slots: the chunk's fp32 logits LT [V][cs], its bf16 gradient GT [V][cs], the
 // per-token loss terms [N], the log-sum-exp partials pm, ps [slices][cs] and the target
@@ -876,19 +885,38 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
     float* pm = reinterpret_cast<float*>(ws + off[3]);
     float* ps = reinterpret_cast<float*>(ws + off[4]);
     float* tl = reinterpret_cast<float*>(ws + off[5]);
-    {
+    if (ce_fused(d)) {  // logits on the tensor core, the log-sum-exp from TMEM
+        static OptIn flag;
+        auto kern = la::la_ce_logits_lse_kernel;
+        st = prepare(kern, flag, la::CeGemmLayout::BYTES);
+        if (st != LA_OK) return st;
+        CUtensorMap th{}, tw{};
+        if (!ce_maps(h, W, N, V, d, &th, &tw)) return LA_ERR_CUDA;
+        for (int c0 = 0; c0 < N; c0 += cc) {
+            const int nc = std::min(cc, N - c0);
+            st = launch_pdl(kern, dim3((nc + la::CeGemmLayout::BM - 1) / la::CeGemmLayout::BM, ns),
+                            la::CeGemmLayout::THREADS, la::CeGemmLayout::BYTES, s, th, tw, c0, nc, cs, V,
+                            d / la::CeGemmLayout::BK, targets + c0, pm, ps, tl);
+            if (st != LA_OK) return st;
+            st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
+                            static_cast<const float*>(ps), static_cast<const float*>(tl), ns, nc, cs, V, targets + c0,
+                            lse + c0, row_loss + c0);
+            if (st != LA_OK) return st;
+        }
+    } else {
+        const int nsr = (V + la::CE_SLICE - 1) / la::CE_SLICE;
         CublasUse cb(s, ws + off[6]);
         if (!cb.ok) return LA_ERR_CUDA;
         for (int c0 = 0; c0 < N; c0 += cc) {
             const int nc = std::min(cc, N - c0);
             if (!ce_logits(cb.h, static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d, W, LT, nc, cs, V, d))
                 return LA_ERR_CUDA;
-            st = launch_pdl(la::la_ce_lse_part_kernel, dim3((nc + la::CE_TOK - 1) / la::CE_TOK, ns),
+            st = launch_pdl(la::la_ce_lse_part_kernel, dim3((nc + la::CE_TOK - 1) / la::CE_TOK, nsr),
                             la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0, pm,
                             ps, tl);
             if (st != LA_OK) return st;
             st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
-                            static_cast<const float*>(ps), static_cast<const float*>(tl), ns, nc, cs, V, targets + c0,
+                            static_cast<const float*>(ps), static_cast<const float*>(tl), nsr, nc, cs, V, targets + c0,
                             lse + c0, row_loss + c0);
             if (st != LA_OK) return st;
         }
