@@ -106,7 +106,8 @@ def measure_chunked_ce(stream):
     h, W, y = (t.to(dev) for t in make_ce_inputs(N, V, d, seed=rank_seed(0)))
     peak, src = measured_bf16_peak()
     out = {"N": N, "V": V, "d": d, "dtype": "bf16",
-           "api": "la_ce_fwd (logits + log-sum-exp on this library's tcgen05 kernel) / la_ce_bwd (GEMMs on cuBLAS)"}
+           "api": "la_ce_fwd / la_ce_bwd (logits on this library's tcgen05 kernel with the log-sum-exp or the "
+                  "gradient in its epilogue; dh, dW on cuBLAS)"}
     for chunk in (512, 128):
         ws = la.ce_workspace(N, V, d, chunk, dev)
         loss = torch.empty((), dtype=torch.float32, device=dev)

@@ -763,25 +763,44 @@ size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 // Token stride of the chunk's vocabulary-major logits and gradient: the chunk rounded up
 // to 32 tokens (one warp's lanes in the row kernels; 128-byte rows for the GEMMs).
 int ce_tstride(int cc) { return (cc + 31) / 32 * 32; }
-// log-sum-exp partial slots per token: one per 128-row vocabulary tile of the fused GEMM
-// (the row-kernel path, 1024-row slices, uses the first eighth of them)
-int ce_slices(int V) { return (V + la::CeGemmLayout::BN - 1) / la::CeGemmLayout::BN; }
-bool ce_fused(int d) { return d % la::CeGemmLayout::BK == 0; }
+// log-sum-exp partial slots per token: one per 256-row vocabulary tile of the fused GEMM
+// (the row-kernel path, 1024-row slices, uses the first quarter of them)
+int ce_slices(int V) { return (V + la::CePersistLayout::BN - 1) / la::CePersistLayout::BN; }
+// d a multiple of 64: the logits on this library's tensor-core kernel, never in memory
+bool ce_fused(int d) { return d % la::CePersistLayout::BK == 0; }
 
-// Maps for the fused GEMM: h [N][d] and W [V][d] in 128-row boxes.
+// Maps for the fused GEMM: h [N][d] in 128-row boxes, W [V][d] in 256-row boxes.
 bool ce_maps(const void* h, const void* W, int N, int V, int d, CUtensorMap* th, CUtensorMap* tw)
 {
-    return tmap_bf16(th, h, 1, N, d, la::CeGemmLayout::BM) && tmap_bf16(tw, W, 1, V, d, la::CeGemmLayout::BN);
+    return tmap_bf16(th, h, 1, N, d, la::CePersistLayout::BM) && tmap_bf16(tw, W, 1, V, d, la::CePersistLayout::BN);
 }
 
-// Workspace slots: the chunk's fp32 logits LT [V][cs], its bf16 gradient GT [V][cs], the
-// per-token loss terms [N], the log-sum-exp partials pm, ps [slices][cs] and the target
-// logits [cs], cuBLAS's workspace.
-size_t ce_layout(int N, int V, int cc, size_t off[7])
+// The persistent fused GEMM over a chunk: one CTA per SM (at most one per tile).
+template <int MODE>
+la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, int c0, int nc, int cs, int V, int d,
+                            const int* y, float* pm, float* ps, float* tl, const float* lse, float scale,
+                            __nv_bfloat16* GT, cudaStream_t s)
+{
+    using PL = la::CePersistLayout;
+    static OptIn flag;
+    auto kern = la::la_ce_persist_kernel<MODE>;
+    const la_status st = prepare(kern, flag, PL::BYTES);
+    if (st != LA_OK) return st;
+    const int mtiles = ((MODE == 0 ? nc : cs) + PL::BM - 1) / PL::BM, ntiles = (V + PL::BN - 1) / PL::BN;
+    const int sms = sm_count();
+    if (sms <= 0) return LA_ERR_CUDA;
+    return launch_pdl(kern, std::min(mtiles * ntiles, sms), PL::THREADS, PL::BYTES, s, th, tw, c0, nc, cs, V,
+                      d / PL::BK, mtiles, ntiles, y, pm, ps, tl, lse, scale, GT);
+}
+
+// Workspace slots: the chunk's fp32 logits LT [V][cs] (only without the fused GEMM), its
+// bf16 gradient GT [V][cs], the per-token loss terms [N], the log-sum-exp partials pm, ps
+// [slices][cs] and the target logits [cs], cuBLAS's workspace.
+size_t ce_layout(int N, int V, int d, int cc, size_t off[7])
 {
     const size_t cs = (size_t)ce_tstride(cc), ns = (size_t)ce_slices(V);
-    const size_t sizes[7] = {(size_t)V * cs * 4, (size_t)V * cs * 2, (size_t)N * 4, ns * cs * 4, ns * cs * 4,
-                             cs * 4, kCublasWsBytes};
+    const size_t sizes[7] = {ce_fused(d) ? 0 : (size_t)V * cs * 4, (size_t)V * cs * 2, (size_t)N * 4, ns * cs * 4,
+                             ns * cs * 4, cs * 4, kCublasWsBytes};
     size_t o = 0;
     for (int i = 0; i < 7; ++i) {
         off[i] = o;
@@ -809,7 +828,7 @@ la_status ce_check(const void* h, const void* W, const int* targets, int N, int 
         reinterpret_cast<uintptr_t>(targets) % 4)
         return LA_ERR_INVALID;
     size_t off[7];
-    *need = ce_layout(N, V, std::min(ce_chunk, N), off);
+    *need = ce_layout(N, V, d, std::min(ce_chunk, N), off);
     if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kCeAlign || workspace_bytes < *need)
         return LA_ERR_INVALID;
     const Buf wsb = {workspace, *need};
@@ -858,7 +877,7 @@ extern "C" size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk)
 {
     if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0) return 0;
     size_t off[7];
-    return ce_layout(N, V, std::min(ce_chunk, std::max(N, 1)), off);
+    return ce_layout(N, V, d, std::min(ce_chunk, std::max(N, 1)), off);
 }
 
 extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets, int N, int V, int d, int ce_chunk,
@@ -878,7 +897,7 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
     if (N == 0) return cudaMemsetAsync(loss, 0, sizeof(float), s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
     const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc), ns = ce_slices(V);
     size_t off[7];
-    ce_layout(N, V, cc, off);
+    ce_layout(N, V, d, cc, off);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     float* LT = reinterpret_cast<float*>(ws + off[0]);
     float* row_loss = reinterpret_cast<float*>(ws + off[2]);
@@ -886,20 +905,15 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
     float* ps = reinterpret_cast<float*>(ws + off[4]);
     float* tl = reinterpret_cast<float*>(ws + off[5]);
     if (ce_fused(d)) {  // logits on the tensor core, the log-sum-exp from TMEM
-        static OptIn flag;
-        auto kern = la::la_ce_logits_lse_kernel;
-        st = prepare(kern, flag, la::CeGemmLayout::BYTES);
-        if (st != LA_OK) return st;
         CUtensorMap th{}, tw{};
         if (!ce_maps(h, W, N, V, d, &th, &tw)) return LA_ERR_CUDA;
+        const int nt = (V + la::CePersistLayout::BN - 1) / la::CePersistLayout::BN;
         for (int c0 = 0; c0 < N; c0 += cc) {
             const int nc = std::min(cc, N - c0);
-            st = launch_pdl(kern, dim3((nc + la::CeGemmLayout::BM - 1) / la::CeGemmLayout::BM, ns),
-                            la::CeGemmLayout::THREADS, la::CeGemmLayout::BYTES, s, th, tw, c0, nc, cs, V,
-                            d / la::CeGemmLayout::BK, targets + c0, pm, ps, tl);
+            st = ce_persist_launch<0>(th, tw, c0, nc, cs, V, d, targets + c0, pm, ps, tl, nullptr, 0.f, nullptr, s);
             if (st != LA_OK) return st;
             st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
-                            static_cast<const float*>(ps), static_cast<const float*>(tl), ns, nc, cs, V, targets + c0,
+                            static_cast<const float*>(ps), static_cast<const float*>(tl), nt, nc, cs, V, targets + c0,
                             lse + c0, row_loss + c0);
             if (st != LA_OK) return st;
         }
@@ -941,22 +955,31 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     if (N == 0) return cudaMemsetAsync(dW, 0, (size_t)V * d * 4, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
     const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc);
     size_t off[7];
-    ce_layout(N, V, cc, off);
+    ce_layout(N, V, d, cc, off);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     float* LT = reinterpret_cast<float*>(ws + off[0]);
     __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[1]);
+    const bool fused = ce_fused(d);
+    CUtensorMap th{}, tw{};
+    if (fused && !ce_maps(h, W, N, V, d, &th, &tw)) return LA_ERR_CUDA;
     CublasUse cb(s, ws + off[6]);
     if (!cb.ok) return LA_ERR_CUDA;
     const float one = 1.f, zero = 0.f, scale = dloss / (float)N;
     for (int c0 = 0; c0 < N; c0 += cc) {
         const int nc = std::min(cc, N - c0);
         const __nv_bfloat16* hc = static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d;
-        if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed
-        constexpr int rows_per_cta = la::CE_ROWS * la::CE_GRAD_ROWS;
-        st = launch_pdl(la::la_ce_grad_kernel, dim3(cs / la::CE_TOK, (V + rows_per_cta - 1) / rows_per_cta),
-                        la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0,
-                        lse + c0, scale, GT);
-        if (st != LA_OK) return st;
+        if (fused) {  // the logits again on the tensor core, the gradient straight from TMEM
+            st = ce_persist_launch<1>(th, tw, c0, nc, cs, V, d, targets + c0, nullptr, nullptr, nullptr, lse + c0,
+                                      scale, GT, s);
+            if (st != LA_OK) return st;
+        } else {
+            if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed
+            constexpr int rows_per_cta = la::CE_ROWS * la::CE_GRAD_ROWS;
+            st = launch_pdl(la::la_ce_grad_kernel, dim3(cs / la::CE_TOK, (V + rows_per_cta - 1) / rows_per_cta),
+                            la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0,
+                            lse + c0, scale, GT);
+            if (st != LA_OK) return st;
+        }
         // dh_c[nc][d] = G W  (column-major: W (d x V) . op_T(GT) (V x nc))
         if (cublasGemmEx(cb.h, CUBLAS_OP_N, CUBLAS_OP_T, d, nc, V, &one, W, CUDA_R_16BF, d, GT, CUDA_R_16BF, cs, &zero,
                          static_cast<__nv_bfloat16*>(dh) + (size_t)c0 * d, CUDA_R_16BF, d, CUBLAS_COMPUTE_32F,

@@ -8,10 +8,11 @@
 //     logits[i][j] = h_i . W_j,   lse_i = log sum_j exp(logits[i][j]),
 //     loss = (1/N) sum_i (lse_i - logits[i][y_i]),
 //     G[i][j] = (exp(logits[i][j] - lse_i) - [j == y_i]) dloss / N,   dh = G W,  dW = G^T h.
-// The forward's logits run on this library's tensor-core kernel with the log-sum-exp in
-// its epilogue (la_ce_logits_lse_kernel, below; d a multiple of 64); the backward's three
-// contractions are plain GEMMs (cuBLAS, bf16 in, fp32 accumulate, in la_api.cu).  The
-// chunk's logits and gradient are kept vocabulary-major, LT[j][i] with the tokens
+// With d a multiple of 64 the logits run on this library's tensor-core kernel with the
+// log-sum-exp (forward) or the gradient (backward) in its epilogue (la_ce_persist_kernel,
+// below), so they never reach memory; dh = G W and dW = G^T h, and the logits for other d,
+// are plain GEMMs (cuBLAS, bf16 in, fp32 accumulate, in la_api.cu) with the row kernels
+// here between them.  The chunk's logits and gradient are kept vocabulary-major, LT[j][i] with the tokens
 // contiguous (row stride cs, a multiple of 32): every GEMM then writes and reads its
 // operands along an aligned dimension (with the odd V = 50257 contiguous instead, the
 // library's GEMM ran 12x slower on this GPU), and the kernels here read coalesced rows of
@@ -168,36 +169,39 @@ la_ce_grad_kernel(const float* LT, int V, int nc, int cs, const int* y, const fl
     }
 }
 
-// ---------------------------------------------------------------- fused forward
-// The logits of a 128-token x 128-row tile on the tensor core (tcgen05, fp32 accumulator
-// in TMEM), K = d streamed through a 3-stage TMA ring of 64-wide K slices (128-byte
-// swizzle, both operands K-major: h rows and W rows), and the log-sum-exp taken straight
-// from TMEM, so the chunk's logits never reach memory: per token, the tile's (max, sum of
-// exp) and, in the one tile that holds it, the target's logit -> pm / ps [tile][i], tl[i]
-// (la_ce_lse_merge_kernel then merges the tiles).  (The same mainloop with the gradient as
-// epilogue measured slower in the backward than the library GEMM plus la_ce_grad_kernel:
-// 206 against 182 us at N = 512, V = 50257, d = 1280 -- a 128 x 128 tile needs ~23 TB/s
-// of L2 bandwidth to keep up with the tensor pipe.)
-// Warps 0-3 own the tile's 128 token rows (TMEM lanes); warp 4 issues the TMA loads; one
-// lane of warp 5 issues the UMMAs (M = 128, N = 128, K = 16) and frees each stage with a
-// commit.  One tile per CTA, two CTAs per SM (one's epilogue runs under the other's
-// MMAs), grid (token tiles, vocabulary tiles) with the token tile fastest, so the CTAs
-// that share a slice of W run together and meet it in L2.
-struct CeGemmLayout {
-    static constexpr int BM = 128, BN = 128, BK = 64, STAGES = 3;
-    static constexpr uint32_t A_BYTES = BM * BK * 2;              // 16 KB
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 32 KB
-    static constexpr uint32_t BARS = STAGES * STAGE_BYTES;        // 96 KB: two CTAs per SM
-    static constexpr uint32_t BYTES = BARS + 128;
-    static constexpr uint32_t TMEM_COLS = BN;
+// ---------------------------------------------------------------- persistent fused GEMM
+// The logits of 128-token x 256-row tiles on the tensor core (tcgen05, fp32 accumulators
+// in TMEM, UMMA M = 128, N = 256, K = 16), K = d streamed in 64-wide, 128-byte-swizzled
+// slices (both operands K-major: h rows and W rows), one CTA per SM looping over the tiles
+// (token tile fastest, so the CTAs that share a slice of W run at the same time), with two
+// TMEM accumulators: the epilogue of one tile runs while the UMMAs of the next fill the
+// other, and the 4-stage TMA ring runs on across tiles.  Epilogue by MODE:
+//   MODE 0 (forward): per token, the tile's (max, sum of exp) and, in the one tile that
+//          holds it, the target's logit -> pm / ps [tile][i], tl[i] (la_ce_lse_merge_kernel
+//          then merges the tiles): the chunk's logits never reach memory;
+//   MODE 1 (backward): G = (exp(logit - lse) - [j == y]) scale -> GT[j][i] (bf16,
+//          vocabulary-major, zero for the chunk's padding tokens), 64 vocabulary rows at a
+//          time through a shared-memory tile so that GT rows leave in 16-byte stores.
+// Barriers: full / empty per stage (TMA -> UMMA -> TMA), tfull / tempty per accumulator
+// (UMMA commit -> epilogue, 128 epilogue arrivals -> UMMA).
+struct CePersistLayout {
+    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;                // 16 KB
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 48 KB
+    static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;        // 16 KB: a gradient chunk [64][128] bf16
+    static constexpr uint32_t BARS = GSTAGE + 64 * BM * 2;
+    static constexpr uint32_t BYTES = BARS + 256;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
     static constexpr int THREADS = 192;
 };
 
-__global__ void __launch_bounds__(192, 2)
-la_ce_logits_lse_kernel(const __grid_constant__ CUtensorMap th, const __grid_constant__ CUtensorMap tw, int c0,
-                        int nc, int cs, int V, int KB, const int* y, float* pm, float* ps, float* tl)
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_constant__ CUtensorMap tw, int c0, int nc,
+                     int cs, int V, int KB, int mtiles, int ntiles, const int* y, float* pm, float* ps, float* tl,
+                     const float* lse, float scale, __nv_bfloat16* GT)
 {
-    using L = CeGemmLayout;
+    using L = CePersistLayout;
     using namespace tc;
     extern __shared__ __align__(1024) unsigned char sm[];
     if (smem_addr(sm) & 1023u) {
@@ -206,20 +210,23 @@ la_ce_logits_lse_kernel(const __grid_constant__ CUtensorMap th, const __grid_con
     }
     const uint32_t sbase = smem_addr(sm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
-    uint64_t* full = bars;                 // [STAGES] a stage's A and B landed (TMA)
-    uint64_t* empty = bars + L::STAGES;    // [STAGES] a stage's UMMAs are done (commit)
-    uint64_t* done = bars + 2 * L::STAGES; // every UMMA of the tile is done
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 8 * (2 * L::STAGES + 1));
+    uint64_t* full = bars;                    // [STAGES]
+    uint64_t* empty = bars + L::STAGES;       // [STAGES]
+    uint64_t* tfull = bars + 2 * L::STAGES;   // [2] an accumulator holds a finished tile
+    uint64_t* tempty = tfull + 2;             // [2] the epilogue has read an accumulator
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mt = blockIdx.x, nt = blockIdx.y;  // token tile (within the chunk), vocabulary tile
-    const int m0 = mt * L::BM, n0 = nt * L::BN;
+    const int ntot = mtiles * ntiles;
 
     if (tid == 0) {
         for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        mbar_init(done, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 128);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -233,72 +240,126 @@ la_ce_logits_lse_kernel(const __grid_constant__ CUtensorMap th, const __grid_con
     pdl_wait();
 
     if (warp == 4) {
-        if (lane == 0) {  // TMA producer
+        if (lane == 0) {  // TMA producer: every (tile, k-slice) of this CTA, in order
             prefetch_tmap(&th);
             prefetch_tmap(&tw);
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % L::STAGES;
-                if (kb >= L::STAGES && !mbar_wait(empty + s, ((kb / L::STAGES) - 1) & 1, ERR_TIMEOUT_MMA)) break;
-                unsigned char* st = sm + s * L::STAGE_BYTES;
-                mbar_expect_tx(full + s, L::STAGE_BYTES);
-                tma_load_3d(st, &th, full + s, kb * L::BK, c0 + m0, 0);
-                tma_load_3d(st + L::A_BYTES, &tw, full + s, kb * L::BK, n0, 0);
+            int g = 0;
+            bool ok = true;
+            for (int T = blockIdx.x; T < ntot && ok; T += gridDim.x) {
+                const int m0 = (T % mtiles) * L::BM, n0 = (T / mtiles) * L::BN;
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % L::STAGES, u = g / L::STAGES;
+                    if (u > 0 && !(ok = mbar_wait(empty + s, (u - 1) & 1, ERR_TIMEOUT_MMA))) break;
+                    unsigned char* st = sm + s * L::STAGE_BYTES;
+                    mbar_expect_tx(full + s, L::STAGE_BYTES);
+                    tma_load_3d(st, &th, full + s, kb * L::BK, c0 + m0, 0);
+                    tma_load_3d(st + L::A_BYTES, &tw, full + s, kb * L::BK, n0, 0);
+                }
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {  // UMMA issuer
             const uint32_t id = idesc_bf16(L::BM, L::BN, false, false);
+            int g = 0, lt = 0;
             bool ok = true;
-            for (int kb = 0; kb < KB && ok; ++kb) {
-                const int s = kb % L::STAGES;
-                ok = mbar_wait(full + s, (kb / L::STAGES) & 1, ERR_TIMEOUT_TMA);
-                if (!ok) break;
+            for (int T = blockIdx.x; T < ntot && ok; T += gridDim.x, ++lt) {
+                const int acc = lt & 1, ua = lt >> 1;
+                if (ua > 0 && !(ok = mbar_wait(tempty + acc, (ua - 1) & 1, ERR_TIMEOUT_MMA))) break;
                 tc_fence_after();
-                const uint32_t a = sbase + s * L::STAGE_BYTES;
-                const uint64_t dA = smem_desc(a, 16, 1024), dB = smem_desc(a + L::A_BYTES, 16, 1024);
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % L::STAGES;
+                    if (!(ok = mbar_wait(full + s, (g / L::STAGES) & 1, ERR_TIMEOUT_TMA))) break;
+                    tc_fence_after();
+                    const uint32_t a = sbase + s * L::STAGE_BYTES;
+                    const uint64_t dA = smem_desc(a, 16, 1024), dB = smem_desc(a + L::A_BYTES, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < L::BK / 16; ++kk)  // +32 bytes per K = 16 step inside the atom
-                    umma_bf16(tmem, dA + kk * 2, dB + kk * 2, id, kb > 0 || kk > 0);
-                umma_commit(empty + s);
+                    for (int kk = 0; kk < L::BK / 16; ++kk)
+                        umma_bf16(tmem + acc * L::BN, dA + kk * 2, dB + kk * 2, id, kb > 0 || kk > 0);
+                    umma_commit(empty + s);
+                }
+                umma_commit(tfull + acc);
             }
-            umma_commit(done);
         }
     } else {
-        // ---- epilogue: token row t of the tile (TMEM lane t), BN vocabulary columns
-        const int t = tid;                    // warps 0-3
-        const int i = m0 + t;                 // token within the chunk
-        const bool live = i < nc;
+        // ---- epilogue (warps 0-3): token row t of each tile, 256 vocabulary columns
+        const int t = tid;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const int tgt = live ? y[i] : -1;
-        mbar_wait(done, 0, ERR_TIMEOUT_MMA);
-        tc_fence_after();
         constexpr float kLog2e = 1.4426950408889634f;
-        {
-            float m = -INFINITY, sum = 0.f;
+        int lt = 0;
+        for (int T = blockIdx.x; T < ntot; T += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            const int mt = T % mtiles, nt = T / mtiles;
+            const int i = mt * L::BM + t, n0 = nt * L::BN;
+            const bool live = i < nc;
+            const int tgt = live ? y[i] : -1;
+            if (!mbar_wait(tfull + acc, (lt >> 1) & 1, ERR_TIMEOUT_MMA)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + lane_base + acc * L::BN;
+            if (MODE == 0) {
+                float m = -INFINITY, sum = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < L::BN / 64; ++c) {
-                uint32_t r[64];
-                tmem_ld32x64(tmem + lane_base + 64 * c, r);
-                const int jc = n0 + 64 * c;
-                float mx = -INFINITY;
+                for (int c = 0; c < L::BN / 64; ++c) {
+                    uint32_t r[64];
+                    tmem_ld32x64(tbase + 64 * c, r);
+                    const int jc = n0 + 64 * c;
+                    float mx = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    if (jc + e < V) mx = fmaxf(mx, __uint_as_float(r[e]));
-                if (mx > m) {
-                    sum *= exp2f((m - mx) * kLog2e);
-                    m = mx;
-                }
-                const float mb = m * kLog2e;
+                    for (int e = 0; e < 64; ++e)
+                        if (jc + e < V) mx = fmaxf(mx, __uint_as_float(r[e]));
+                    if (mx > m) {
+                        sum *= exp2f((m - mx) * kLog2e);
+                        m = mx;
+                    }
+                    const float mb = m * kLog2e;
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float x = __uint_as_float(r[e]);
-                    if (jc + e < V) sum += exp2f(fmaf(x, kLog2e, -mb));
-                    if (jc + e == tgt) tl[i] = x;
+                    for (int e = 0; e < 64; ++e) {
+                        const float x = __uint_as_float(r[e]);
+                        if (jc + e < V) sum += exp2f(fmaf(x, kLog2e, -mb));
+                        if (jc + e == tgt) tl[i] = x;
+                    }
                 }
-            }
-            if (live) {
-                pm[(size_t)nt * cs + i] = m;
-                ps[(size_t)nt * cs + i] = sum;
+                tc_fence_before();
+                mbar_arrive(tempty + acc);  // the accumulator may take the next tile
+                if (live) {
+                    pm[(size_t)nt * cs + i] = m;
+                    ps[(size_t)nt * cs + i] = sum;
+                }
+            } else {
+                const float lb = live ? lse[i] * kLog2e : 0.f;
+                __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE);  // [64][128]
+                const int m0 = mt * L::BM;
+#pragma unroll 1
+                for (int c = 0; c < L::BN / 64; ++c) {
+                    uint32_t r[64];
+                    tmem_ld32x64(tbase + 64 * c, r);
+                    if (c == L::BN / 64 - 1) {  // the accumulator has been read: the next tile may use it
+                        tc_fence_before();
+                        mbar_arrive(tempty + acc);
+                    }
+                    const int jc = n0 + 64 * c;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        float g = 0.f;
+                        if (live) {
+                            g = exp2f(fmaf(__uint_as_float(r[e]), kLog2e, -lb));
+                            if (jc + e == tgt) g -= 1.f;
+                            g *= scale;
+                        }
+                        stage[e * L::BM + t] = __float2bfloat16_rn(g);
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // the chunk is staged
+                    // rows jc .. jc+63, tokens m0 .. m0+127: 16-byte pieces of 8 tokens (cs is a
+                    // multiple of 32, so a piece is wholly inside or outside the chunk)
+#pragma unroll
+                    for (int q = t; q < 64 * L::BM / 8; q += 128) {
+                        const int row = q / (L::BM / 8), col = (q % (L::BM / 8)) * 8;
+                        const int j = jc + row;
+                        if (j < V && m0 + col < cs)
+                            *reinterpret_cast<uint4*>(GT + (size_t)j * cs + m0 + col) =
+                                *reinterpret_cast<const uint4*>(stage + row * L::BM + col);
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // read before the next chunk overwrites it
+                }
             }
         }
     }

@@ -238,17 +238,18 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
  *     loss = (1/N) sum_i (lse_i - logits[i][y_i]),
  * computed ce_chunk tokens at a time so that only one chunk's logits (fp32) exist at once;
  * the backward recomputes them.  The contractions run on cuBLAS (bf16 in, fp32
- * accumulate; a plain library GEMM) -- except the forward's logits when d is a multiple of
- * 64 (see la_ce_workspace_bytes) -- and the row work (log-sum-exp, target logit, the
- * softmax gradient) on this library's kernels.
+ * accumulate; a plain library GEMM) -- except the logits when d is a multiple of 64 (see
+ * la_ce_workspace_bytes) -- and the row work (log-sum-exp, target logit, the softmax
+ * gradient) on this library's kernels.
  *
- * la_ce_workspace_bytes: the device workspace both calls need: the chunk's fp32 logits and
- * bf16 gradient, vocabulary-major with the chunk padded to 32 tokens (6 bytes per logit),
- * N floats, the log-sum-exp partials (2 floats per token and 128-row vocabulary tile) and
+ * la_ce_workspace_bytes: the device workspace both calls need: the chunk's bf16 gradient
+ * (and, when d is not a multiple of 64, its fp32 logits), vocabulary-major with the chunk
+ * padded to 32 tokens,
+ * N floats, the log-sum-exp partials (2 floats per token and 256-row vocabulary tile) and
  * a 32 MiB GEMM workspace, each at a 256-byte boundary; 0 for a negative or zero size.
- * No CUDA call.  With d a multiple of 64 the forward computes the logits on this
- * library's tensor-core kernel and takes their log-sum-exp straight from its accumulator
- * (the logits never reach memory); otherwise, and in the backward, cuBLAS writes them into
+ * No CUDA call.  With d a multiple of 64 the logits are computed on this library's
+ * tensor-core kernel and their log-sum-exp (forward) or gradient (backward) taken straight
+ * from its accumulator: the logits never reach memory.  Otherwise cuBLAS writes them into
  * the workspace.
  *
  * la_ce_fwd: loss (one float, device) and lse ([N] float32, device; the backward's input).
