@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of each kernel on this workload, with the hash of the kernel sources they were taken on
 # (profiles/la_*_tc_fractus1b_G160_C128_D64.md).  Reported as null once the sources differ.
 NCU_TRAFFIC = {
-    "la_fwd": {"bytes": 10573568 + 0, "src": "0473266fe20a8492"},
-    "la_bwd": {"bytes": 15884800 + 0, "src": "35955d51be7464a6"},
+    "la_fwd": {"bytes": 10573312 + 0, "src": "3f063d20f2795252"},
+    "la_bwd": {"bytes": 15884544 + 0, "src": "6e4e8d383bb4881d"},
 }
 
 
