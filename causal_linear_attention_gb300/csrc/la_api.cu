@@ -775,11 +775,27 @@ bool ce_maps(const void* h, const void* W, int N, int V, int d, CUtensorMap* th,
     return tmap_bf16(th, h, 1, N, d, la::CePersistLayout::BM) && tmap_bf16(tw, W, 1, V, d, la::CePersistLayout::BN);
 }
 
-// The persistent fused GEMM over a chunk: one CTA per SM (at most one per tile).
+// The chunk's gradient GT [V][cs] bf16 as the store map of the fused backward: boxes of
+// 128 tokens x 64 vocabulary rows, no swizzle (the kernel stages them row-major).
+bool ce_grad_map(const __nv_bfloat16* GT, int V, int cs, CUtensorMap* map)
+{
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cs, (cuuint64_t)V, 1u};
+    cuuint64_t strides[2] = {(cuuint64_t)cs * 2, (cuuint64_t)V * cs * 2};
+    cuuint32_t box[3] = {(cuuint32_t)la::CePersistLayout::BM, 64u, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(GT), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The persistent fused GEMM over a chunk: one CTA per SM (at most one per tile).  tgt is
+// the gradient's store map (MODE 1; unused by MODE 0).
 template <int MODE>
-la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, int c0, int nc, int cs, int V, int d,
-                            const int* y, float* pm, float* ps, float* tl, const float* lse, float scale,
-                            __nv_bfloat16* GT, cudaStream_t s)
+la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, const CUtensorMap& tgt, int c0, int nc,
+                            int cs, int V, int d, const int* y, float* pm, float* ps, float* tl, const float* lse,
+                            float scale, cudaStream_t s)
 {
     using PL = la::CePersistLayout;
     static OptIn flag;
@@ -789,8 +805,8 @@ la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, int c0
     const int mtiles = ((MODE == 0 ? nc : cs) + PL::BM - 1) / PL::BM, ntiles = (V + PL::BN - 1) / PL::BN;
     const int sms = sm_count();
     if (sms <= 0) return LA_ERR_CUDA;
-    return launch_pdl(kern, std::min(mtiles * ntiles, sms), PL::THREADS, PL::BYTES, s, th, tw, c0, nc, cs, V,
-                      d / PL::BK, mtiles, ntiles, y, pm, ps, tl, lse, scale, GT);
+    return launch_pdl(kern, std::min(mtiles * ntiles, sms), PL::THREADS, PL::BYTES, s, th, tw, tgt, c0, nc, cs, V,
+                      d / PL::BK, mtiles, ntiles, y, pm, ps, tl, lse, scale);
 }
 
 // Workspace slots: the chunk's fp32 logits LT [V][cs] (only without the fused GEMM), its
@@ -910,7 +926,7 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
         const int nt = (V + la::CePersistLayout::BN - 1) / la::CePersistLayout::BN;
         for (int c0 = 0; c0 < N; c0 += cc) {
             const int nc = std::min(cc, N - c0);
-            st = ce_persist_launch<0>(th, tw, c0, nc, cs, V, d, targets + c0, pm, ps, tl, nullptr, 0.f, nullptr, s);
+            st = ce_persist_launch<0>(th, tw, tw, c0, nc, cs, V, d, targets + c0, pm, ps, tl, nullptr, 0.f, s);
             if (st != LA_OK) return st;
             st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
                             static_cast<const float*>(ps), static_cast<const float*>(tl), nt, nc, cs, V, targets + c0,
@@ -960,8 +976,8 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     float* LT = reinterpret_cast<float*>(ws + off[0]);
     __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[1]);
     const bool fused = ce_fused(d);
-    CUtensorMap th{}, tw{};
-    if (fused && !ce_maps(h, W, N, V, d, &th, &tw)) return LA_ERR_CUDA;
+    CUtensorMap th{}, tw{}, tgt{};
+    if (fused && (!ce_maps(h, W, N, V, d, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt))) return LA_ERR_CUDA;
     CublasUse cb(s, ws + off[6]);
     if (!cb.ok) return LA_ERR_CUDA;
     const float one = 1.f, zero = 0.f, scale = dloss / (float)N;
@@ -969,8 +985,8 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
         const int nc = std::min(cc, N - c0);
         const __nv_bfloat16* hc = static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d;
         if (fused) {  // the logits again on the tensor core, the gradient straight from TMEM
-            st = ce_persist_launch<1>(th, tw, c0, nc, cs, V, d, targets + c0, nullptr, nullptr, nullptr, lse + c0,
-                                      scale, GT, s);
+            st = ce_persist_launch<1>(th, tw, tgt, c0, nc, cs, V, d, targets + c0, nullptr, nullptr, nullptr,
+                                      lse + c0, scale, s);
             if (st != LA_OK) return st;
         } else {
             if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed

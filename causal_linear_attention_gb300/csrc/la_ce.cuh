@@ -181,15 +181,17 @@ la_ce_grad_kernel(const float* LT, int V, int nc, int cs, const int* y, const fl
 //          then merges the tiles): the chunk's logits never reach memory;
 //   MODE 1 (backward): G = (exp(logit - lse) - [j == y]) scale -> GT[j][i] (bf16,
 //          vocabulary-major, zero for the chunk's padding tokens), 64 vocabulary rows at a
-//          time through a shared-memory tile so that GT rows leave in 16-byte stores.
+//          time through two shared-memory tiles, each leaving in one TMA store (tgrad: GT as
+//          [V][cs], 128 x 64 boxes; rows past V and tokens past cs are clipped).
 // Barriers: full / empty per stage (TMA -> UMMA -> TMA), tfull / tempty per accumulator
 // (UMMA commit -> epilogue, 128 epilogue arrivals -> UMMA).
 struct CePersistLayout {
     static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
     static constexpr uint32_t A_BYTES = BM * BK * 2;                // 16 KB
     static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 48 KB
-    static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;        // 16 KB: a gradient chunk [64][128] bf16
-    static constexpr uint32_t BARS = GSTAGE + 64 * BM * 2;
+    static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;        // 2 x 16 KB: gradient chunks [64][128] bf16
+    static constexpr uint32_t GCHUNK = 64 * BM * 2;
+    static constexpr uint32_t BARS = GSTAGE + 2 * GCHUNK;
     static constexpr uint32_t BYTES = BARS + 256;
     static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
     static constexpr int THREADS = 192;
@@ -197,9 +199,9 @@ struct CePersistLayout {
 
 template <int MODE>
 __global__ void __launch_bounds__(192, 1)
-la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_constant__ CUtensorMap tw, int c0, int nc,
-                     int cs, int V, int KB, int mtiles, int ntiles, const int* y, float* pm, float* ps, float* tl,
-                     const float* lse, float scale, __nv_bfloat16* GT)
+la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_constant__ CUtensorMap tw,
+                     const __grid_constant__ CUtensorMap tgrad, int c0, int nc, int cs, int V, int KB, int mtiles,
+                     int ntiles, const int* y, float* pm, float* ps, float* tl, const float* lse, float scale)
 {
     using L = CePersistLayout;
     using namespace tc;
@@ -285,7 +287,7 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
         const int t = tid;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         constexpr float kLog2e = 1.4426950408889634f;
-        int lt = 0;
+        int lt = 0, nchunk = 0;  // (MODE 1) gradient chunks staged so far
         for (int T = blockIdx.x; T < ntot; T += gridDim.x, ++lt) {
             const int acc = lt & 1;
             const int mt = T % mtiles, nt = T / mtiles;
@@ -326,16 +328,19 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                 }
             } else {
                 const float lb = live ? lse[i] * kLog2e : 0.f;
-                __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE);  // [64][128]
                 const int m0 = mt * L::BM;
 #pragma unroll 1
-                for (int c = 0; c < L::BN / 64; ++c) {
+                for (int c = 0; c < L::BN / 64; ++c, ++nchunk) {
                     uint32_t r[64];
                     tmem_ld32x64(tbase + 64 * c, r);
                     if (c == L::BN / 64 - 1) {  // the accumulator has been read: the next tile may use it
                         tc_fence_before();
                         mbar_arrive(tempty + acc);
                     }
+                    // this chunk's staging tile was last read by the store two chunks ago
+                    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE + (nchunk & 1) * L::GCHUNK);
+                    if (t == 0 && nchunk >= 2) tma_store_wait_read_le1();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
                     const int jc = n0 + 64 * c;
 #pragma unroll
                     for (int e = 0; e < 64; ++e) {
@@ -345,24 +350,19 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                             if (jc + e == tgt) g -= 1.f;
                             g *= scale;
                         }
-                        stage[e * L::BM + t] = __float2bfloat16_rn(g);
+                        stage[e * L::BM + t] = __float2bfloat16_rn(g);  // [row e][token t]
                     }
+                    fence_async_smem();
                     asm volatile("bar.sync 1, 128;" ::: "memory");  // the chunk is staged
-                    // rows jc .. jc+63, tokens m0 .. m0+127: 16-byte pieces of 8 tokens (cs is a
-                    // multiple of 32, so a piece is wholly inside or outside the chunk)
-#pragma unroll
-                    for (int q = t; q < 64 * L::BM / 8; q += 128) {
-                        const int row = q / (L::BM / 8), col = (q % (L::BM / 8)) * 8;
-                        const int j = jc + row;
-                        if (j < V && m0 + col < cs)
-                            *reinterpret_cast<uint4*>(GT + (size_t)j * cs + m0 + col) =
-                                *reinterpret_cast<const uint4*>(stage + row * L::BM + col);
+                    if (t == 0) {
+                        tma_store_3d(&tgrad, stage, m0, jc, 0);
+                        tma_store_commit();
                     }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");  // read before the next chunk overwrites it
                 }
             }
         }
     }
+    if (MODE == 1 && tid == 0) tma_store_wait_all();  // the gradient stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);

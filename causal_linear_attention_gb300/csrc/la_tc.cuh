@@ -126,6 +126,8 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 // Wait until the smem sources of all committed stores have been read.
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until at most one committed store group still has to read its shared memory.
+__device__ __forceinline__ void tma_store_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Plain (non-tensor) bulk copies: 16-byte aligned addresses, size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {
