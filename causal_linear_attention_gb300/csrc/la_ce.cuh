@@ -29,6 +29,18 @@
 
 namespace la {
 
+// 2^x on the multi-function unit (PTX ex2.approx.ftz.f32): a few ulp of fp32, results
+// below the normal range flushed to zero, 2^-inf = 0.  The epilogues below take it for
+// exp(x) = 2^(x log2 e): with the library exp2f each of the 256 exponentials a thread
+// takes per tile went through a range-checking sequence with branches, and the
+// backward's epilogue took longer than the tile's MMAs.
+__device__ __forceinline__ float ex2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 constexpr int CE_TOK = 32;        // tokens per CTA (one warp's lanes)
 constexpr int CE_ROWS = 8;        // warps per CTA, each walking every 8th vocabulary row
 constexpr int CE_SLICE = 1024;    // vocabulary rows per CTA in the log-sum-exp
@@ -309,14 +321,14 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                     for (int e = 0; e < 64; ++e)
                         if (jc + e < V) mx = fmaxf(mx, __uint_as_float(r[e]));
                     if (mx > m) {
-                        sum *= exp2f((m - mx) * kLog2e);
+                        sum *= ex2_fast((m - mx) * kLog2e);
                         m = mx;
                     }
                     const float mb = m * kLog2e;
 #pragma unroll
                     for (int e = 0; e < 64; ++e) {
                         const float x = __uint_as_float(r[e]);
-                        if (jc + e < V) sum += exp2f(fmaf(x, kLog2e, -mb));
+                        if (jc + e < V) sum += ex2_fast(fmaf(x, kLog2e, -mb));
                         if (jc + e == tgt) tl[i] = x;
                     }
                 }
@@ -346,7 +358,7 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                     for (int e = 0; e < 64; ++e) {
                         float g = 0.f;
                         if (live) {
-                            g = exp2f(fmaf(__uint_as_float(r[e]), kLog2e, -lb));
+                            g = ex2_fast(fmaf(__uint_as_float(r[e]), kLog2e, -lb));
                             if (jc + e == tgt) g -= 1.f;
                             g *= scale;
                         }
