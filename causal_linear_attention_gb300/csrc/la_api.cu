@@ -763,50 +763,92 @@ size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 // Token stride of the chunk's vocabulary-major logits and gradient: the chunk rounded up
 // to 32 tokens (one warp's lanes in the row kernels; 128-byte rows for the GEMMs).
 int ce_tstride(int cc) { return (cc + 31) / 32 * 32; }
-// log-sum-exp partial slots per token: one per 256-row vocabulary tile of the fused GEMM
-// (the row-kernel path, 1024-row slices, uses the first quarter of them)
-int ce_slices(int V) { return (V + la::CePersistLayout::BN - 1) / la::CePersistLayout::BN; }
+// Vocabulary tile widths of the fused GEMM, widest first; the log-sum-exp partial slots
+// per token are sized for the narrowest (one per tile; the row-kernel path, 1024-row
+// slices, uses fewer).
+constexpr int kCeTileWidths[3] = {256, 224, 192};
+constexpr int kCeTokTile = 128;  // tokens per tile of the fused GEMM
+int ce_slices(int V) { return (V + kCeTileWidths[2] - 1) / kCeTileWidths[2]; }
 // d a multiple of 64: the logits on this library's tensor-core kernel, never in memory
-bool ce_fused(int d) { return d % la::CePersistLayout::BK == 0; }
+bool ce_fused(int d) { return d % 64 == 0; }
 
-// Maps for the fused GEMM: h [N][d] in 128-row boxes, W [V][d] in 256-row boxes.
-bool ce_maps(const void* h, const void* W, int N, int V, int d, CUtensorMap* th, CUtensorMap* tw)
+// The fused GEMM's tile width for mtiles token tiles: the one whose whole waves over the
+// SMs (one persistent CTA each) cover the fewest vocabulary columns; ties go to the wider
+// tile (fewer, larger UMMAs per byte loaded).
+int ce_tile_width(int mtiles, int V, int sms)
 {
-    return tmap_bf16(th, h, 1, N, d, la::CePersistLayout::BM) && tmap_bf16(tw, W, 1, V, d, la::CePersistLayout::BN);
+    int best = kCeTileWidths[0];
+    long long best_cost = -1;
+    for (int bn : kCeTileWidths) {
+        const long long tiles = (long long)mtiles * ((V + bn - 1) / bn);
+        const long long cost = (tiles + sms - 1) / sms * bn;
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// Maps for the fused GEMM: h [N][d] in 128-row boxes, W [V][d] in bn-row boxes.
+bool ce_maps(const void* h, const void* W, int N, int V, int d, int bn, CUtensorMap* th, CUtensorMap* tw)
+{
+    return tmap_bf16(th, h, 1, N, d, kCeTokTile) && tmap_bf16(tw, W, 1, V, d, bn);
 }
 
 // The chunk's gradient GT [V][cs] bf16 as the store map of the fused backward: boxes of
-// 128 tokens x 64 vocabulary rows, no swizzle (the kernel stages them row-major).
+// 128 tokens x 32 vocabulary rows, no swizzle (the kernel stages them row-major).
 bool ce_grad_map(const __nv_bfloat16* GT, int V, int cs, CUtensorMap* map)
 {
     auto enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cs, (cuuint64_t)V, 1u};
     cuuint64_t strides[2] = {(cuuint64_t)cs * 2, (cuuint64_t)V * cs * 2};
-    cuuint32_t box[3] = {(cuuint32_t)la::CePersistLayout::BM, 64u, 1u};
+    cuuint32_t box[3] = {(cuuint32_t)kCeTokTile, (cuuint32_t)la::CE_GRAD_BOX, 1u};
     cuuint32_t es[3] = {1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(GT), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The persistent fused GEMM over a chunk: one CTA per SM (at most one per tile).  tgt is
-// the gradient's store map (MODE 1; unused by MODE 0).
+// Token tiles of the fused GEMM over a chunk: its nc tokens (forward), or all cs so that
+// the padding tokens' gradient columns are written as zeros (backward).
 template <int MODE>
-la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, const CUtensorMap& tgt, int c0, int nc,
-                            int cs, int V, int d, const int* y, float* pm, float* ps, float* tl, const float* lse,
-                            float scale, cudaStream_t s)
+int ce_mtiles(int nc, int cs)
 {
-    using PL = la::CePersistLayout;
+    return ((MODE == 0 ? nc : cs) + kCeTokTile - 1) / kCeTokTile;
+}
+
+template <int MODE, int BN>
+la_status ce_persist_launch_bn(const CUtensorMap& th, const CUtensorMap& tw, const CUtensorMap& tgt, int c0, int nc,
+                               int cs, int V, int d, int sms, const int* y, float* pm, float* ps, float* tl,
+                               const float* lse, float scale, cudaStream_t s)
+{
+    using PL = la::CePersistLayout<BN>;
+    static_assert(PL::BM == kCeTokTile, "token tile");
     static OptIn flag;
-    auto kern = la::la_ce_persist_kernel<MODE>;
+    auto kern = la::la_ce_persist_kernel<MODE, BN>;
     const la_status st = prepare(kern, flag, PL::BYTES);
     if (st != LA_OK) return st;
-    const int mtiles = ((MODE == 0 ? nc : cs) + PL::BM - 1) / PL::BM, ntiles = (V + PL::BN - 1) / PL::BN;
-    const int sms = sm_count();
-    if (sms <= 0) return LA_ERR_CUDA;
+    const int mtiles = ce_mtiles<MODE>(nc, cs), ntiles = (V + BN - 1) / BN;
     return launch_pdl(kern, std::min(mtiles * ntiles, sms), PL::THREADS, PL::BYTES, s, th, tw, tgt, c0, nc, cs, V,
                       d / PL::BK, mtiles, ntiles, y, pm, ps, tl, lse, scale);
+}
+
+// The persistent fused GEMM over a chunk: one CTA per SM (at most one per tile), tiles of
+// bn vocabulary rows (tw made with bn-row boxes).  tgt is the gradient's store map
+// (MODE 1; unused by MODE 0).
+template <int MODE>
+la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, const CUtensorMap& tgt, int bn, int c0,
+                            int nc, int cs, int V, int d, int sms, const int* y, float* pm, float* ps, float* tl,
+                            const float* lse, float scale, cudaStream_t s)
+{
+    switch (bn) {
+    case 256: return ce_persist_launch_bn<MODE, 256>(th, tw, tgt, c0, nc, cs, V, d, sms, y, pm, ps, tl, lse, scale, s);
+    case 224: return ce_persist_launch_bn<MODE, 224>(th, tw, tgt, c0, nc, cs, V, d, sms, y, pm, ps, tl, lse, scale, s);
+    case 192: return ce_persist_launch_bn<MODE, 192>(th, tw, tgt, c0, nc, cs, V, d, sms, y, pm, ps, tl, lse, scale, s);
+    default: return LA_ERR_INVALID;
+    }
 }
 
 // Workspace slots: the chunk's fp32 logits LT [V][cs] (only without the fused GEMM), its
@@ -921,12 +963,19 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
     float* ps = reinterpret_cast<float*>(ws + off[4]);
     float* tl = reinterpret_cast<float*>(ws + off[5]);
     if (ce_fused(d)) {  // logits on the tensor core, the log-sum-exp from TMEM
+        const int sms = sm_count();
+        if (sms <= 0) return LA_ERR_CUDA;
         CUtensorMap th{}, tw{};
-        if (!ce_maps(h, W, N, V, d, &th, &tw)) return LA_ERR_CUDA;
-        const int nt = (V + la::CePersistLayout::BN - 1) / la::CePersistLayout::BN;
+        int bn_map = 0;  // the tile width tw was made for
         for (int c0 = 0; c0 < N; c0 += cc) {
             const int nc = std::min(cc, N - c0);
-            st = ce_persist_launch<0>(th, tw, tw, c0, nc, cs, V, d, targets + c0, pm, ps, tl, nullptr, 0.f, s);
+            const int bn = ce_tile_width(ce_mtiles<0>(nc, cs), V, sms), nt = (V + bn - 1) / bn;
+            if (bn != bn_map) {
+                if (!ce_maps(h, W, N, V, d, bn, &th, &tw)) return LA_ERR_CUDA;
+                bn_map = bn;
+            }
+            st = ce_persist_launch<0>(th, tw, tw, bn, c0, nc, cs, V, d, sms, targets + c0, pm, ps, tl, nullptr, 0.f,
+                                      s);
             if (st != LA_OK) return st;
             st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
                             static_cast<const float*>(ps), static_cast<const float*>(tl), nt, nc, cs, V, targets + c0,
@@ -976,8 +1025,12 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     float* LT = reinterpret_cast<float*>(ws + off[0]);
     __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[1]);
     const bool fused = ce_fused(d);
+    // the backward's tiles cover all cs token columns of every chunk: one tile width
+    const int sms = sm_count();
+    if (sms <= 0) return LA_ERR_CUDA;
+    const int bn = ce_tile_width(ce_mtiles<1>(cc, cs), V, sms);
     CUtensorMap th{}, tw{}, tgt{};
-    if (fused && (!ce_maps(h, W, N, V, d, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt))) return LA_ERR_CUDA;
+    if (fused && (!ce_maps(h, W, N, V, d, bn, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt))) return LA_ERR_CUDA;
     CublasUse cb(s, ws + off[6]);
     if (!cb.ok) return LA_ERR_CUDA;
     const float one = 1.f, zero = 0.f, scale = dloss / (float)N;
@@ -985,8 +1038,8 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
         const int nc = std::min(cc, N - c0);
         const __nv_bfloat16* hc = static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d;
         if (fused) {  // the logits again on the tensor core, the gradient straight from TMEM
-            st = ce_persist_launch<1>(th, tw, tgt, c0, nc, cs, V, d, targets + c0, nullptr, nullptr, nullptr,
-                                      lse + c0, scale, s);
+            st = ce_persist_launch<1>(th, tw, tgt, bn, c0, nc, cs, V, d, sms, targets + c0, nullptr, nullptr,
+                                      nullptr, lse + c0, scale, s);
             if (st != LA_OK) return st;
         } else {
             if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed

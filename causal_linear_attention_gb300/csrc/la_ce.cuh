@@ -25,6 +25,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "la_tc.cuh"
 
 namespace la {
@@ -182,40 +184,48 @@ la_ce_grad_kernel(const float* LT, int V, int nc, int cs, const int* y, const fl
 }
 
 // ---------------------------------------------------------------- persistent fused GEMM
-// The logits of 128-token x 256-row tiles on the tensor core (tcgen05, fp32 accumulators
-// in TMEM, UMMA M = 128, N = 256, K = 16), K = d streamed in 64-wide, 128-byte-swizzled
+// The logits of 128-token x BN-row tiles on the tensor core (tcgen05, fp32 accumulators
+// in TMEM, UMMA M = 128, N = BN, K = 16), K = d streamed in 64-wide, 128-byte-swizzled
 // slices (both operands K-major: h rows and W rows), one CTA per SM looping over the tiles
 // (token tile fastest, so the CTAs that share a slice of W run at the same time), with two
 // TMEM accumulators: the epilogue of one tile runs while the UMMAs of the next fill the
-// other, and the 4-stage TMA ring runs on across tiles.  Epilogue by MODE:
+// other, and the 4-stage TMA ring runs on across tiles.  BN is 256, 224 or 192: the host
+// takes the one whose whole waves of tiles over the SMs cost least (V = 50257 in chunks of
+// 512 tokens: 788 tiles of 256 rows are 5.2 waves on 152 SMs, 900 of 224 rows 5.9).
+// Epilogue by MODE, in chunks of 64 accumulator columns (and one of 32 when BN = 224):
 //   MODE 0 (forward): per token, the tile's (max, sum of exp) and, in the one tile that
 //          holds it, the target's logit -> pm / ps [tile][i], tl[i] (la_ce_lse_merge_kernel
 //          then merges the tiles): the chunk's logits never reach memory;
 //   MODE 1 (backward): G = (exp(logit - lse) - [j == y]) scale -> GT[j][i] (bf16,
-//          vocabulary-major, zero for the chunk's padding tokens), 64 vocabulary rows at a
-//          time through two shared-memory tiles, each leaving in one TMA store (tgrad: GT as
-//          [V][cs], 128 x 64 boxes; rows past V and tokens past cs are clipped).
+//          vocabulary-major, zero for the chunk's padding tokens), a chunk at a time
+//          through two shared-memory tiles that leave in TMA stores (tgrad: GT as [V][cs],
+//          128 x 32 boxes; rows past V and tokens past cs are clipped).
 // Barriers: full / empty per stage (TMA -> UMMA -> TMA), tfull / tempty per accumulator
 // (UMMA commit -> epilogue, 128 epilogue arrivals -> UMMA).
+template <int BN_>
 struct CePersistLayout {
-    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+    static_assert(BN_ % 32 == 0 && BN_ >= 64 && BN_ <= 256, "vocabulary tile");
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = 4;
     static constexpr uint32_t A_BYTES = BM * BK * 2;                // 16 KB
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 48 KB
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 48 KB at BN = 256
     static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;        // 2 x 16 KB: gradient chunks [64][128] bf16
     static constexpr uint32_t GCHUNK = 64 * BM * 2;
     static constexpr uint32_t BARS = GSTAGE + 2 * GCHUNK;
     static constexpr uint32_t BYTES = BARS + 256;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators
+    static constexpr uint32_t ACC_COLS = 256;                       // accumulator a at TMEM column 256 a
+    static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 192;
+    static_assert(STAGE_BYTES % 1024 == 0 && BYTES <= 227 * 1024, "shared memory");
 };
+constexpr int CE_GRAD_BOX = 32;  // vocabulary rows per TMA store of the gradient
 
-template <int MODE>
+template <int MODE, int BN>
 __global__ void __launch_bounds__(192, 1)
 la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_constant__ CUtensorMap tw,
                      const __grid_constant__ CUtensorMap tgrad, int c0, int nc, int cs, int V, int KB, int mtiles,
                      int ntiles, const int* y, float* pm, float* ps, float* tl, const float* lse, float scale)
 {
-    using L = CePersistLayout;
+    using L = CePersistLayout<BN>;
     using namespace tc;
     extern __shared__ __align__(1024) unsigned char sm[];
     if (smem_addr(sm) & 1023u) {
@@ -288,37 +298,48 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                     const uint64_t dA = smem_desc(a, 16, 1024), dB = smem_desc(a + L::A_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < L::BK / 16; ++kk)
-                        umma_bf16(tmem + acc * L::BN, dA + kk * 2, dB + kk * 2, id, kb > 0 || kk > 0);
+                        umma_bf16(tmem + acc * L::ACC_COLS, dA + kk * 2, dB + kk * 2, id, kb > 0 || kk > 0);
                     umma_commit(empty + s);
                 }
                 umma_commit(tfull + acc);
             }
         }
     } else {
-        // ---- epilogue (warps 0-3): token row t of each tile, 256 vocabulary columns
+        // ---- epilogue (warps 0-3): token row t of each tile, BN vocabulary columns
         const int t = tid;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         constexpr float kLog2e = 1.4426950408889634f;
-        int lt = 0, nchunk = 0;  // (MODE 1) gradient chunks staged so far
+        constexpr int NFULL = L::BN / 64;         // 64-column chunks
+        constexpr bool TAIL = (L::BN % 64) != 0;  // and one of 32 columns after them
+        int lt = 0, nchunk = 0;                   // (MODE 1) gradient chunks staged so far
         for (int T = blockIdx.x; T < ntot; T += gridDim.x, ++lt) {
             const int acc = lt & 1;
             const int mt = T % mtiles, nt = T / mtiles;
-            const int i = mt * L::BM + t, n0 = nt * L::BN;
+            const int m0 = mt * L::BM, i = m0 + t, n0 = nt * L::BN;
             const bool live = i < nc;
             const int tgt = live ? y[i] : -1;
             if (!mbar_wait(tfull + acc, (lt >> 1) & 1, ERR_TIMEOUT_MMA)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem + lane_base + acc * L::BN;
-            if (MODE == 0) {
-                float m = -INFINITY, sum = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < L::BN / 64; ++c) {
-                    uint32_t r[64];
-                    tmem_ld32x64(tbase + 64 * c, r);
-                    const int jc = n0 + 64 * c;
+            const uint32_t tbase = tmem + lane_base + acc * L::ACC_COLS;
+            float m = -INFINITY, sum = 0.f;                                // MODE 0: online (max, sum)
+            const float lb = (MODE == 1 && live) ? lse[i] * kLog2e : 0.f;  // MODE 1: lse in base 2
+            // accumulator columns [col, col + W) of this tile
+            auto chunk = [&](auto width, int col, bool last) {
+                constexpr int W = decltype(width)::value;
+                uint32_t r[W];
+                if constexpr (W == 64)
+                    tmem_ld32x64(tbase + col, r);
+                else
+                    tmem_ld32(tbase + col, r);
+                if (last) {  // the accumulator has been read: the next tile may use it
+                    tc_fence_before();
+                    mbar_arrive(tempty + acc);
+                }
+                const int jc = n0 + col;
+                if constexpr (MODE == 0) {
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 64; ++e)
+                    for (int e = 0; e < W; ++e)
                         if (jc + e < V) mx = fmaxf(mx, __uint_as_float(r[e]));
                     if (mx > m) {
                         sum *= ex2_fast((m - mx) * kLog2e);
@@ -326,36 +347,19 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                     }
                     const float mb = m * kLog2e;
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) {
+                    for (int e = 0; e < W; ++e) {
                         const float x = __uint_as_float(r[e]);
                         if (jc + e < V) sum += ex2_fast(fmaf(x, kLog2e, -mb));
                         if (jc + e == tgt) tl[i] = x;
                     }
-                }
-                tc_fence_before();
-                mbar_arrive(tempty + acc);  // the accumulator may take the next tile
-                if (live) {
-                    pm[(size_t)nt * cs + i] = m;
-                    ps[(size_t)nt * cs + i] = sum;
-                }
-            } else {
-                const float lb = live ? lse[i] * kLog2e : 0.f;
-                const int m0 = mt * L::BM;
-#pragma unroll 1
-                for (int c = 0; c < L::BN / 64; ++c, ++nchunk) {
-                    uint32_t r[64];
-                    tmem_ld32x64(tbase + 64 * c, r);
-                    if (c == L::BN / 64 - 1) {  // the accumulator has been read: the next tile may use it
-                        tc_fence_before();
-                        mbar_arrive(tempty + acc);
-                    }
-                    // this chunk's staging tile was last read by the store two chunks ago
-                    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE + (nchunk & 1) * L::GCHUNK);
+                } else {
+                    // this chunk's staging tile was last read by the stores two chunks ago
+                    __nv_bfloat16* stage =
+                        reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE + (nchunk & 1) * L::GCHUNK);
                     if (t == 0 && nchunk >= 2) tma_store_wait_read_le1();
                     asm volatile("bar.sync 1, 128;" ::: "memory");
-                    const int jc = n0 + 64 * c;
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) {
+                    for (int e = 0; e < W; ++e) {
                         float g = 0.f;
                         if (live) {
                             g = ex2_fast(fmaf(__uint_as_float(r[e]), kLog2e, -lb));
@@ -367,10 +371,20 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                     fence_async_smem();
                     asm volatile("bar.sync 1, 128;" ::: "memory");  // the chunk is staged
                     if (t == 0) {
-                        tma_store_3d(&tgrad, stage, m0, jc, 0);
+#pragma unroll
+                        for (int b = 0; b < W / CE_GRAD_BOX; ++b)
+                            tma_store_3d(&tgrad, stage + b * CE_GRAD_BOX * L::BM, m0, jc + b * CE_GRAD_BOX, 0);
                         tma_store_commit();
                     }
+                    ++nchunk;
                 }
+            };
+#pragma unroll 1
+            for (int c = 0; c < NFULL; ++c) chunk(std::integral_constant<int, 64>{}, 64 * c, !TAIL && c == NFULL - 1);
+            if constexpr (TAIL) chunk(std::integral_constant<int, 32>{}, 64 * NFULL, true);
+            if (MODE == 0 && live) {
+                pm[(size_t)nt * cs + i] = m;
+                ps[(size_t)nt * cs + i] = sum;
             }
         }
     }

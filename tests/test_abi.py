@@ -250,12 +250,13 @@ def test_cumsum_workspace_bytes_closed_form(L):
 
 def test_ce_workspace_bytes_closed_form(L):
     """One chunk's vocabulary-major fp32 logits (only when d is not a multiple of 64) and
-    bf16 gradient (the chunk padded to 32 tokens), N floats, two [tiles][chunk] partial arrays (256-row vocabulary tiles), the
-    chunk's target logits and a 32 MiB GEMM workspace, each rounded up to 256 bytes; the
+    bf16 gradient (the chunk padded to 32 tokens), N floats, two [tiles][chunk] partial
+    arrays (a slot per tile of the narrowest vocabulary tile, 192 rows), the chunk's target
+    logits and a 32 MiB GEMM workspace, each rounded up to 256 bytes; the
     chunk is at most N tokens."""
     r = lambda n: (n + 255) // 256 * 256
     for N, V, d, cc in ((512, 50257, 1280, 512), (512, 50257, 1280, 128), (300, 1000, 128, 1000), (1, 7, 8, 4)):
-        cs, ns = (min(cc, N) + 31) // 32 * 32, (V + 255) // 256
+        cs, ns = (min(cc, N) + 31) // 32 * 32, (V + 191) // 192
         logits = 0 if d % 64 == 0 else r(V * cs * 4)  # the fused GEMM keeps the logits off memory
         want = logits + r(V * cs * 2) + r(N * 4) + 2 * r(ns * cs * 4) + r(cs * 4) + (32 << 20)
         assert la.la_ce_workspace_bytes(N, V, d, cc) == want
