@@ -105,8 +105,8 @@ la_ce_lse_part_kernel(const float* LT, int V, int nc, int cs, const int* y, floa
 }
 
 // Token i < nc (one warp per token, 8 per CTA): merge the nslice partial pairs (lane l
-// takes slices l, l + 32, ..., then the lanes meet in a fixed shuffle order) -> lse[i],
-// row_loss[i].
+// takes slices l, l + 32, ..., CE_U of them loaded together and folded in with one
+// rescale; then the lanes meet in a fixed shuffle order) -> lse[i], row_loss[i].
 __global__ void __launch_bounds__(256)
 la_ce_lse_merge_kernel(const float* pm, const float* ps, const float* tl, int nslice, int nc, int cs, int V,
                        const int* y, float* lse, float* row_loss)
@@ -116,7 +116,23 @@ la_ce_lse_merge_kernel(const float* pm, const float* ps, const float* tl, int ns
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (i >= nc) return;
     float m = -INFINITY, s = 0.f;
-    for (int k = lane; k < nslice; k += 32) ce_merge(m, s, pm[(size_t)k * cs + i], ps[(size_t)k * cs + i]);
+    for (int k0 = lane; k0 < nslice; k0 += 32 * CE_U) {
+        float mu[CE_U], su[CE_U];
+#pragma unroll
+        for (int u = 0; u < CE_U; ++u) {
+            const int k = k0 + 32 * u;
+            mu[u] = k < nslice ? pm[(size_t)k * cs + i] : -INFINITY;
+            su[u] = k < nslice ? ps[(size_t)k * cs + i] : 0.f;
+        }
+        float mx = m;
+#pragma unroll
+        for (int u = 0; u < CE_U; ++u) mx = fmaxf(mx, mu[u]);
+        if (mx == -INFINITY) continue;  // nothing yet
+        s *= expf(m - mx);              // (m = -inf: s is 0 and stays 0)
+#pragma unroll
+        for (int u = 0; u < CE_U; ++u) s += su[u] * expf(mu[u] - mx);  // absent slices: 0 * 0
+        m = mx;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
