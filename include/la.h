@@ -245,8 +245,8 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
  * la_ce_workspace_bytes: the device workspace both calls need: the chunk's bf16 gradient
  * (and, when d is not a multiple of 64, its fp32 logits), vocabulary-major with the chunk
  * padded to 32 tokens,
- * N floats, the log-sum-exp partials (2 floats per token and 256-row vocabulary tile) and
- * a 32 MiB GEMM workspace, each at a 256-byte boundary; 0 for a negative or zero size.
+ * N floats, the log-sum-exp partials (2 floats per token and vocabulary tile, counted for
+ * the narrowest tile, 192 rows), the chunk's target logits and a 32 MiB GEMM workspace, each at a 256-byte boundary; 0 for a negative or zero size.
  * No CUDA call.  With d a multiple of 64 the logits are computed on this library's
  * tensor-core kernel and their log-sum-exp (forward) or gradient (backward) taken straight
  * from its accumulator: the logits never reach memory.  Otherwise cuBLAS writes them into
