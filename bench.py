@@ -549,12 +549,13 @@ def measure_other_configs(stream, eps, hbm):
     return out
 
 
-def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=3):
+def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=6):
     """End to end through the C ABI with HOST buffers: every step copies its inputs from
     pinned host memory into a device workspace, runs forward + backward and copies every
-    output back (la_chunked_step_host).  Three streams with a workspace and an output set
-    each let one step's copies overlap the next steps', as a pipelined caller would (two
-    streams measured 5 % slower, four no faster)."""
+    output back (la_chunked_step_host; with page-locked buffers each direction is one
+    copy kernel of the library).  Six streams with a workspace and an output set each let
+    one step's copies overlap the other steps', as a pipelined caller would (three
+    streams measured 4 % slower, four 2 %)."""
     import torch
 
     import causal_linear_attention_gb300 as la
@@ -616,7 +617,8 @@ def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nst
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": job_value(world, G, C, n, secs), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "steps": n, "api": f"la_chunked_step_host (C ABI, pinned host buffers), {nstreams} streams",
+            "steps": n, "api": f"la_chunked_step_host (C ABI, pinned host buffers copied by the library's SM-copy "
+                   f"kernels), {nstreams} streams",
             "host_cpus": f"{len(near)} cpus of the GPU's NUMA node" if near else "unrestricted",
             "copy_gbs": gbs}
 

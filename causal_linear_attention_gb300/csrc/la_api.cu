@@ -25,6 +25,7 @@
 #include "la_fwd_split.cuh"
 #include "la_cumsum.cuh"
 #include "la_ce.cuh"
+#include "la_hostcopy.cuh"
 
 namespace {
 
@@ -1083,6 +1084,59 @@ size_t ws_layout(size_t n_x, size_t n_S, size_t n_z, size_t off[16])
     return at;
 }
 
+// The device mapping of page-locked host memory at p, or nullptr when p is not page-locked
+// or not 16-byte aligned (that memory goes through cudaMemcpyAsync instead).
+void* host_mapping(const void* p)
+{
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return nullptr;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// The step's copies of tensors i0 .. i0 + 7 (those present: dev[i] != nullptr) in one
+// direction: one SM-copy launch when every host side is page-locked and every length a
+// multiple of 16 bytes, else one cudaMemcpyAsync per tensor.
+la_status step_copies(const void* const host[16], void* const dev[16], const size_t bytes[16], int i0,
+                      bool to_device, cudaStream_t s)
+{
+    la::HostCopyList L{};
+    bool mapped = true;
+    for (int i = i0; i < i0 + 8 && mapped; ++i) {
+        if (!dev[i]) continue;
+        void* m = bytes[i] % 16 == 0 ? host_mapping(host[i]) : nullptr;
+        if (!m) {
+            mapped = false;
+            break;
+        }
+        L.src[L.nseg] = static_cast<const uint4*>(to_device ? m : dev[i]);
+        L.dst[L.nseg] = static_cast<uint4*>(to_device ? dev[i] : m);
+        L.n16[L.nseg] = (long long)(bytes[i] / 16);
+        L.total16 += L.n16[L.nseg];
+        ++L.nseg;
+    }
+    if (mapped) {
+        if (L.nseg == 0) return LA_OK;
+        const long long per_block = (long long)la::HC_THREADS * la::HC_UNROLL;
+        const int blocks = (int)std::min<long long>(la::HC_MAX_BLOCKS, (L.total16 + per_block - 1) / per_block);
+        return launch_pdl(la::la_host_copy_kernel, dim3(blocks), la::HC_THREADS, 0, s, L);
+    }
+    for (int i = i0; i < i0 + 8; ++i) {
+        if (!dev[i]) continue;
+        const cudaError_t e = to_device ? cudaMemcpyAsync(dev[i], host[i], bytes[i], cudaMemcpyHostToDevice, s)
+                                        : cudaMemcpyAsync(const_cast<void*>(host[i]), dev[i], bytes[i],
+                                                          cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_CUDA;
+        }
+    }
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" size_t la_step_workspace_bytes(int G, int C, int D, la_dtype dtype)
@@ -1123,11 +1177,8 @@ extern "C" la_status la_chunked_step_host(const void* q, const void* k, const vo
     void* dev[16];
     for (int i = 0; i < 16; ++i) dev[i] = host[i] && bytes[i] ? ws + off[i] : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    for (int i = 0; i < 8; ++i)
-        if (dev[i] && cudaMemcpyAsync(dev[i], host[i], bytes[i], cudaMemcpyHostToDevice, s) != cudaSuccess) {
-            cudaGetLastError();
-            return LA_ERR_CUDA;
-        }
+    st = step_copies(host, dev, bytes, 0, true, s);
+    if (st != LA_OK) return st;
     auto F = [](void* p) { return static_cast<float*>(p); };
     st = la_chunked_fwd(dev[0], dev[1], dev[2], F(dev[4]), F(dev[5]), dev[8], F(dev[12]), F(dev[13]), G, C, D, block,
                         dtype, eps, stream);
@@ -1135,13 +1186,7 @@ extern "C" la_status la_chunked_step_host(const void* q, const void* k, const vo
     st = la_chunked_bwd(dev[0], dev[1], dev[2], F(dev[4]), F(dev[5]), dev[3], F(dev[6]), F(dev[7]), dev[9], dev[10],
                         dev[11], F(dev[14]), F(dev[15]), G, C, D, block, dtype, eps, stream);
     if (st != LA_OK) return st;
-    for (int i = 8; i < 16; ++i)
-        if (dev[i] && cudaMemcpyAsync(const_cast<void*>(host[i]), dev[i], bytes[i], cudaMemcpyDeviceToHost, s) !=
-                          cudaSuccess) {
-            cudaGetLastError();
-            return LA_ERR_CUDA;
-        }
-    return LA_OK;
+    return step_copies(host, dev, bytes, 8, false, s);
 }
 
 extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)

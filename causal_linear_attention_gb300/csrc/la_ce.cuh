@@ -334,7 +334,9 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
             const int m0 = mt * L::BM, i = m0 + t, n0 = nt * L::BN;
             const bool live = i < nc;
             const int tgt = live ? y[i] : -1;
-            if (!mbar_wait(tfull + acc, (lt >> 1) & 1, ERR_TIMEOUT_MMA)) break;
+            const bool late = !mbar_wait(tfull + acc, (lt >> 1) & 1, ERR_TIMEOUT_MMA);
+            // MODE 1's threads meet at named barriers below: they leave together or not at all
+            if (MODE == 1 ? bar_sync_any(1, 128, late) : late) break;
             tc_fence_after();
             const uint32_t tbase = tmem + lane_base + acc * L::ACC_COLS;
             float m = -INFINITY, sum = 0.f;                                // MODE 0: online (max, sum)

@@ -81,6 +81,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     return true;
 }
 
+// Named barrier `id` over `nthreads` threads that also returns whether any of them passed
+// true: lets a group of threads that share named barriers agree to leave a loop together
+// after a bounded wait gave up for some of them.
+__device__ __forceinline__ bool bar_sync_any(uint32_t id, uint32_t nthreads, bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+        " bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+        : "=r"(r) : "r"(p ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever
 // arrives at; the wait must give up after `limit_ns` and the kernel return normally.
 __global__ void la_selftest_wait_kernel(unsigned long long limit_ns)

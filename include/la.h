@@ -283,14 +283,17 @@ la_status la_ce_bwd(const void* h, const void* W, const int* targets, const floa
  * room for every input and output tensor, each at a 256-byte boundary; 0 when the
  * shape or dtype is invalid or unsupported.  It makes no CUDA call.
  *
- * la_chunked_step_host enqueues on `stream`, in this order: one cudaMemcpyAsync per
- * present input (q, k, v, S0, z0, dO, dS_out, dz_out; host -> workspace), the
- * la_chunked_fwd and la_chunked_bwd launches on those copies, and one cudaMemcpyAsync
- * per requested output (o, S_out, z_out, dq, dk, dv, dS0, dz0; workspace -> host).
+ * la_chunked_step_host enqueues on `stream`, in this order: the copies of the present
+ * inputs (q, k, v, S0, z0, dO, dS_out, dz_out; host -> workspace), the la_chunked_fwd
+ * and la_chunked_bwd launches on those copies, and the copies of the requested outputs
+ * (o, S_out, z_out, dq, dk, dv, dS0, dz0; workspace -> host).  The copies of one
+ * direction are a single kernel of this library that reads (or writes) the host side
+ * through its device mapping when every host tensor of that direction is page-locked
+ * (cudaHostAlloc / cudaHostRegister, as cudaPointerGetAttributes reports it) and
+ * 16-byte aligned; otherwise one cudaMemcpyAsync per tensor.
  *   - Every tensor pointer is HOST memory with the layouts above.  Page-locked memory
- *     (cudaHostAlloc / cudaHostRegister) keeps the copies asynchronous; pageable
- *     memory works, but then the copies synchronise with the host.  The outputs are
- *     valid once the stream has completed.
+ *     keeps the step asynchronous; pageable memory works, but then the copies
+ *     synchronise with the host.  The outputs are valid once the stream has completed.
  *   - S0, z0, dS_out, dz_out may be NULL (zeros); S_out, z_out, dS0, dz0 may be NULL
  *     (not computed).  q, k, v, dO, o, dq, dk, dv are required when G * C > 0.
  *     S_out may equal S0, z_out z0, dS0 dS_out and dz0 dz_out (the inputs are copied

@@ -81,6 +81,34 @@ def test_host_step_pageable_memory_and_absent_carries():
     check(got[3:6], bo[:3], "bf16", ("dq", "dk", "dv"))
 
 
+def test_host_step_mixed_memory_kinds():
+    """Page-locked inputs with pageable outputs, and a page-locked input that is not 16-byte
+    aligned: each direction takes the kernel copy only when all of its host tensors allow
+    it, and the results are the same either way."""
+    x = make_inputs(7, 96, 64, dtype="bf16", seed=6, grads=True)
+    ref = run_device(x, 64)
+    pin = {k: t.pin_memory() for k, t in x.__dict__.items()}
+    ws = la.step_workspace(7, 96, 64, torch.bfloat16, DEV)
+    s = torch.cuda.Stream(device=DEV)
+    out = host_outputs(x, False)
+    la.chunked_step_host(pin["q"], pin["k"], pin["v"], pin["S0"], pin["z0"], pin["dO"], pin["dS_out"],
+                         pin["dz_out"], out=out, workspace=ws, block=64, eps=EPS, stream=s)
+    s.synchronize()
+    for n, a, b in zip(NAMES, out, ref):
+        assert torch.equal(a, b), n
+    # v 8 bytes past a 16-byte boundary of a page-locked buffer
+    buf = torch.empty(x.v.numel() + 4, dtype=torch.bfloat16, pin_memory=True)
+    v_odd = buf[4:].view(x.v.shape)
+    v_odd.copy_(x.v)
+    assert v_odd.data_ptr() % 16 == 8
+    out2 = host_outputs(x, True)
+    la.chunked_step_host(pin["q"], pin["k"], v_odd, pin["S0"], pin["z0"], pin["dO"], pin["dS_out"],
+                         pin["dz_out"], out=out2, workspace=ws, block=64, eps=EPS, stream=s)
+    s.synchronize()
+    for n, a, b in zip(NAMES, out2, ref):
+        assert torch.equal(a, b), n
+
+
 def test_host_step_in_place_carry():
     """S_out may be the S0 buffer and dS0 the dS_out buffer: the inputs are copied in first."""
     x = make_inputs(5, 128, 64, dtype="bf16", seed=4, grads=True)
