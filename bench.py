@@ -549,13 +549,13 @@ def measure_other_configs(stream, eps, hbm):
     return out
 
 
-def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=6):
+def run_e2e(args, host, G, C, D, block, eps, local, barrier, max_over_ranks, nstreams=8):
     """End to end through the C ABI with HOST buffers: every step copies its inputs from
     pinned host memory into a device workspace, runs forward + backward and copies every
     output back (la_chunked_step_host; with page-locked buffers each direction is one
-    copy kernel of the library).  Six streams with a workspace and an output set each let
-    one step's copies overlap the other steps', as a pipelined caller would (three
-    streams measured 4 % slower, four 2 %)."""
+    copy kernel of the library).  Eight streams with a workspace and an output set each
+    let one step's copies overlap the other steps', as a pipelined caller would (six
+    streams measured 4 % slower, four 10 %, twelve the same)."""
     import torch
 
     import causal_linear_attention_gb300 as la

@@ -7,7 +7,9 @@
 // step for 8 + 8 transfers against 102 us for one transfer each way).  One kernel per
 // direction instead reads (or writes) the host side through its device mapping,
 // 16 bytes per access, with four accesses in flight per thread: 79 us host -> device,
-// 86 us device -> host, 103 us with both directions running at once.
+// 86 us device -> host, 103 us with both directions running at once (64 CTAs; 16 CTAs
+// reach 82 us host -> device).  In the pipelined step fewer CTAs leave more of the SMs
+// to the step's own kernels: 114 us per step with 16 CTAs against 119 with 32 or 64.
 #pragma once
 #include <stdint.h>
 
@@ -17,7 +19,7 @@ namespace la {
 
 constexpr int HC_MAX_SEGS = 8;      // tensors per launch
 constexpr int HC_THREADS = 512;
-constexpr int HC_MAX_BLOCKS = 64;   // enough to keep the host link busy in both directions
+constexpr int HC_MAX_BLOCKS = 16;   // enough to keep the host link busy
 constexpr int HC_UNROLL = 4;        // 16-byte accesses in flight per thread
 
 // A list of (source, destination, length) copies, lengths in 16-byte units; either side
