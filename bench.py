@@ -45,6 +45,10 @@ NCU_TRAFFIC = {
 }
 
 
+# GB300's nominal HBM3e bandwidth (GB/s), reported beside the measured copy rate.
+NOMINAL_HBM_GBS = 7900.0
+
+
 # The headers that make up each timed kernel (its body and everything it includes).
 KERNEL_FILES = {
     "la_fwd": ("la_fwd_tc.cuh", "la_tc.cuh", "la_device.cuh"),
@@ -380,7 +384,8 @@ def run_ours(args, rank, world, local):
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(kernels[dom]["gbs"], 1), "peak": hbm,
             "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / hbm, 4), "peak_source": peak_src,
             "traffic": traffic["bytes"] if traffic and traffic["src"] == src_hash else None,
-            "alg_bytes": kernels[dom]["alg_bytes"]}
+            "alg_bytes": kernels[dom]["alg_bytes"],
+            "frac_of_nominal": round(kernels[dom]["gbs"] / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS}
     for k in kernels:
         kernels[k]["frac"] = round(kernels[k]["gbs"] / hbm, 4)
         kernels[k]["avg_us"] = round(kernels[k]["avg_us"], 3)
@@ -446,12 +451,19 @@ def gpu_local_cpus(local):
 
 
 # The other workloads (parity cases in tests/), measured the same way as the headline's
-# per-kernel numbers, for context: (name, G, C, D, block, directions)
+# per-kernel numbers, for context: (name, G, C, D, block, directions, implementation).
+# "threaded" runs the C tokens as C / 128 launches of 128 tokens each, the carry passed
+# from launch to launch in place; its bytes count every launch's carry round trip.
+THREAD_CHUNK = 128
 OTHER_CONFIGS = (
     ("batch16_fwdbwd: G=640, C=128, D=64, block=64, bf16", 640, 128, 64, 64, ("fwd", "bwd"), "chunked"),
     ("long_stream_fwd: G=160, T=8192 as one C=8192 launch, D=64, bf16", 160, 8192, 64, 64, ("fwd",), "chunked"),
+    ("long_stream_threaded_fwd: G=160, T=8192 as 64 launches of C=128, carry threaded in place, D=64, bf16", 160,
+     8192, 64, 64, ("fwd",), "threaded"),
     ("wide_heads_fwdbwd: G=320, C=256, D=128, block=64, bf16", 320, 256, 128, 64, ("fwd", "bwd"), "chunked"),
     ("wide_heads_ragged_fwdbwd: G=320, C=200, D=128, block=64, bf16", 320, 200, 128, 64, ("fwd", "bwd"), "chunked"),
+    ("wide_heads_block128_fwdbwd: G=320, C=256, D=128, block=128, bf16", 320, 256, 128, 128, ("fwd", "bwd"),
+     "chunked"),
     ("cumsum_form_fwdbwd: G=160, C=128, D=64, bf16, token-by-token scan", 160, 128, 64, 64, ("fwd", "bwd"),
      "cumsum"),
 )
@@ -486,6 +498,9 @@ def measure_other_configs(stream, eps, hbm):
     for name, G, C, D, block, dirs, impl in OTHER_CONFIGS:
         x = make_inputs(G, C, D, dtype="bf16", seed=rank_seed(0), grads="bwd" in dirs).to(dev)
         fb, bb = algorithmic_bytes(G, C, D, 2)
+        if impl == "threaded":
+            nch = C // THREAD_CHUNK
+            fb = nch * algorithmic_bytes(G, THREAD_CHUNK, D, 2)[0]
         nsets = max(1, min(8, -(-4 * l2 // (fb + (bb if "bwd" in dirs else 0)))))
         sets = []
         for _ in range(nsets):
@@ -496,6 +511,10 @@ def measure_other_configs(stream, eps, hbm):
             ws = None
             if impl == "cumsum" and "bwd" in dirs:
                 ws = torch.empty(la.la_cumsum_bwd_workspace_bytes(G, C, D, la.LA_BF16), dtype=torch.uint8, device=dev)
+            if impl == "threaded":  # contiguous [G][128][D] pieces of q, k, v; o as 64 pieces
+                for key in ("q", "k", "v"):
+                    d[key] = [t.contiguous() for t in d[key].split(THREAD_CHUNK, dim=1)]
+                o = ([t.contiguous() for t in o[0].split(THREAD_CHUNK, dim=1)], o[1], o[2])
             sets.append((d, o, gr, ws))
         entry = {"G": G, "C": C, "D": D, "block": block, "impl": impl}
         for direction in dirs:
@@ -503,6 +522,10 @@ def measure_other_configs(stream, eps, hbm):
                 d, o, gr, ws = sets[i % nsets]
                 if impl == "cumsum" and direction == "fwd":
                     la.cumsum_fwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], eps=eps, o=o[0], S_out=o[1], z_out=o[2])
+                elif impl == "threaded":  # the first piece reads S0, z0; the rest the carry in place
+                    for c, (qc, kc, vc, oc) in enumerate(zip(d["q"], d["k"], d["v"], o[0])):
+                        S_in, z_in = (d["S0"], d["z0"]) if c == 0 else (o[1], o[2])
+                        la.chunked_fwd(qc, kc, vc, S_in, z_in, block=block, eps=eps, o=oc, S_out=o[1], z_out=o[2])
                 elif impl == "cumsum":
                     la.cumsum_bwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], d["dO"], d["dS_out"], d["dz_out"],
                                   eps=eps, out=gr, workspace=ws)
