@@ -142,6 +142,21 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // The tiles and the carries start towards L2 while the previous kernel in the stream
+    // finishes.  A prefetch hands nothing to this kernel, and L2 is where that kernel's
+    // writes land, so the loads after the wait still read what it wrote.
+    if (C > 0 && warp == 4 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&tg);
+        tma_prefetch_3d(&tq, 0, 0, (int)g);
+        tma_prefetch_3d(&tk, 0, 0, (int)g);
+        tma_prefetch_3d(&tg, 0, 0, (int)g);
+        tma_prefetch_3d(&tv, 0, 0, (int)g);
+        if (S0) prefetch_l2(S0 + g * D * D, 16384);
+        if (dS_out) prefetch_l2(dS_out + g * D * D, 16384);
+    }
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
     if (C == 0) {  // empty chunk: the carry gradients pass straight through
@@ -153,16 +168,10 @@ la_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     } else if (warp == 4) {
         // =================================================== producer (one lane)
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            prefetch_tmap(&tg);
             // in the order the work needs them: Q, K (M1), the carries (E1), dO (E1), V (M2)
             mbar_expect_tx(bar_qk, L::LOAD_BYTES / 2);
             tma_load_3d(sm + L::QT, &tq, bar_qk, 0, 0, (int)g);
             tma_load_3d(sm + L::KT, &tk, bar_qk, 0, 0, (int)g);
-            if (S0) prefetch_l2(S0 + g * D * D, 16384);
-            if (dS_out) prefetch_l2(dS_out + g * D * D, 16384);
             // (with neither z0 nor dz_out this arrival alone completes the phase)
             mbar_expect_tx(bar_aux, (z0 ? 256u : 0u) + (dz_out ? 256u : 0u));
             if (z0) bulk_load(sm + L::Z0, z0 + g * D, 256, bar_aux);

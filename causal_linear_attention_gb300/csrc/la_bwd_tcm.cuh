@@ -234,6 +234,25 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // The first tile and the carries start towards L2 while the previous kernel in the
+    // stream finishes.  A prefetch hands nothing to this kernel, and L2 is where that
+    // kernel's writes land, so the loads after the wait still read what it wrote.
+    if (nsb > 0 && warp == 8 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&tg);
+        const int row = rbase + (mode == 2 ? nsb - 1 : 0) * 128;  // the tile the first pass starts on
+#pragma unroll
+        for (int a = 0; a < NA; ++a) {
+            tma_prefetch_3d(&tq, 64 * a, row, (int)g);
+            tma_prefetch_3d(&tk, 64 * a, row, (int)g);
+            tma_prefetch_3d(&tg, 64 * a, row, (int)g);
+            tma_prefetch_3d(&tv, 64 * a, row, (int)g);
+        }
+        if (Ssrc) prefetch_l2(Ssrc, D * D * 4);
+        if (Rsrc) prefetch_l2(Rsrc, D * D * 4);
+    }
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
     if (nsb == 0) {  // empty chunk: the carry gradients pass straight through
@@ -245,10 +264,6 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     } else if (warp == 8) {
         // =================================================== producer (one lane)
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            prefetch_tmap(&tg);
             auto load = [&](int b) {
                 mbar_expect_tx(bar_qk, L::HALF_BYTES);
 #pragma unroll

@@ -163,15 +163,25 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // The first tile and the carry start towards L2 while the previous kernel in the stream
+    // finishes.  A prefetch hands nothing to this kernel, and L2 is where that kernel's
+    // writes land, so the loads after the wait still read what it wrote.
+    if (warp == 4 && lane == 0 && nsb > 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&to);
+        tma_prefetch_3d(&tq, 0, rbase, g);
+        tma_prefetch_3d(&tk, 0, rbase, g);
+        tma_prefetch_3d(&tv, 0, rbase, g);
+        if (S0g) prefetch_l2(S0g, 16384);
+        if (z0g) prefetch_l2(z0g, 256);
+    }
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
     if (warp == 4) {
         // =================================================== producer (one lane)
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            prefetch_tmap(&to);
             auto issue_qk = [&](int sb) {
                 mbar_expect_tx(bar_qk, L::LOAD_BYTES / 3 * 2);
                 tma_load_3d(sm + L::QT, &tq, bar_qk, 0, rbase + sb * 128, g);

@@ -127,15 +127,27 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // The first tile and the carry start towards L2 while the previous kernel in the stream
+    // finishes.  A prefetch hands nothing to this kernel, and L2 is where that kernel's
+    // writes land, so the loads after the wait still read what it wrote.
+    if (warp == 4 && lane == 0 && nsb > 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&to);
+        for (int a = 0; a < 2; ++a) {
+            tma_prefetch_3d(&tq, 64 * a, 0, g);
+            tma_prefetch_3d(&tk, 64 * a, 0, g);
+            tma_prefetch_3d(&tv, 64 * a, 0, g);
+        }
+        if (S0) prefetch_l2(S0 + (size_t)g * D * D, 65536);
+        if (z0) prefetch_l2(z0 + (size_t)g * D, 512);
+    }
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
     if (warp == 4) {
         // =================================================== producer (one lane)
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            prefetch_tmap(&to);
             auto issue_qk = [&](int sb) {
                 mbar_expect_tx(bar_qk, L::QK_BYTES);
                 tma_load_3d(sm + L::QT, &tq, bar_qk, 0, sb * 128, g);
