@@ -245,7 +245,8 @@ def la_bwd_max_c(D: int, block: int, dtype: int) -> int:
 
 def la_device_status(clear: bool = True) -> int:
     """Synchronise the device; LA_ERR_TIMEOUT (4) if a kernel gave up a bounded wait,
-    LA_ERR_DEVICE (5) if one found its shared memory misaligned and did nothing."""
+    LA_ERR_DEVICE (5) if one found its shared memory misaligned (and did nothing) or a
+    cross-entropy target was outside [0, V)."""
     return int(lib().la_device_status(1 if clear else 0))
 
 
