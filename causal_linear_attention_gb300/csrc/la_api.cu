@@ -774,16 +774,17 @@ int ce_slices(int V) { return (V + kCeTileWidths[2] - 1) / kCeTileWidths[2]; }
 bool ce_fused(int d) { return d % 64 == 0; }
 
 // The fused GEMM's tile width for mtiles token tiles: the one whose whole waves over the
-// SMs (one persistent CTA each) cover the fewest vocabulary columns; ties go to the wider
-// tile (fewer, larger UMMAs per byte loaded).
-int ce_tile_width(int mtiles, int V, int sms)
+// SMs (one persistent CTA each) cover the fewest vocabulary columns.  Ties go to the wider
+// tile (fewer, larger UMMAs per byte loaded), or with `narrow` to the narrower one (the
+// backward: beside its gradient staging a 192-row tile leaves room for a fifth TMA stage).
+int ce_tile_width(int mtiles, int V, int sms, bool narrow = false)
 {
     int best = kCeTileWidths[0];
     long long best_cost = -1;
     for (int bn : kCeTileWidths) {
         const long long tiles = (long long)mtiles * ((V + bn - 1) / bn);
         const long long cost = (tiles + sms - 1) / sms * bn;
-        if (best_cost < 0 || cost < best_cost) {
+        if (best_cost < 0 || cost < best_cost || (narrow && cost == best_cost)) {
             best = bn;
             best_cost = cost;
         }
@@ -825,7 +826,7 @@ la_status ce_persist_launch_bn(const CUtensorMap& th, const CUtensorMap& tw, con
                                int cs, int V, int d, int sms, const int* y, float* pm, float* ps, float* tl,
                                const float* lse, float scale, cudaStream_t s)
 {
-    using PL = la::CePersistLayout<BN>;
+    using PL = la::CePersistLayout<BN, MODE>;
     static_assert(PL::BM == kCeTokTile, "token tile");
     static OptIn flag;
     auto kern = la::la_ce_persist_kernel<MODE, BN>;
@@ -1029,7 +1030,7 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     // the backward's tiles cover all cs token columns of every chunk: one tile width
     const int sms = sm_count();
     if (sms <= 0) return LA_ERR_CUDA;
-    const int bn = ce_tile_width(ce_mtiles<1>(cc, cs), V, sms);
+    const int bn = ce_tile_width(ce_mtiles<1>(cc, cs), V, sms, true);
     CUtensorMap th{}, tw{}, tgt{};
     if (fused && (!ce_maps(h, W, N, V, d, bn, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt))) return LA_ERR_CUDA;
     CublasUse cb(s, ws + off[6]);

@@ -205,7 +205,9 @@ la_ce_grad_kernel(const float* LT, int V, int nc, int cs, const int* y, const fl
 // slices (both operands K-major: h rows and W rows), one CTA per SM looping over the tiles
 // (token tile fastest, so the CTAs that share a slice of W run at the same time), with two
 // TMEM accumulators: the epilogue of one tile runs while the UMMAs of the next fill the
-// other, and the 4-stage TMA ring runs on across tiles.  BN is 256, 224 or 192: the host
+// other, and the TMA ring runs on across tiles: as many stages as fit beside the
+// backward's 16 KB gradient staging (5 at BN = 224 or 192, 4 at 256; a fifth stage took
+// the forward from 53.4 to 49.2 us on the tied 50257-row head: the ring's lookahead binds).  BN is 256, 224 or 192: the host
 // takes the one whose whole waves of tiles over the SMs cost least (V = 50257 in chunks of
 // 512 tokens: 788 tiles of 256 rows are 5.2 waves on 152 SMs, 900 of 224 rows 5.9).
 // Epilogue by MODE, in chunks of 64 accumulator columns (and one of 32 when BN = 224):
@@ -214,19 +216,23 @@ la_ce_grad_kernel(const float* LT, int V, int nc, int cs, const int* y, const fl
 //          then merges the tiles): the chunk's logits never reach memory;
 //   MODE 1 (backward): G = (exp(logit - lse) - [j == y]) scale -> GT[j][i] (bf16,
 //          vocabulary-major, zero for the chunk's padding tokens), a chunk at a time
-//          through two shared-memory tiles that leave in TMA stores (tgrad: GT as [V][cs],
+//          through a shared-memory tile that leaves in TMA stores (tgrad: GT as [V][cs],
 //          128 x 32 boxes; rows past V and tokens past cs are clipped).
 // Barriers: full / empty per stage (TMA -> UMMA -> TMA), tfull / tempty per accumulator
 // (UMMA commit -> epilogue, 128 epilogue arrivals -> UMMA).
-template <int BN_>
+template <int BN_, int MODE_>
 struct CePersistLayout {
     static_assert(BN_ % 32 == 0 && BN_ >= 64 && BN_ <= 256, "vocabulary tile");
-    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = 4;
+    static constexpr int BM = 128, BN = BN_, BK = 64;
     static constexpr uint32_t A_BYTES = BM * BK * 2;                // 16 KB
     static constexpr uint32_t STAGE_BYTES = A_BYTES + BN * BK * 2;  // 48 KB at BN = 256
-    static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;        // 2 x 16 KB: gradient chunks [64][128] bf16
-    static constexpr uint32_t GCHUNK = 64 * BM * 2;
-    static constexpr uint32_t BARS = GSTAGE + 2 * GCHUNK;
+    static constexpr uint32_t GCHUNK = 64 * BM * 2;                 // a gradient chunk [64][128] bf16
+    static constexpr uint32_t G_BYTES = MODE_ == 1 ? GCHUNK : 0;
+    // as many ring stages as fit beside the gradient staging (at most 6)
+    static constexpr int STAGES_FIT = (int)((227u * 1024u - 256u - G_BYTES) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT < 6 ? STAGES_FIT : 6;
+    static constexpr uint32_t GSTAGE = STAGES * STAGE_BYTES;
+    static constexpr uint32_t BARS = GSTAGE + G_BYTES;
     static constexpr uint32_t BYTES = BARS + 256;
     static constexpr uint32_t ACC_COLS = 256;                       // accumulator a at TMEM column 256 a
     static constexpr uint32_t TMEM_COLS = 512;
@@ -241,7 +247,7 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                      const __grid_constant__ CUtensorMap tgrad, int c0, int nc, int cs, int V, int KB, int mtiles,
                      int ntiles, const int* y, float* pm, float* ps, float* tl, const float* lse, float scale)
 {
-    using L = CePersistLayout<BN>;
+    using L = CePersistLayout<BN, MODE>;
     using namespace tc;
     extern __shared__ __align__(1024) unsigned char sm[];
     if (smem_addr(sm) & 1023u) {
@@ -371,10 +377,9 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
                         if (jc + e == tgt) tl[i] = x;
                     }
                 } else {
-                    // this chunk's staging tile was last read by the stores two chunks ago
-                    __nv_bfloat16* stage =
-                        reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE + (nchunk & 1) * L::GCHUNK);
-                    if (t == 0 && nchunk >= 2) tma_store_wait_read_le1();
+                    // the staging tile is free once the previous chunk's stores have read it
+                    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + L::GSTAGE);
+                    if (t == 0 && nchunk >= 1) tma_store_wait_read();
                     asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
                     for (int e = 0; e < W; ++e) {
