@@ -220,6 +220,11 @@ la_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int kk = 0; kk < 4; ++kk)  // I1a: A = Q K^T
                     umma_bf16(tmem + L::T_SCORE, dQ + kk * 2, dKS + kk * 2, id_qk, kk > 0);
                 umma_commit(bar_mma1);
+                if (sb + 1 < nsb) {  // the next tile towards L2 while this one computes
+                    tma_prefetch_3d(&tq, 0, rbase + (sb + 1) * 128, g);
+                    tma_prefetch_3d(&tk, 0, rbase + (sb + 1) * 128, g);
+                    tma_prefetch_3d(&tv, 0, rbase + (sb + 1) * 128, g);
+                }
                 // incoming state published (first block: carry-in; later: previous block's EPI2)
                 ok = mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
                 if (!ok) break;

@@ -192,6 +192,12 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 for (int kk = 0; kk < 8; ++kk)  // I1a: A = Q K^T
                     umma_bf16(tmem + L::T_SCORE, kstep(dQ, kk), kstep(dK, kk), id_kk, kk > 0);
                 umma_commit(bar_mma1);
+                if (sb + 1 < nsb)  // the next tile towards L2 while this one computes
+                    for (int a = 0; a < 2; ++a) {
+                        tma_prefetch_3d(&tq, 64 * a, (sb + 1) * 128, g);
+                        tma_prefetch_3d(&tk, 64 * a, (sb + 1) * 128, g);
+                        tma_prefetch_3d(&tv, 64 * a, (sb + 1) * 128, g);
+                    }
                 // the block's incoming state (first block: the carry-in; later: the previous EPI2)
                 ok = mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
                 if (!ok) break;
