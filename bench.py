@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of each kernel on this workload, with the hash of the kernel sources they were taken on
 # (profiles/la_*_tc_fractus1b_G160_C128_D64.md).  Reported as null once the sources differ.
 NCU_TRAFFIC = {
-    "la_fwd": {"bytes": 10574336 + 0, "src": "2089828d383a1f5c"},
-    "la_bwd": {"bytes": 15887360 + 0, "src": "65faeb3f84575bc7"},
+    "la_fwd": {"bytes": 10575360 + 0, "src": "fa57fb186ae1323a"},
+    "la_bwd": {"bytes": 15884928 + 0, "src": "f344e290658b28ea"},
 }
 
 
