@@ -19,6 +19,7 @@
 #include "la_bwd.cuh"
 #include "la_fwd.cuh"
 #include "la_fwd_tc.cuh"
+#include "la_fwd_tile.cuh"
 #include "la_bwd_tc.cuh"
 #include "la_fwd_tc128.cuh"
 #include "la_bwd_tcm.cuh"
@@ -199,6 +200,21 @@ la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float
     }
     return launch_pdl(kern, G * P, la::FwdTcLayout::THREADS, la::FwdTcLayout::BYTES, stream, tq, tk, tv, to, S0, z0,
                       S_out, z_out, C, eps, P, PL, piece_carry);
+}
+
+// The bf16 head-size-64 forward of a chunk that fits one 128-token tile (1 <= C <= 128).
+la_status fwd_tile_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
+                          float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    static OptIn flag;
+    auto kern = la::la_fwd_tile_kernel;
+    const la_status st = prepare(kern, flag, la::FwdTileLayout::BYTES);
+    if (st != LA_OK) return st;
+    CUtensorMap tq{}, tk{}, tv{};
+    if (!tmap_bf16(&tq, q, G, C, 64, 128) || !tmap_bf16(&tk, k, G, C, 64, 128) || !tmap_bf16(&tv, v, G, C, 64, 128))
+        return LA_ERR_CUDA;
+    return launch_pdl(kern, G, la::FwdTileLayout::THREADS, la::FwdTileLayout::BYTES, stream, tq, tk, tv, o, S0, z0,
+                      S_out, z_out, C, eps);
 }
 
 la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
@@ -390,7 +406,11 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
 
     // bf16, head size 64: the tensor-core (tcgen05 / TMEM / TMA) kernel, 128-token score
     // tiles for either block size (the block size changes only the rounding)
-    if (dtype == LA_BF16 && D == 64) return fwd_tc_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+    if (dtype == LA_BF16 && D == 64) {
+        if (C >= 1 && C <= la::FwdTileLayout::MAX_C)
+            return fwd_tile_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+        return fwd_tc_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
+    }
     if (dtype == LA_BF16 && D == 128) return fwd_tc128_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
 
 #define LA_FWD_CASE(DT, P, DD, BB, NW, ST)                                                                  \
