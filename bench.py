@@ -54,7 +54,7 @@ NOMINAL_HBM_GBS = 7900.0
 # The headers that make up each timed kernel (its body and everything it includes).
 KERNEL_FILES = {
     "la_fwd": ("la_fwd_tile.cuh", "la_fwd_tc.cuh", "la_tc.cuh", "la_device.cuh"),
-    "la_bwd": ("la_bwd_tc.cuh", "la_fwd_tc.cuh", "la_tc.cuh", "la_device.cuh"),
+    "la_bwd": ("la_bwd_tile.cuh", "la_fwd_tc.cuh", "la_tc.cuh", "la_device.cuh"),
 }
 
 

@@ -22,7 +22,7 @@ from ._lib import (LA_BF16, LA_F32, LAError, build, la_bwd_max_c, la_bwd_split_w
                    la_chunked_bwd_split, la_chunked_fwd, la_chunked_fwd_split, la_chunked_fwd_split_static,
                    la_ce_bwd, la_ce_fwd, la_ce_workspace_bytes, la_chunked_step_host, la_cumsum_bwd,
                    la_cumsum_bwd_workspace_bytes, la_cumsum_fwd,
-                   la_device_status, la_fwd_split_workspace_bytes,
+                   la_device_status, la_fwd_split_workspace_bytes, la_host_copy_eligible,
                    la_selftest_bounded_wait, la_status_string, la_step_workspace_bytes, la_version, lib)
 
 __all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_bwd_split", "chunked_step_host",
@@ -30,7 +30,8 @@ __all__ = ["chunked_fwd", "chunked_fwd_split", "chunked_bwd", "chunked_bwd_split
            "la_fwd_split_workspace_bytes", "la_chunked_bwd", "la_chunked_bwd_split", "la_bwd_split_workspace_bytes",
            "cumsum_fwd", "cumsum_bwd", "la_cumsum_fwd", "la_cumsum_bwd", "la_cumsum_bwd_workspace_bytes",
            "ce_workspace", "ce_fwd", "ce_bwd", "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
-           "la_chunked_step_host", "la_step_workspace_bytes", "la_bwd_max_c", "la_device_status",
+           "la_chunked_step_host", "la_step_workspace_bytes", "la_host_copy_eligible", "la_bwd_max_c",
+           "la_device_status",
            "la_selftest_bounded_wait",
            "la_status_string", "la_version", "build", "lib", "LAError", "LA_F32", "LA_BF16"]
 

@@ -87,6 +87,8 @@ def lib():
         L.la_step_workspace_bytes.restype = ctypes.c_size_t
         L.la_chunked_step_host.argtypes = [P] * 17 + [ctypes.c_size_t, I, I, I, I, I, F, P]
         L.la_chunked_step_host.restype = I
+        L.la_host_copy_eligible.argtypes = [P, ctypes.c_size_t]
+        L.la_host_copy_eligible.restype = I
         L.la_fwd_split_workspace_bytes.argtypes = [I, I, I, I]
         L.la_fwd_split_workspace_bytes.restype = ctypes.c_size_t
         L.la_chunked_fwd_split.argtypes = [P] * 8 + [I, I, I, I, I, F, P, ctypes.c_size_t, P]
@@ -125,7 +127,7 @@ EXPORTS = ("la_chunked_fwd", "la_chunked_bwd", "la_fwd_split_workspace_bytes", "
            "la_chunked_fwd_split_static", "la_bwd_split_workspace_bytes", "la_chunked_bwd_split",
            "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
            "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
-           "la_step_workspace_bytes", "la_chunked_step_host", "la_bwd_max_c",
+           "la_step_workspace_bytes", "la_chunked_step_host", "la_host_copy_eligible", "la_bwd_max_c",
            "la_device_status", "la_selftest_bounded_wait", "la_status_string", "la_version")
 
 
@@ -228,6 +230,11 @@ def la_chunked_fwd_split_static(q, k, v, S0, z0, o, S_out, z_out, G: int, C: int
 
 def la_step_workspace_bytes(G: int, C: int, D: int, dtype: int) -> int:
     return int(lib().la_step_workspace_bytes(G, C, D, dtype))
+
+
+def la_host_copy_eligible(ptr: int, nbytes: int) -> int:
+    """1 when la_chunked_step_host would move this host buffer with its SM-copy kernel."""
+    return int(lib().la_host_copy_eligible(ctypes.c_void_p(ptr), nbytes))
 
 
 def la_chunked_step_host(q, k, v, S0, z0, dO, dS_out, dz_out, o, S_out, z_out, dq, dk, dv, dS0, dz0,

@@ -20,7 +20,7 @@
 #include "la_fwd.cuh"
 #include "la_fwd_tc.cuh"
 #include "la_fwd_tile.cuh"
-#include "la_bwd_tc.cuh"
+#include "la_bwd_tile.cuh"
 #include "la_fwd_tc128.cuh"
 #include "la_bwd_tcm.cuh"
 #include "la_fwd_split.cuh"
@@ -166,21 +166,6 @@ bool tmap_bf16(CUtensorMap* map, const void* base, int G, int C, int D, int box_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [G][D][D] fp32 carry seen as a 3-D map (x = value column, y = key row, z = group); boxes
-// of 32 columns (128 bytes) x D rows, 128-byte swizzle.
-bool tmap_state_f32(CUtensorMap* map, const float* base, int G, int D)
-{
-    auto enc = tmap_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)G};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
-    cuuint32_t box[3] = {32u, (cuuint32_t)D, 1u};
-    cuuint32_t es[3] = {1u, 1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The bf16 head-size-64 forward; with piece_carry != nullptr, the G * P pieces of the
 // chunk-parallel forward (la_chunked_fwd_split).
 la_status fwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
@@ -235,24 +220,21 @@ la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const fl
                       z0, S_out, z_out, C, eps);
 }
 
-la_status bwd_tc_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, const void* dO,
-                        const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv, float* dS0, float* dz0,
-                        int G, int C, float eps, cudaStream_t stream)
+// The bf16 head-size-64 backward of a chunk that fits one 128-token tile (0 <= C <= 128).
+la_status bwd_tile_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                          const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv,
+                          float* dS0, float* dz0, int G, int C, float eps, cudaStream_t stream)
 {
     static OptIn flag;
-    auto kern = la::la_bwd_tc_kernel;
-    const la_status st = prepare(kern, flag, la::BwdTcLayout::BYTES);
+    auto kern = la::la_bwd_tile_kernel;
+    const la_status st = prepare(kern, flag, la::BwdTileLayout::BYTES);
     if (st != LA_OK) return st;
-    CUtensorMap tq{}, tk{}, tv{}, tg{}, tdq{}, tdk{}, tdv{}, tds{};
-    if (C > 0) {
-        constexpr int R = la::BwdTcLayout::BOX_ROWS;
-        if (!tmap_bf16(&tq, q, G, C, 64, R) || !tmap_bf16(&tk, k, G, C, 64, R) || !tmap_bf16(&tv, v, G, C, 64, R) ||
-            !tmap_bf16(&tg, dO, G, C, 64, R) || !tmap_bf16(&tdq, dq, G, C, 64, R) || !tmap_bf16(&tdk, dk, G, C, 64, R) ||
-            !tmap_bf16(&tdv, dv, G, C, 64, R) || (dS0 && !tmap_state_f32(&tds, dS0, G, 64)))
-            return LA_ERR_CUDA;
-    }
-    return launch_pdl(kern, G, la::BwdTcLayout::THREADS, la::BwdTcLayout::BYTES, stream, tq, tk, tv, tg, tdq, tdk, tdv,
-                      tds, S0, z0, dS_out, dz_out, dS0, dz0, C, eps);
+    CUtensorMap tq{}, tk{}, tv{}, tg{};
+    if (C > 0 && (!tmap_bf16(&tq, q, G, C, 64, 128) || !tmap_bf16(&tk, k, G, C, 64, 128) ||
+                  !tmap_bf16(&tv, v, G, C, 64, 128) || !tmap_bf16(&tg, dO, G, C, 64, 128)))
+        return LA_ERR_CUDA;
+    return launch_pdl(kern, G, la::BwdTileLayout::THREADS, la::BwdTileLayout::BYTES, stream, tq, tk, tv, tg, S0, z0,
+                      dS_out, dz_out, dq, dk, dv, dS0, dz0, C, eps);
 }
 
 // Multi-tile tensor-core backward (bf16, head size 64 or 128, any C).  mode 0: both passes
@@ -292,7 +274,13 @@ la_status bwd_tcm_launch(const void* q, const void* k, const void* v, const floa
     X(LA_F32, F32Simt, 64, 128, 8, 1)
 
 #define LA_BWD_TABLE(X)                         \
-    X(LA_F32, F32Simt, 64, 64, 8, 1, false)
+    X(LA_F32, F32Simt, 64, 64, 8, 1, false)     \
+    X(LA_F32, F32Simt, 128, 64, 8, 1, true)     \
+    X(LA_F32, F32Simt, 64, 128, 8, 1, true)
+
+// fp32 (D, block) pairs whose tiles do not fit on chip run the block-64 tiling: the result is
+// the same function of the inputs for every block size (block changes only the rounding).
+int f32_block(int D, int block) { return (D == 128 && block == 128) ? 64 : block; }
 
 // ---------------------------------------------------------------- argument checks
 struct Buf {
@@ -413,6 +401,7 @@ extern "C" la_status la_chunked_fwd(const void* q, const void* k, const void* v,
     }
     if (dtype == LA_BF16 && D == 128) return fwd_tc128_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
 
+    if (dtype == LA_F32) block = f32_block(D, block);
 #define LA_FWD_CASE(DT, P, DD, BB, NW, ST)                                                                  \
     if (dtype == DT && D == DD && block == BB)                                                             \
         return fwd_launch<P, DD, BB, NW, ST>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, s);
@@ -618,14 +607,15 @@ extern "C" la_status la_chunked_bwd(const void* q, const void* k, const void* v,
     if (G == 0) return LA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // bf16, head size 64, one 128-token tile: the tensor-core (tcgen05 / TMEM / TMA) kernel
-    if (dtype == LA_BF16 && D == 64 && C <= la::BwdTcLayout::MAX_C)
-        return bwd_tc_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
+    if (dtype == LA_BF16 && D == 64 && C <= la::BwdTileLayout::MAX_C)
+        return bwd_tile_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
     // bf16, longer chunks or head size 128: the multi-tile tensor-core kernel
     if (dtype == LA_BF16 && (D == 64 || D == 128)) {
         if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
         return D == 64 ? bwd_tcm_launch<64>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s)
                        : bwd_tcm_launch<128>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, s);
     }
+    if (dtype == LA_F32) block = f32_block(D, block);
     if (C > la_bwd_max_c(D, block, dtype)) return LA_ERR_UNSUPPORTED;
 
 #define LA_BWD_CASE(DT, P, DD, BB, NW, ST, AL)                                                               \
@@ -1107,15 +1097,24 @@ size_t ws_layout(size_t n_x, size_t n_S, size_t n_z, size_t off[16])
 
 // The device mapping of page-locked host memory at p, or nullptr when p is not page-locked
 // or not 16-byte aligned (that memory goes through cudaMemcpyAsync instead).
-void* host_mapping(const void* p)
+// The device mapping of a page-locked host buffer [p, p + bytes), or nullptr when the SM
+// copy may not use it: the address and length must be multiples of 16 bytes, and the first
+// and the last byte must both be page-locked with device mappings bytes - 1 apart (a buffer
+// registered only in part would otherwise send the copy kernel into unmapped memory).
+void* host_mapping(const void* p, size_t bytes)
 {
-    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return nullptr;
-    cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    if (!p || bytes == 0 || reinterpret_cast<uintptr_t>(p) % 16 != 0 || bytes % 16 != 0) return nullptr;
+    cudaPointerAttributes a{}, b{};
+    const char* last = static_cast<const char*>(p) + bytes - 1;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess || cudaPointerGetAttributes(&b, last) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+    if (a.type != cudaMemoryTypeHost || b.type != cudaMemoryTypeHost || !a.devicePointer || !b.devicePointer)
+        return nullptr;
+    if (static_cast<const char*>(b.devicePointer) != static_cast<const char*>(a.devicePointer) + bytes - 1)
+        return nullptr;
+    return a.devicePointer;
 }
 
 // The step's copies of tensors i0 .. i0 + 7 (those present: dev[i] != nullptr) in one
@@ -1128,7 +1127,7 @@ la_status step_copies(const void* const host[16], void* const dev[16], const siz
     bool mapped = true;
     for (int i = i0; i < i0 + 8 && mapped; ++i) {
         if (!dev[i]) continue;
-        void* m = bytes[i] % 16 == 0 ? host_mapping(host[i]) : nullptr;
+        void* m = host_mapping(host[i], bytes[i]);
         if (!m) {
             mapped = false;
             break;
@@ -1159,6 +1158,11 @@ la_status step_copies(const void* const host[16], void* const dev[16], const siz
 }
 
 }  // namespace
+
+extern "C" int la_host_copy_eligible(const void* p, size_t bytes)
+{
+    return host_mapping(p, bytes) != nullptr ? 1 : 0;
+}
 
 extern "C" size_t la_step_workspace_bytes(int G, int C, int D, la_dtype dtype)
 {
@@ -1214,6 +1218,7 @@ extern "C" int la_bwd_max_c(int D, int block, la_dtype dtype)
 {
     // bf16: the tensor-core kernels keep nothing per token on chip
     if (dtype == LA_BF16 && (block == 64 || block == 128) && (D == 64 || D == 128)) return 1 << 30;
+    if (dtype == LA_F32) block = f32_block(D, block);
     const int lim = smem_optin_limit(nullptr);
     if (lim < 0) {
         cudaGetLastError();  // leave no sticky "no device" error behind

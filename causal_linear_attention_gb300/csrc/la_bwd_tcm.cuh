@@ -1,6 +1,6 @@
 // la_bwd_tcm.cuh -- backward of chunked causal linear attention on the tensor cores
 // (tcgen05 + TMEM + TMA) for chunks of any length, bf16 inputs, fp32 state, head size
-// 64 or 128.  (Chunks of at most 128 tokens at head size 64 use la_bwd_tc.cuh.)
+// 64 or 128.  (Chunks of at most 128 tokens at head size 64 use la_bwd_tile.cuh.)
 //
 // "Fractus-1B training optimization -- 2026-08-22", section 1, "Bottleneck #1": the
 // derivative of a cumsum is a reverse cumsum.  The chunk is cut into 128-token tiles b;

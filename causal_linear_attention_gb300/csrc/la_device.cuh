@@ -4,7 +4,8 @@
 //   * F32Simt : float32 tiles in shared memory, warp tiles of 16 x 32 fp32
 //               accumulators computed with FMA on the CUDA cores (lane l owns column
 //               l of the tile).
-// (bfloat16 inputs run on the tensor-core kernels: la_fwd_tc*.cuh, la_bwd_tc*.cuh.)
+// (bfloat16 inputs run on the tensor-core kernels: la_fwd_tc*.cuh, la_fwd_tile.cuh, la_bwd_tile.cuh,
+// la_bwd_tcm.cuh.)
 // An operand is described by a base pointer in shared memory, a row stride
 // (elements) and a layout flag:
 //   A(m, k): row-major  A[m * lda + k]     or transposed  A[k * lda + m]

@@ -158,6 +158,8 @@ la_status la_chunked_fwd_split(const void* q, const void* k, const void* v,
  *   - The first call on each device looks the array up and sets the kernels' shared-memory
  *     limits (CUDA runtime calls that do not belong in a stream capture): make one call
  *     outside any capture before capturing calls into a CUDA graph.
+ *   - The array's device address is looked up once per device and kept for the life of
+ *     the process: do not reset a device (cudaDeviceReset) between calls on it.
  */
 la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* v,
                                       const float* S0, const float* z0,
@@ -315,6 +317,16 @@ la_status la_chunked_step_host(const void* q, const void* k, const void* v,
                                void* workspace, size_t workspace_bytes,
                                int G, int C, int D, int block, la_dtype dtype, float eps,
                                void* stream);
+
+/* Whether la_chunked_step_host would move a host buffer of `bytes` bytes at `p` with its
+ * SM-copy kernel (through the buffer's device mapping) rather than cudaMemcpyAsync: 1 when
+ * the address and the length are multiples of 16 bytes and BOTH the first and the last
+ * byte are page-locked host memory whose device mappings are `bytes - 1` apart (a buffer
+ * page-locked only in part, e.g. by cudaHostRegister on a sub-range, gives 0: the kernel
+ * would read unmapped memory there, cudaMemcpyAsync does not); 0 otherwise, including
+ * NULL, bytes == 0 and any CUDA error (cleared).  Makes only cudaPointerGetAttributes
+ * calls.  No counterpart on the page: a diagnostic of the host-buffer step. */
+int la_host_copy_eligible(const void* p, size_t bytes);
 
 /* Self-test of the bounded on-device waits (the failure-detection path): synchronises
  * the current device, launches one kernel whose single wait is on an mbarrier nothing

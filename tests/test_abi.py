@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
                                            "la_cumsum_fwd", "la_cumsum_bwd_workspace_bytes", "la_cumsum_bwd",
                                            "la_ce_workspace_bytes", "la_ce_fwd", "la_ce_bwd",
                                            "la_step_workspace_bytes",
-                                           "la_chunked_step_host", "la_bwd_max_c", "la_device_status",
+                                           "la_chunked_step_host", "la_host_copy_eligible", "la_bwd_max_c",
+                                           "la_device_status",
                                            "la_selftest_bounded_wait", "la_status_string", "la_version"])
 
 

@@ -109,6 +109,30 @@ def test_host_step_mixed_memory_kinds():
         assert torch.equal(a, b), n
 
 
+def test_copy_kernel_needs_the_whole_buffer_page_locked():
+    """The SM copy reads host memory through its device mapping, so it is chosen only when the
+    first AND the last byte of a buffer are page-locked with one contiguous mapping: a buffer
+    registered only in part (cudaHostRegister on a sub-range) goes to cudaMemcpyAsync.  Only
+    the decision is checked here; no copy runs over the partly registered buffer."""
+    pinned = torch.empty(1 << 16, dtype=torch.uint8, pin_memory=True)
+    assert la.la_host_copy_eligible(pinned.data_ptr(), pinned.numel()) == 1
+    assert la.la_host_copy_eligible(pinned.data_ptr() + 16, pinned.numel() - 32) == 1
+    assert la.la_host_copy_eligible(pinned.data_ptr() + 8, 64) == 0      # address not 16-byte aligned
+    assert la.la_host_copy_eligible(pinned.data_ptr(), 24) == 0          # length not a multiple of 16
+    pageable = torch.empty(1 << 20, dtype=torch.uint8)
+    assert la.la_host_copy_eligible(pageable.data_ptr(), 1 << 16) == 0
+    # register the first 256 KiB of a pageable (page-aligned) region only
+    base = (pageable.data_ptr() + 4095) & ~4095
+    rt = torch.cuda.cudart()
+    assert int(rt.cudaHostRegister(base, 1 << 18, 0)) == 0
+    try:
+        assert la.la_host_copy_eligible(base, 1 << 18) == 1              # inside the registration
+        assert la.la_host_copy_eligible(base, (1 << 18) + 4096) == 0     # runs past its end
+    finally:
+        assert int(rt.cudaHostUnregister(base)) == 0
+    assert la.la_host_copy_eligible(base, 1 << 18) == 0
+
+
 def test_host_step_in_place_carry():
     """S_out may be the S0 buffer and dS0 the dS_out buffer: the inputs are copied in first."""
     x = make_inputs(5, 128, 64, dtype="bf16", seed=4, grads=True)

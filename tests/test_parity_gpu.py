@@ -124,15 +124,32 @@ def test_bf16_shapes_and_tails(D, block, C):
     bwd_case(5, C, D, block, "bf16", seed=C)
 
 
-@pytest.mark.parametrize("D,block", [(64, 64), (128, 64), (64, 128)])
+FP32_SHAPES = [(64, 64), (128, 64), (64, 128), (128, 128)]
+
+
+@pytest.mark.parametrize("D,block", FP32_SHAPES)
 @pytest.mark.parametrize("C", [1, 33, 128, 200])
 def test_fp32_forward_shapes(D, block, C):
     fwd_case(3, C, D, block, "f32", seed=C + 1)
 
 
+@pytest.mark.parametrize("D,block", FP32_SHAPES)
 @pytest.mark.parametrize("C", [1, 33, 128, 200])
-def test_fp32_backward_shapes(C):
-    bwd_case(3, C, 64, 64, "f32", seed=C + 2)
+def test_fp32_backward_shapes(D, block, C):
+    bwd_case(3, C, D, block, "f32", seed=C + 2)
+
+
+@pytest.mark.parametrize("D,block", FP32_SHAPES)
+def test_fp32_backward_longest_chunk(D, block):
+    """The fp32 backward keeps 1/den and dd of every token on chip: the largest chunk it
+    accepts (la_bwd_max_c) runs and matches the oracle, one token more is refused."""
+    cmax = la.la_bwd_max_c(D, block, la.LA_F32)
+    assert cmax >= 1000
+    bwd_case(1, cmax, D, block, "f32", seed=D + block)
+    x = make_inputs(1, cmax + 1, D, dtype="f32", seed=1, grads=True).to(DEV)
+    with pytest.raises(la.LAError) as e:
+        la.chunked_bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, block=block, eps=EPS)
+    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -179,6 +196,30 @@ def test_in_place_carry_and_carry_grad():
     check((o, S, z), ref, "bf16", FWD_NAMES)
     gref = oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS)
     check(g, gref, "bf16", BWD_NAMES)
+
+
+def test_long_stream_single_launch():
+    """The fused multi-chunk stream: G=160, D=64, T=8192 tokens in ONE forward launch (the
+    carry stays on chip from tile to tile), against one oracle pass over all 8192 tokens."""
+    fwd_case(160, 8192, 64, 64, "bf16", seed=3)
+
+
+@pytest.mark.parametrize("G,C", [(8, 1024), (4, 1333)])
+def test_wide_heads_long_chunk_forward(G, C):
+    """Head size 128, many 128-token tiles in one launch (C = 1333 ends on a ragged tile)."""
+    fwd_case(G, C, 128, 64, "bf16", seed=G + C)
+
+
+@pytest.mark.parametrize("D,C", [(64, 128), (64, 300), (128, 200)])
+def test_bf16_block_size_is_the_same_tiling(D, C):
+    """The bf16 tensor-core kernels tile by 128 tokens whatever `block` is (the result is the
+    same function of the inputs for every block size; only the rounding could differ, and
+    here it does not): block 64 and block 128 give bit-identical outputs and gradients."""
+    x = make_inputs(8, C, D, dtype="bf16", seed=D + C, grads=True)
+    for u, w in zip(run_fwd(x, 64), run_fwd(x, 128)):
+        assert torch.equal(u, w)
+    for u, w in zip(run_bwd(x, 64), run_bwd(x, 128)):
+        assert torch.equal(u, w)
 
 
 def test_block_size_changes_only_rounding():

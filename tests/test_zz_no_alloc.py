@@ -16,17 +16,23 @@ EPS = 1e-6
 
 
 def test_static_scratch_forward_equals_the_workspace_form_on_consecutive_calls():
+    """Two calls in a row with different plans, issued back to back on one stream before a
+    single synchronisation: the second reuses the module array the first has just used, and
+    each must still equal its workspace-form result bit for bit."""
     la.build()
-    for G, C, seed in ((2, 4096, 31), (8, 1000, 32)):  # two calls in a row, different plans
+    cases = ((2, 4096, 31), (8, 1000, 32))
+    refs, outs = [], []
+    for G, C, seed in cases:
         assert la.la_fwd_split_workspace_bytes(G, C, 64, la.LA_BF16) > 0
         x = make_inputs(G, C, 64, dtype="bf16", seed=seed, carry=True).to(DEV)
-        ref = la.chunked_fwd_split(x.q, x.k, x.v, x.S0, x.z0, block=64, eps=EPS)
-        o = torch.empty_like(x.q)
-        S = torch.empty(G, 64, 64, device=DEV)
-        z = torch.empty(G, 64, device=DEV)
-        la.la_chunked_fwd_split_static(x.q, x.k, x.v, x.S0, x.z0, o, S, z, G, C, 64, 64, la.LA_BF16, EPS,
-                                       torch.cuda.current_stream().cuda_stream)
-        torch.cuda.synchronize()
+        refs.append(la.chunked_fwd_split(x.q, x.k, x.v, x.S0, x.z0, block=64, eps=EPS))
+        outs.append((x, torch.empty_like(x.q), torch.empty(G, 64, 64, device=DEV), torch.empty(G, 64, device=DEV)))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream().cuda_stream
+    for (G, C, _), (x, o, S, z) in zip(cases, outs):
+        la.la_chunked_fwd_split_static(x.q, x.k, x.v, x.S0, x.z0, o, S, z, G, C, 64, 64, la.LA_BF16, EPS, stream)
+    torch.cuda.synchronize()
+    for ref, (x, o, S, z) in zip(refs, outs):
         for name, a, b in zip(("o", "S_out", "z_out"), (o, S, z), ref):
             assert torch.equal(a, b), name
     assert la.la_device_status() == 0
