@@ -113,7 +113,7 @@ def measure_chunked_ce(stream):
     peak, src = measured_bf16_peak()
     out = {"N": N, "V": V, "d": d, "dtype": "bf16",
            "api": "la_ce_fwd / la_ce_bwd (logits on this library's tcgen05 kernel with the log-sum-exp or the "
-                  "gradient in its epilogue; dh, dW on cuBLAS)"}
+                  "gradient in its epilogue; dh, dW on its persistent tcgen05 GEMM)"}
     for chunk in (512, 128):
         ws = la.ce_workspace(N, V, d, chunk, dev)
         loss = torch.empty((), dtype=torch.float32, device=dev)

@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(["nvcc", ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
-                    *objs, "-lcublas", "-o", tmp], check=True)
+                    *objs, "-o", tmp], check=True)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

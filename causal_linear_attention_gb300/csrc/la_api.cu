@@ -4,7 +4,6 @@
 // two CTAs ever touch the same output element and results are bitwise reproducible.
 #include "la.h"
 
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -26,6 +25,7 @@
 #include "la_fwd_split.cuh"
 #include "la_cumsum.cuh"
 #include "la_ce.cuh"
+#include "la_gemm.cuh"
 #include "la_hostcopy.cuh"
 
 namespace {
@@ -767,7 +767,7 @@ extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, 
 namespace {
 
 constexpr size_t kCeAlign = 256;
-constexpr size_t kCublasWsBytes = (size_t)32 << 20;  // cuBLAS's workspace, carved from the caller's
+constexpr int kGemmMaxSplit = 8;  // vocabulary ranges of the dh GEMM (its fp32 slices live in the workspace)
 
 size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 
@@ -780,8 +780,6 @@ int ce_tstride(int cc) { return (cc + 31) / 32 * 32; }
 constexpr int kCeTileWidths[3] = {256, 224, 192};
 constexpr int kCeTokTile = 128;  // tokens per tile of the fused GEMM
 int ce_slices(int V) { return (V + kCeTileWidths[2] - 1) / kCeTileWidths[2]; }
-// d a multiple of 64: the logits on this library's tensor-core kernel, never in memory
-bool ce_fused(int d) { return d % 64 == 0; }
 
 // The fused GEMM's tile width for mtiles token tiles: the one whose whole waves over the
 // SMs (one persistent CTA each) cover the fewest vocabulary columns.  Ties go to the wider
@@ -863,41 +861,33 @@ la_status ce_persist_launch(const CUtensorMap& th, const CUtensorMap& tw, const 
     }
 }
 
-// Workspace slots: the chunk's fp32 logits LT [V][cs] (only without the fused GEMM), its
-// bf16 gradient GT [V][cs], the per-token loss terms [N], the log-sum-exp partials pm, ps
-// [slices][cs] and the target logits [cs], cuBLAS's workspace.
-size_t ce_layout(int N, int V, int d, int cc, size_t off[7])
+// Workspace slots: the chunk's bf16 gradient GT [V][cs] (vocabulary-major), the per-token
+// loss terms [N], the log-sum-exp partials pm, ps [slices][cs] and the target logits [cs],
+// and the dh GEMM's fp32 slices [kGemmMaxSplit][cs][d].
+size_t ce_layout(int N, int V, int d, int cc, size_t off[6])
 {
     const size_t cs = (size_t)ce_tstride(cc), ns = (size_t)ce_slices(V);
-    const size_t sizes[7] = {ce_fused(d) ? 0 : (size_t)V * cs * 4, (size_t)V * cs * 2, (size_t)N * 4, ns * cs * 4,
-                             ns * cs * 4, cs * 4, kCublasWsBytes};
+    const size_t sizes[6] = {(size_t)V * cs * 2, (size_t)N * 4, ns * cs * 4, ns * cs * 4, cs * 4,
+                             (size_t)kGemmMaxSplit * cs * d * 4};
     size_t o = 0;
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 6; ++i) {
         off[i] = o;
         o += ce_round(sizes[i]);
     }
     return o;
 }
 
-// One cuBLAS handle per device, made on first use (cuBLAS keeps a little device state of
-// its own for it); calls that use it hold its lock while they enqueue, so the stream and
-// workspace it is given are theirs.
-struct CublasSlot {
-    std::mutex mu;
-    cublasHandle_t h = nullptr;
-};
-CublasSlot g_cublas[kMaxDevices];
-
 la_status ce_check(const void* h, const void* W, const int* targets, int N, int V, int d, int ce_chunk,
                    const void* workspace, size_t workspace_bytes, size_t* need)
 {
     if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0) return LA_ERR_INVALID;
+    if (d % 64 != 0) return LA_ERR_UNSUPPORTED;  // the tensor-core GEMMs take d in 64-wide slices
     if (N == 0) return LA_OK;
     if (!h || !W || !targets) return LA_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(h) % 16 || reinterpret_cast<uintptr_t>(W) % 16 ||
         reinterpret_cast<uintptr_t>(targets) % 4)
         return LA_ERR_INVALID;
-    size_t off[7];
+    size_t off[6];
     *need = ce_layout(N, V, d, std::min(ce_chunk, N), off);
     if (!workspace || reinterpret_cast<uintptr_t>(workspace) % kCeAlign || workspace_bytes < *need)
         return LA_ERR_INVALID;
@@ -908,45 +898,59 @@ la_status ce_check(const void* h, const void* W, const int* targets, int N, int 
     return LA_OK;
 }
 
-// A locked cuBLAS handle on `stream` with the caller's workspace slot
-struct CublasUse {
-    std::unique_lock<std::mutex> lock;
-    cublasHandle_t h = nullptr;
-    bool ok = false;
-    CublasUse(cudaStream_t stream, void* ws)
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) {
-            cudaGetLastError();
-            return;
-        }
-        lock = std::unique_lock<std::mutex>(g_cublas[dev].mu);
-        if (!g_cublas[dev].h && cublasCreate(&g_cublas[dev].h) != CUBLAS_STATUS_SUCCESS) {
-            g_cublas[dev].h = nullptr;
-            return;
-        }
-        h = g_cublas[dev].h;
-        ok = cublasSetStream(h, stream) == CUBLAS_STATUS_SUCCESS &&
-             cublasSetWorkspace(h, ws, kCublasWsBytes) == CUBLAS_STATUS_SUCCESS &&
-             cublasSetMathMode(h, CUBLAS_DEFAULT_MATH) == CUBLAS_STATUS_SUCCESS;
-    }
-};
-
-// LT[V][cs] (fp32, vocabulary-major: LT[j][i] = logits[i][j]) = W h_c^T for the chunk's nc
-// tokens (column-major: op_T(h_c) . W -> nc x V, ld cs)
-bool ce_logits(cublasHandle_t hb, const void* hc, const void* W, float* LT, int nc, int cs, int V, int d)
+// bf16 [rows][cols] (cols contiguous) as a 3-D map with boxes of 64 columns x box_rows
+// rows, 128-byte swizzle; rows and columns past the extent read as zero.
+bool tmap_bf16_2d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows)
 {
-    const float one = 1.f, zero = 0.f;
-    return cublasGemmEx(hb, CUBLAS_OP_T, CUBLAS_OP_N, nc, V, d, &one, hc, CUDA_R_16BF, d, W, CUDA_R_16BF, d, &zero,
-                        LT, CUDA_R_32F, cs, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1u};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 [slices][rows][cols] as the GEMM's output map: boxes of 32 columns (128 bytes) x 32
+// rows, 128-byte swizzle; stores past the extent are clipped.
+bool tmap_f32_out(CUtensorMap* map, float* base, int slices, int rows, int cols)
+{
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)slices};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)rows * cols * 4};
+    cuuint32_t box[3] = {32u, 32u, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One GEMM of the cross-entropy's backward (la_gemm.cuh): persistent, one CTA per SM (at
+// most one per work unit).
+template <bool A_MN>
+la_status gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tout, int a_k0, int b_k0,
+                      int M, int N, int KB, int nsplit, int kbs, int reduce, int sms, cudaStream_t s)
+{
+    using L = la::GemmLayout;
+    static OptIn flag;
+    auto kern = la::la_gemm_kernel<A_MN>;
+    const la_status st = prepare(kern, flag, L::BYTES);
+    if (st != LA_OK) return st;
+    const int mtiles = (M + L::BM - 1) / L::BM, ntiles = (N + L::BN - 1) / L::BN;
+    const int units = mtiles * ntiles * nsplit;
+    return launch_pdl(kern, std::min(units, sms), L::THREADS, L::BYTES, s, ta, tb, tout, a_k0, b_k0, mtiles, ntiles,
+                      KB, nsplit, kbs, M, N, reduce);
 }
 
 }  // namespace
 
 extern "C" size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk)
 {
-    if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0) return 0;
-    size_t off[7];
+    if (N < 0 || V <= 0 || d <= 0 || ce_chunk <= 0 || d % 64 != 0) return 0;
+    size_t off[6];
     return ce_layout(N, V, d, std::min(ce_chunk, std::max(N, 1)), off);
 }
 
@@ -965,52 +969,32 @@ extern "C" la_status la_ce_fwd(const void* h, const void* W, const int* targets,
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (N == 0) return cudaMemsetAsync(loss, 0, sizeof(float), s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
-    const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc), ns = ce_slices(V);
-    size_t off[7];
+    const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc);
+    size_t off[6];
     ce_layout(N, V, d, cc, off);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    float* LT = reinterpret_cast<float*>(ws + off[0]);
-    float* row_loss = reinterpret_cast<float*>(ws + off[2]);
-    float* pm = reinterpret_cast<float*>(ws + off[3]);
-    float* ps = reinterpret_cast<float*>(ws + off[4]);
-    float* tl = reinterpret_cast<float*>(ws + off[5]);
-    if (ce_fused(d)) {  // logits on the tensor core, the log-sum-exp from TMEM
-        const int sms = sm_count();
-        if (sms <= 0) return LA_ERR_CUDA;
-        CUtensorMap th{}, tw{};
-        int bn_map = 0;  // the tile width tw was made for
-        for (int c0 = 0; c0 < N; c0 += cc) {
-            const int nc = std::min(cc, N - c0);
-            const int bn = ce_tile_width(ce_mtiles<0>(nc, cs), V, sms), nt = (V + bn - 1) / bn;
-            if (bn != bn_map) {
-                if (!ce_maps(h, W, N, V, d, bn, &th, &tw)) return LA_ERR_CUDA;
-                bn_map = bn;
-            }
-            st = ce_persist_launch<0>(th, tw, tw, bn, c0, nc, cs, V, d, sms, targets + c0, pm, ps, tl, nullptr, 0.f,
-                                      s);
-            if (st != LA_OK) return st;
-            st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
-                            static_cast<const float*>(ps), static_cast<const float*>(tl), nt, nc, cs, V, targets + c0,
-                            lse + c0, row_loss + c0);
-            if (st != LA_OK) return st;
+    float* row_loss = reinterpret_cast<float*>(ws + off[1]);
+    float* pm = reinterpret_cast<float*>(ws + off[2]);
+    float* ps = reinterpret_cast<float*>(ws + off[3]);
+    float* tl = reinterpret_cast<float*>(ws + off[4]);
+    // the logits on the tensor core, the log-sum-exp from TMEM: they never reach memory
+    const int sms = sm_count();
+    if (sms <= 0) return LA_ERR_CUDA;
+    CUtensorMap th{}, tw{};
+    int bn_map = 0;  // the tile width tw was made for
+    for (int c0 = 0; c0 < N; c0 += cc) {
+        const int nc = std::min(cc, N - c0);
+        const int bn = ce_tile_width(ce_mtiles<0>(nc, cs), V, sms), nt = (V + bn - 1) / bn;
+        if (bn != bn_map) {
+            if (!ce_maps(h, W, N, V, d, bn, &th, &tw)) return LA_ERR_CUDA;
+            bn_map = bn;
         }
-    } else {
-        const int nsr = (V + la::CE_SLICE - 1) / la::CE_SLICE;
-        CublasUse cb(s, ws + off[6]);
-        if (!cb.ok) return LA_ERR_CUDA;
-        for (int c0 = 0; c0 < N; c0 += cc) {
-            const int nc = std::min(cc, N - c0);
-            if (!ce_logits(cb.h, static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d, W, LT, nc, cs, V, d))
-                return LA_ERR_CUDA;
-            st = launch_pdl(la::la_ce_lse_part_kernel, dim3((nc + la::CE_TOK - 1) / la::CE_TOK, nsr),
-                            la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0, pm,
-                            ps, tl);
-            if (st != LA_OK) return st;
-            st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
-                            static_cast<const float*>(ps), static_cast<const float*>(tl), nsr, nc, cs, V, targets + c0,
-                            lse + c0, row_loss + c0);
-            if (st != LA_OK) return st;
-        }
+        st = ce_persist_launch<0>(th, tw, tw, bn, c0, nc, cs, V, d, sms, targets + c0, pm, ps, tl, nullptr, 0.f, s);
+        if (st != LA_OK) return st;
+        st = launch_pdl(la::la_ce_lse_merge_kernel, (nc + 7) / 8, 256, 0, s, static_cast<const float*>(pm),
+                        static_cast<const float*>(ps), static_cast<const float*>(tl), nt, nc, cs, V, targets + c0,
+                        lse + c0, row_loss + c0);
+        if (st != LA_OK) return st;
     }
     return launch_pdl(la::la_ce_mean_kernel, 1, 1024, 0, s, static_cast<const float*>(row_loss), N, loss);
 }
@@ -1031,46 +1015,45 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (N == 0) return cudaMemsetAsync(dW, 0, (size_t)V * d * 4, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
     const int cc = std::min(ce_chunk, N), cs = ce_tstride(cc);
-    size_t off[7];
+    size_t off[6];
     ce_layout(N, V, d, cc, off);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    float* LT = reinterpret_cast<float*>(ws + off[0]);
-    __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[1]);
-    const bool fused = ce_fused(d);
-    // the backward's tiles cover all cs token columns of every chunk: one tile width
+    __nv_bfloat16* GT = reinterpret_cast<__nv_bfloat16*>(ws + off[0]);
+    float* dhp = reinterpret_cast<float*>(ws + off[5]);
     const int sms = sm_count();
     if (sms <= 0) return LA_ERR_CUDA;
+    // the backward's tiles cover all cs token columns of every chunk: one tile width
     const int bn = ce_tile_width(ce_mtiles<1>(cc, cs), V, sms, true);
-    CUtensorMap th{}, tw{}, tgt{};
-    if (fused && (!ce_maps(h, W, N, V, d, bn, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt))) return LA_ERR_CUDA;
-    CublasUse cb(s, ws + off[6]);
-    if (!cb.ok) return LA_ERR_CUDA;
-    const float one = 1.f, zero = 0.f, scale = dloss / (float)N;
+    // dh = G W: M = the chunk's tokens (A = GT read token-major), N = d, K = the vocabulary,
+    // cut into nsplit ranges (one fp32 slice each, summed in a fixed order);
+    // dW += G^T h: M = the vocabulary (A = GT rows), N = d, K = the chunk's tokens
+    const int kbv = (V + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
+    const int ntot_dh = ((cs + la::GemmLayout::BM - 1) / la::GemmLayout::BM) * ((d + la::GemmLayout::BN - 1) / la::GemmLayout::BN);
+    int nsplit = std::max(1, std::min(kGemmMaxSplit, std::min(kbv, sms / std::max(1, ntot_dh))));
+    const int kbs = (kbv + nsplit - 1) / nsplit;
+    nsplit = (kbv + kbs - 1) / kbs;
+    CUtensorMap th{}, tw{}, tgt{}, ta_mn{}, ta_k{}, tb_w{}, tb_h{}, to_dh{}, to_dw{};
+    if (!ce_maps(h, W, N, V, d, bn, &th, &tw) || !ce_grad_map(GT, V, cs, &tgt) ||
+        !tmap_bf16_2d(&ta_mn, GT, V, cs, 64) || !tmap_bf16_2d(&ta_k, GT, V, cs, la::GemmLayout::BM) ||
+        !tmap_bf16_2d(&tb_w, W, V, d, 64) || !tmap_bf16_2d(&tb_h, h, N, d, 64) ||
+        !tmap_f32_out(&to_dh, dhp, nsplit, cs, d) || !tmap_f32_out(&to_dw, dW, 1, V, d))
+        return LA_ERR_CUDA;
+    const float scale = dloss / (float)N;
     for (int c0 = 0; c0 < N; c0 += cc) {
         const int nc = std::min(cc, N - c0);
-        const __nv_bfloat16* hc = static_cast<const __nv_bfloat16*>(h) + (size_t)c0 * d;
-        if (fused) {  // the logits again on the tensor core, the gradient straight from TMEM
-            st = ce_persist_launch<1>(th, tw, tgt, bn, c0, nc, cs, V, d, sms, targets + c0, nullptr, nullptr,
-                                      nullptr, lse + c0, scale, s);
-            if (st != LA_OK) return st;
-        } else {
-            if (!ce_logits(cb.h, hc, W, LT, nc, cs, V, d)) return LA_ERR_CUDA;  // recomputed
-            constexpr int rows_per_cta = la::CE_ROWS * la::CE_GRAD_ROWS;
-            st = launch_pdl(la::la_ce_grad_kernel, dim3(cs / la::CE_TOK, (V + rows_per_cta - 1) / rows_per_cta),
-                            la::CE_TOK * la::CE_ROWS, 0, s, static_cast<const float*>(LT), V, nc, cs, targets + c0,
-                            lse + c0, scale, GT);
-            if (st != LA_OK) return st;
-        }
-        // dh_c[nc][d] = G W  (column-major: W (d x V) . op_T(GT) (V x nc))
-        if (cublasGemmEx(cb.h, CUBLAS_OP_N, CUBLAS_OP_T, d, nc, V, &one, W, CUDA_R_16BF, d, GT, CUDA_R_16BF, cs, &zero,
-                         static_cast<__nv_bfloat16*>(dh) + (size_t)c0 * d, CUDA_R_16BF, d, CUBLAS_COMPUTE_32F,
-                         CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-            return LA_ERR_CUDA;
-        // dW[V][d] (+)= G^T h_c  (column-major: h_c (d x nc) . GT (nc x V))
-        if (cublasGemmEx(cb.h, CUBLAS_OP_N, CUBLAS_OP_N, d, V, nc, &one, hc, CUDA_R_16BF, d, GT, CUDA_R_16BF, cs,
-                         c0 == 0 ? &zero : &one, dW, CUDA_R_32F, d, CUBLAS_COMPUTE_32F,
-                         CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-            return LA_ERR_CUDA;
+        // the logits again on the tensor core, the gradient straight from TMEM -> GT
+        st = ce_persist_launch<1>(th, tw, tgt, bn, c0, nc, cs, V, d, sms, targets + c0, nullptr, nullptr, nullptr,
+                                  lse + c0, scale, s);
+        if (st != LA_OK) return st;
+        st = gemm_launch<true>(ta_mn, tb_w, to_dh, 0, 0, cs, d, kbv, nsplit, kbs, 0, sms, s);
+        if (st != LA_OK) return st;
+        const int sum_blocks = (int)std::min<long long>(8LL * sms, ((long long)nc * d / 4 + 255) / 256);
+        st = launch_pdl(la::la_gemm_sum_slices_kernel, sum_blocks, 256, 0, s, static_cast<const float*>(dhp), nsplit,
+                        cs, d, nc, static_cast<__nv_bfloat16*>(dh) + (size_t)c0 * d);
+        if (st != LA_OK) return st;
+        st = gemm_launch<false>(ta_k, tb_h, to_dw, 0, c0, V, d, (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK, 1,
+                                (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK, c0 > 0 ? 1 : 0, sms, s);
+        if (st != LA_OK) return st;
     }
     return LA_OK;
 }

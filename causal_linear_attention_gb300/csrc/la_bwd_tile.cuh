@@ -71,13 +71,6 @@ struct BwdTileLayout {
 };
 static_assert(BwdTileLayout::BYTES <= 115712, "two single-tile backward CTAs must fit one SM");
 
-__device__ __forceinline__ bool elect_one_lane()
-{
-    uint32_t pred = 0;
-    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
-    return pred != 0;
-}
-
 // Warp-level store of this warp's 32 rows of a [C][64] bf16 output: row t's eight 16-byte
 // chunks are staged at `stage` (a 128-byte-swizzled tile, rows = tile rows) and written back
 // as 512 contiguous bytes per instruction; rows >= C are not written.

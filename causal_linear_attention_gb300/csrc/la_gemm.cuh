@@ -1,0 +1,241 @@
+// la_gemm.cuh -- the two GEMMs of the chunked cross-entropy's backward on the 5th-generation
+// tensor cores: dh = G W and dW = G^T h.
+//
+// "Fractus-1B training optimization -- 2026-08-22", section 1, "Bottleneck #3" (the tied
+// 50257-token head) and section 2, "Opt 3" (chunked cross-entropy, identical gradients).
+// For a chunk of nc tokens with the gradient of its logits held vocabulary-major,
+// GT[j][i] = G[i][j] (bf16, row stride cs, tokens contiguous):
+//     dh[i][p] = sum_j G[i][j] W[j][p]      (M = tokens, N = d, K = the vocabulary)
+//     dW[j][p] += sum_i G[i][j] h[i][p]     (M = the vocabulary, N = d, K = the chunk's tokens)
+// One persistent kernel computes D[m][n] = sum_k A[m][k] B[n][k] in 128 x 256 fp32 tiles:
+//   - B is read N-major (h and W are row-major with d contiguous): 64-wide atoms of n, one
+//     TMA box each, four per 64-deep slice of K;
+//   - A is read K-major (dW: rows j of GT) or M-major (dh: the tokens of GT are contiguous);
+//   - K is streamed in 64-deep slices through a ring of four stages; one elected lane of
+//     the MMA warp issues the UMMAs (M = 128, N = 256, K = 16) into one of two TMEM
+//     accumulators, so a tile's epilogue runs under the next tile's MMAs;
+//   - work units are (tile, K range): dh's K (the vocabulary) is cut into nsplit ranges,
+//     each unit storing its partial tile into its own fp32 slice (a fixed-order sum over
+//     the slices then gives dh, the same bits every run); dW takes all K at once;
+//   - the epilogue (warps 0-3, one tile row per thread) moves the accumulator out in
+//     32 x 32 fp32 boxes, each warp through two staging buffers of its own, by TMA store or
+//     by TMA reduce-add (dW over chunks after the first: one add per element per launch, in
+//     stream order).  Rows and columns past the output's extent are clipped by the tensor
+//     map; operand rows past K read as zero.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "la_tc.cuh"
+
+namespace la {
+
+struct GemmLayout {
+    static constexpr int BM = 128, BN = 256, BK = 64;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;                // 16 KB
+    static constexpr uint32_t B_BYTES = BN * BK * 2;                // 32 KB
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;      // 48 KB
+    static constexpr int STAGES = 4;
+    static constexpr uint32_t OSTAGE = STAGES * STAGE_BYTES;        // output staging: 2 boxes per epilogue warp
+    static constexpr uint32_t WBOX = 32 * 32 * 4;                   // 32 rows x 32 fp32
+    static constexpr uint32_t BARS = OSTAGE + 4 * 2 * WBOX;
+    static constexpr uint32_t BYTES = BARS + 256;
+    static constexpr uint32_t ACC_COLS = 256;                       // accumulator a at TMEM column 256 a
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 192;
+    static_assert(STAGE_BYTES % 1024 == 0 && BYTES <= 227 * 1024, "shared memory");
+};
+
+// ta: A as K-major boxes [64 k][128 m] (A_MN false) or M-major boxes [64 m][64 k] (A_MN true);
+// tb: B as N-major boxes [64 n][64 k]; tout: the fp32 output [slices][rows][ncols] as boxes
+// [32 n][32 m][1].  a_k0 / b_k0: K coordinates of the first slice in A / B; mtiles x ntiles
+// output tiles; KB 64-deep slices of K cut into nsplit ranges of kbs slices; unit (split s,
+// tile) writes output slice s.  reduce: TMA reduce-add instead of store.  Boxes that start
+// at or past nrows or ncols are not written (no store starts outside the output).
+template <bool A_MN>
+__global__ void __launch_bounds__(192, 1)
+la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+               const __grid_constant__ CUtensorMap tout, int a_k0, int b_k0, int mtiles, int ntiles, int KB, int nsplit,
+               int kbs, int nrows, int ncols, int reduce)
+{
+    using L = GemmLayout;
+    using namespace tc;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t sbase = smem_addr(sm);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* full = bars;                    // [STAGES]
+    uint64_t* empty = bars + L::STAGES;       // [STAGES]
+    uint64_t* tfull = bars + 2 * L::STAGES;   // [2] an accumulator holds a finished unit
+    uint64_t* tempty = tfull + 2;             // [2] the epilogue has read an accumulator
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntot = mtiles * ntiles, nunits = ntot * nsplit;
+
+    if (tid == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 128);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();
+
+    // unit u: split s = u / ntot (units of one split, which share B's K range, run together),
+    // tile T = u % ntot.  dh (A M-major: few M tiles, K cut in ranges) takes the M tile fastest;
+    // dW (A K-major: one stripe of G's rows per M tile, B small and L2-resident) the N tile,
+    // so the N tiles of a stripe run at once and read it from DRAM once between them.
+    auto unit = [&](int u, int& m0, int& n0, int& kb0, int& kb1, int& s) {
+        s = u / ntot;
+        const int T = u % ntot;
+        m0 = (A_MN ? T % mtiles : T / ntiles) * L::BM;
+        n0 = (A_MN ? T / mtiles : T % ntiles) * L::BN;
+        kb0 = s * kbs;
+        kb1 = min(KB, kb0 + kbs);
+    };
+
+    if (warp == 4) {
+        if (lane == 0) {  // TMA producer: every (unit, K slice) of this CTA, in order
+            prefetch_tmap(&ta);
+            prefetch_tmap(&tb);
+            int g = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+                int m0, n0, kb0, kb1, s;
+                unit(u, m0, n0, kb0, kb1, s);
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int st = g % L::STAGES, r = g / L::STAGES;
+                    if (r > 0 && !(ok = mbar_wait(empty + st, (r - 1) & 1, ERR_TIMEOUT_MMA))) break;
+                    unsigned char* p = sm + st * L::STAGE_BYTES;
+                    mbar_expect_tx(full + st, L::STAGE_BYTES);
+                    if (A_MN) {
+                        tma_load_3d(p, &ta, full + st, m0, a_k0 + kb * L::BK, 0);
+                        tma_load_3d(p + 8192, &ta, full + st, m0 + 64, a_k0 + kb * L::BK, 0);
+                    } else {
+                        tma_load_3d(p, &ta, full + st, a_k0 + kb * L::BK, m0, 0);
+                    }
+#pragma unroll
+                    for (int b = 0; b < L::BN / 64; ++b)
+                        tma_load_3d(p + L::A_BYTES + b * 8192, &tb, full + st, n0 + 64 * b, b_k0 + kb * L::BK, 0);
+                }
+            }
+        }
+    } else if (warp == 5) {  // UMMA issuer: the whole warp waits, one elected lane issues
+        const uint32_t id = idesc_bf16(L::BM, L::BN, A_MN, true);
+        int g = 0, lt = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++lt) {
+            int m0, n0, kb0, kb1, s;
+            unit(u, m0, n0, kb0, kb1, s);
+            const int acc = lt & 1, ua = lt >> 1;
+            if (ua > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(tempty + acc, (ua - 1) & 1, ERR_TIMEOUT_MMA)))) break;
+            tc_fence_after();
+            for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                const int st = g % L::STAGES;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(full + st, (g / L::STAGES) & 1, ERR_TIMEOUT_TMA)))) break;
+                tc_fence_after();
+                if (elect_one_lane()) {
+                    const uint32_t a = sbase + st * L::STAGE_BYTES;
+                    // K-major A: +32 B per K = 16 step; M-major A and N-major B: +16 rows (2048 B);
+                    // M-major atoms 8 KB apart (the LBO field), 8-row K groups 1 KB apart
+                    const uint64_t dA = A_MN ? smem_desc(a, 8192, 1024) : smem_desc(a, 16, 1024);
+                    const uint64_t dB = smem_desc(a + L::A_BYTES, 8192, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < L::BK / 16; ++kk)
+                        umma_bf16(tmem + acc * L::ACC_COLS, dA + (A_MN ? kk * 128 : kk * 2), dB + kk * 128, id,
+                                  kb > kb0 || kk > 0);
+                    umma_commit(empty + st);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (elect_one_lane()) umma_commit(tfull + acc);
+            __syncwarp();
+        }
+    } else {
+        // ---- epilogue (warps 0-3): tile row t.  Each warp moves its own 32 rows out in boxes
+        //      of 32 rows x 32 fp32 columns through two 4 KB staging buffers of its own, so the
+        //      warps stream independently (no barrier across them); lane 0 issues the stores.
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        unsigned char* wst = sm + L::OSTAGE + warp * 2 * L::WBOX;
+        int lt = 0, nbox = 0;
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lt) {
+            int m0, n0, kb0, kb1, s;
+            unit(u, m0, n0, kb0, kb1, s);
+            const int acc = lt & 1;
+            const bool late = !mbar_wait(tfull + acc, (lt >> 1) & 1, ERR_TIMEOUT_MMA);
+            if (bar_sync_any(1, 128, late)) break;  // the threads leave together or not at all
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < L::BN / 32; ++c, ++nbox) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + acc * L::ACC_COLS + 32 * c, r);
+                if (c == L::BN / 32 - 1) {  // the accumulator has been read: the next unit may use it
+                    tc_fence_before();
+                    mbar_arrive(tempty + acc);
+                }
+                unsigned char* ob = wst + (nbox & 1) * L::WBOX;
+                if (lane == 0) tma_store_wait_read_le1();  // this warp's box two boxes ago has been read
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 8; ++q)  // row `lane`: 128 B, 16-byte chunks XOR-swizzled by lane % 8
+                    *reinterpret_cast<uint4*>(ob + lane * 128 + (((uint32_t)q ^ (uint32_t)lane) & 7u) * 16) =
+                        make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (n0 + 32 * c < ncols && m0 + 32 * warp < nrows) {
+                        if (reduce)
+                            tma_reduce_add_3d(&tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
+                        else
+                            tma_store_3d(&tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
+                    }
+                    tma_store_commit();  // (an empty group when nothing was written)
+                }
+            }
+        }
+        if (lane == 0) tma_store_wait_all();  // the output has landed before the CTA's memory goes away
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+// dh = the fixed-order sum over the nsplit fp32 slices [nsplit][rows][d] (rows apart), as bf16.
+__global__ void la_gemm_sum_slices_kernel(const float* part, int nsplit, int rows, int d, int nc,
+                                          __nv_bfloat16* out)
+{
+    pdl_wait();
+    const size_t n = (size_t)nc * d / 4;  // d is a multiple of 64
+    const size_t slice = (size_t)rows * d / 4;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float4 a = reinterpret_cast<const float4*>(part)[i];
+        for (int s = 1; s < nsplit; ++s) {
+            const float4 b = reinterpret_cast<const float4*>(part)[s * slice + i];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out) + 2 * i;
+        o[0] = __floats2bfloat162_rn(a.x, a.y);
+        o[1] = __floats2bfloat162_rn(a.z, a.w);
+    }
+}
+
+}  // namespace la

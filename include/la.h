@@ -238,34 +238,32 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
  * [V][d], V = 50257 on the page) and integer targets y_i in [0, V):
  *     logits[i][j] = h_i . W_j,  lse_i = log sum_j exp(logits[i][j]),
  *     loss = (1/N) sum_i (lse_i - logits[i][y_i]),
- * computed ce_chunk tokens at a time so that only one chunk's logits (fp32) exist at once;
- * the backward recomputes them.  The contractions run on cuBLAS (bf16 in, fp32
- * accumulate; a plain library GEMM) -- except the logits when d is a multiple of 64 (see
- * la_ce_workspace_bytes) -- and the row work (log-sum-exp, target logit, the softmax
- * gradient) on this library's kernels.
+ * computed ce_chunk tokens at a time; the backward recomputes each chunk's logits.
+ * Everything runs on this library's tensor-core kernels: the logits of a chunk with the
+ * log-sum-exp (forward) or the softmax gradient G = (softmax - one-hot) dloss / N
+ * (backward) taken straight from the accumulator, so the logits never reach memory; then
+ * dh = G W and dW = G^T h on its persistent GEMM.  d must be a multiple of 64
+ * (LA_ERR_UNSUPPORTED otherwise).
  *
- * la_ce_workspace_bytes: the device workspace both calls need: the chunk's bf16 gradient
- * (and, when d is not a multiple of 64, its fp32 logits), vocabulary-major with the chunk
- * padded to 32 tokens,
- * N floats, the log-sum-exp partials (2 floats per token and vocabulary tile, counted for
- * the narrowest tile, 192 rows), the chunk's target logits and a 32 MiB GEMM workspace, each at a 256-byte boundary; 0 for a negative or zero size.
- * No CUDA call.  With d a multiple of 64 the logits are computed on this library's
- * tensor-core kernel and their log-sum-exp (forward) or gradient (backward) taken straight
- * from its accumulator: the logits never reach memory.  Otherwise cuBLAS writes them into
- * the workspace.
+ * la_ce_workspace_bytes: the device workspace both calls need: the chunk's bf16 gradient,
+ * vocabulary-major with the chunk padded to 32 tokens; N floats; the log-sum-exp partials
+ * (2 floats per token and vocabulary tile, counted for the narrowest tile, 192 rows); the
+ * chunk's target logits; and up to 8 fp32 partial sums of the chunk's dh (the vocabulary
+ * is cut into up to 8 ranges; their fixed-order sum gives the same bits every call), each
+ * at a 256-byte boundary.  0 for a negative or zero size or a d that is not a multiple of
+ * 64.  No CUDA call.
  *
  * la_ce_fwd: loss (one float, device) and lse ([N] float32, device; the backward's input).
  * la_ce_bwd: dloss is the gradient reaching the loss (1 for a plain mean loss); writes dh
- * (bfloat16 [N][d]) and dW (float32 [V][d], overwritten: the gradient of this call alone).
+ * (bfloat16 [N][d]) and dW (float32 [V][d], overwritten: the gradient of this call alone;
+ * chunks after the first add into it in stream order).
  *
  * All pointers are device memory: h, W 16-byte aligned, targets 4-byte aligned, the
  * workspace 256-byte aligned, at least la_ce_workspace_bytes(N, V, d, ce_chunk) bytes and
  * disjoint from every tensor; outputs disjoint from inputs (LA_ERR_INVALID otherwise).
  * N = 0 writes loss = 0 (forward) or dW = 0 (backward).  A target outside [0, V) gives its
  * row a NaN loss and makes la_device_status report LA_ERR_DEVICE.  Asynchronous on
- * `stream`; the library allocates nothing itself, but cuBLAS keeps one handle per device,
- * made on the first call (make that call outside any stream capture), which calls share
- * under a lock while they enqueue.
+ * `stream`; the library allocates nothing and keeps no state between calls.
  */
 size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk);
 

@@ -129,6 +129,16 @@ def test_step_workspace_bytes_closed_form(L, G, C, D, dtype):
     assert la.la_step_workspace_bytes(G, C, D, dtype) == want
 
 
+def test_ce_needs_d_a_multiple_of_64(L):
+    """The cross-entropy runs on the tensor-core kernels, which take d in 64-wide slices: any
+    other d gets no workspace size and is refused before any CUDA call."""
+    assert la.la_ce_workspace_bytes(8, 50, 64, 8) > 0
+    assert la.la_ce_workspace_bytes(8, 50, 96, 8) == 0
+    A = 0x20000000
+    assert L.la_ce_fwd(A, A + 0x100000, A + 0x200000, 8, 50, 96, 8, A + 0x300000, A + 0x300100, A + 0x400000,
+                       1 << 24, None) == UNSUPPORTED
+
+
 def test_step_workspace_bytes_rejects_bad_shapes(L):
     assert la.la_step_workspace_bytes(2, 8, 96, 1) == 0
     assert la.la_step_workspace_bytes(-1, 8, 64, 1) == 0
@@ -250,26 +260,25 @@ def test_cumsum_workspace_bytes_closed_form(L):
 
 
 def test_ce_workspace_bytes_closed_form(L):
-    """One chunk's vocabulary-major fp32 logits (only when d is not a multiple of 64) and
-    bf16 gradient (the chunk padded to 32 tokens), N floats, two [tiles][chunk] partial
-    arrays (a slot per tile of the narrowest vocabulary tile, 192 rows), the chunk's target
-    logits and a 32 MiB GEMM workspace, each rounded up to 256 bytes; the
-    chunk is at most N tokens."""
+    """The chunk's vocabulary-major bf16 gradient (the chunk padded to 32 tokens), N floats,
+    two [tiles][chunk] partial arrays (a slot per tile of the narrowest vocabulary tile, 192
+    rows), the chunk's target logits and 8 fp32 [chunk][d] partial sums of dh, each rounded
+    up to 256 bytes; the chunk is at most N tokens; d must be a multiple of 64."""
     r = lambda n: (n + 255) // 256 * 256
-    for N, V, d, cc in ((512, 50257, 1280, 512), (512, 50257, 1280, 128), (300, 1000, 128, 1000), (1, 7, 8, 4)):
+    for N, V, d, cc in ((512, 50257, 1280, 512), (512, 50257, 1280, 128), (300, 1000, 128, 1000), (1, 7, 64, 4)):
         cs, ns = (min(cc, N) + 31) // 32 * 32, (V + 191) // 192
-        logits = 0 if d % 64 == 0 else r(V * cs * 4)  # the fused GEMM keeps the logits off memory
-        want = logits + r(V * cs * 2) + r(N * 4) + 2 * r(ns * cs * 4) + r(cs * 4) + (32 << 20)
+        want = r(V * cs * 2) + r(N * 4) + 2 * r(ns * cs * 4) + r(cs * 4) + r(8 * cs * d * 4)
         assert la.la_ce_workspace_bytes(N, V, d, cc) == want
-    assert la.la_ce_workspace_bytes(-1, 5, 5, 5) == 0
-    assert la.la_ce_workspace_bytes(5, 0, 5, 5) == 0
-    assert la.la_ce_workspace_bytes(5, 5, 5, 0) == 0
+    assert la.la_ce_workspace_bytes(-1, 5, 64, 5) == 0
+    assert la.la_ce_workspace_bytes(5, 0, 64, 5) == 0
+    assert la.la_ce_workspace_bytes(5, 5, 64, 0) == 0
+    assert la.la_ce_workspace_bytes(5, 5, 8, 5) == 0
 
 
 def ce_call(fwd=True, **kw):
     WS = 0x40000000
     args = dict(h=A, W=A + 0x100000, targets=A + 0x200000, lse=A + 0x300000, loss=A + 0x400000,
-                dh=A + 0x500000, dW=A + 0x600000, N=4, V=16, d=8, ce_chunk=4, workspace=WS, workspace_bytes=1 << 30)
+                dh=A + 0x500000, dW=A + 0x600000, N=4, V=16, d=64, ce_chunk=4, workspace=WS, workspace_bytes=1 << 30)
     args.update(kw)
     L = la.lib()
     if fwd:

@@ -47,7 +47,7 @@ def check(inp, got, chunk, dloss=1.0):
 
 
 @pytest.mark.parametrize("N,V,d,chunk", [(300, 1000, 128, 64), (300, 1000, 128, 300), (257, 4099, 64, 100),
-                                         (1, 7, 8, 4), (512, 9728, 128, 512)])
+                                         (1, 7, 64, 4), (512, 9728, 128, 512)])
 def test_ce_matches_oracle(N, V, d, chunk):
     """The fused GEMM's vocabulary tile follows the waves over the SMs: on 152 SMs the
     small shapes take 192-row tiles, (512, 9728) 256-row ones, and the page's head 224
@@ -89,10 +89,19 @@ def test_ce_empty_batch():
     assert float(loss) == 0.0 and dh.numel() == 0 and not dW.any()
 
 
+@pytest.mark.parametrize("N,V,d,chunk", [(200, 700, 192, 77), (129, 3000, 320, 129)])
+def test_ce_gemm_tails(N, V, d, chunk):
+    """The backward's GEMMs at widths that leave part of a 256-column tile empty (d = 192,
+    320), a vocabulary that is not a multiple of 64 and chunks that are not a multiple of
+    the 128-token tile."""
+    inp, got = run(N, V, d, chunk, seed=N + d)
+    check(inp, got, chunk)
+
+
 def test_ce_out_of_range_target_is_reported():
     """A target outside [0, V): that row's loss is NaN (the kernel reads nothing outside
     the row) and la_device_status reports LA_ERR_DEVICE; the next calls are clean."""
-    h, W, y = make_ce_inputs(8, 50, 16, seed=7)
+    h, W, y = make_ce_inputs(8, 50, 64, seed=7)
     y[3] = 50
     hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
     loss, _ = la.ce_fwd(hd, Wd, yd, ce_chunk=8)
@@ -100,5 +109,5 @@ def test_ce_out_of_range_target_is_reported():
     assert np.isnan(float(loss))
     assert la.la_device_status(1) == 5  # LA_ERR_DEVICE, and clear it
     assert la.la_device_status() == 0
-    inp, got = run(8, 50, 16, 8, seed=7)
+    inp, got = run(8, 50, 64, 8, seed=7)
     check(inp, got, 8)
