@@ -768,6 +768,7 @@ namespace {
 
 constexpr size_t kCeAlign = 256;
 constexpr int kGemmMaxSplit = 8;  // vocabulary ranges of the dh GEMM (its fp32 slices live in the workspace)
+constexpr double kDhShare = 0.4;  // the share of the SMs that the dh GEMM gets beside dW (measured best of 0.4, 0.5, 0.6)
 
 size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 
@@ -928,21 +929,40 @@ bool tmap_f32_out(CUtensorMap* map, float* base, int slices, int rows, int cols)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One GEMM of the cross-entropy's backward (la_gemm.cuh): persistent, one CTA per SM (at
-// most one per work unit).
-template <bool A_MN>
-la_status gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tout, int a_k0, int b_k0,
-                      int M, int N, int KB, int nsplit, int kbs, int reduce, int sms, cudaStream_t s)
+// The cross-entropy backward's GEMM kernel (la_gemm.cuh): persistent, one CTA per SM, the
+// grid cut between one or two problems (p.ctas CTAs each).
+la::GemmProblem gemm_problem(int a_k0, int b_k0, int M, int N, int KB, int nsplit, int kbs, int reduce, bool a_mn)
+{
+    using L = la::GemmLayout;
+    la::GemmProblem p{};
+    p.a_k0 = a_k0;
+    p.b_k0 = b_k0;
+    p.mtiles = (M + L::BM - 1) / L::BM;
+    p.ntiles = (N + L::BN - 1) / L::BN;
+    p.KB = KB;
+    p.nsplit = nsplit;
+    p.kbs = kbs;
+    p.nrows = M;
+    p.ncols = N;
+    p.reduce = reduce;
+    p.a_mn = a_mn ? 1 : 0;
+    p.ctas = 0;
+    return p;
+}
+
+int gemm_units(const la::GemmProblem& p) { return p.mtiles * p.ntiles * p.nsplit; }
+
+la_status gemm_launch(const CUtensorMap& ta0, const CUtensorMap& tb0, const CUtensorMap& to0, const CUtensorMap& ta1,
+                      const CUtensorMap& tb1, const CUtensorMap& to1, const la::GemmProblem& p0,
+                      const la::GemmProblem& p1, cudaStream_t s)
 {
     using L = la::GemmLayout;
     static OptIn flag;
-    auto kern = la::la_gemm_kernel<A_MN>;
-    const la_status st = prepare(kern, flag, L::BYTES);
+    const la_status st = prepare(la::la_gemm_kernel, flag, L::BYTES);
     if (st != LA_OK) return st;
-    const int mtiles = (M + L::BM - 1) / L::BM, ntiles = (N + L::BN - 1) / L::BN;
-    const int units = mtiles * ntiles * nsplit;
-    return launch_pdl(kern, std::min(units, sms), L::THREADS, L::BYTES, s, ta, tb, tout, a_k0, b_k0, mtiles, ntiles,
-                      KB, nsplit, kbs, M, N, reduce);
+    if (p0.ctas <= 0 || p1.ctas < 0) return LA_ERR_INVALID;
+    return launch_pdl(la::la_gemm_kernel, p0.ctas + p1.ctas, L::THREADS, L::BYTES, s, ta0, tb0, to0, ta1, tb1, to1,
+                      p0, p1);
 }
 
 }  // namespace
@@ -1026,10 +1046,13 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     const int bn = ce_tile_width(ce_mtiles<1>(cc, cs), V, sms, true);
     // dh = G W: M = the chunk's tokens (A = GT read token-major), N = d, K = the vocabulary,
     // cut into nsplit ranges (one fp32 slice each, summed in a fixed order);
-    // dW += G^T h: M = the vocabulary (A = GT rows), N = d, K = the chunk's tokens
+    // dW += G^T h: M = the vocabulary (A = GT rows), N = d, K = the chunk's tokens.
+    // Both in one launch: dh gets about kDhShare of the SMs, one unit each (dh is bound by its
+    // MMAs, dW by the write of its fp32 output; side by side they overlap).
     const int kbv = (V + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
     const int ntot_dh = ((cs + la::GemmLayout::BM - 1) / la::GemmLayout::BM) * ((d + la::GemmLayout::BN - 1) / la::GemmLayout::BN);
-    int nsplit = std::max(1, std::min(kGemmMaxSplit, std::min(kbv, sms / std::max(1, ntot_dh))));
+    const int dh_target = std::max(1, (int)(kDhShare * sms + 0.5));
+    int nsplit = std::max(1, std::min(kGemmMaxSplit, std::min(kbv, (dh_target + ntot_dh / 2) / ntot_dh)));
     const int kbs = (kbv + nsplit - 1) / nsplit;
     nsplit = (kbv + kbs - 1) / kbs;
     CUtensorMap th{}, tw{}, tgt{}, ta_mn{}, ta_k{}, tb_w{}, tb_h{}, to_dh{}, to_dw{};
@@ -1045,14 +1068,17 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
         st = ce_persist_launch<1>(th, tw, tgt, bn, c0, nc, cs, V, d, sms, targets + c0, nullptr, nullptr, nullptr,
                                   lse + c0, scale, s);
         if (st != LA_OK) return st;
-        st = gemm_launch<true>(ta_mn, tb_w, to_dh, 0, 0, cs, d, kbv, nsplit, kbs, 0, sms, s);
+        const int kbc = (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
+        la::GemmProblem p_dh = gemm_problem(0, 0, cs, d, kbv, nsplit, kbs, 0, true);
+        la::GemmProblem p_dw = gemm_problem(0, c0, V, d, kbc, 1, kbc, c0 > 0 ? 1 : 0, false);
+        // one CTA per dh unit while that leaves dW at least a quarter of the SMs, else dh_target CTAs
+        p_dh.ctas = gemm_units(p_dh) <= sms - sms / 4 ? gemm_units(p_dh) : std::min(dh_target, sms - 1);
+        p_dw.ctas = std::min(gemm_units(p_dw), sms - p_dh.ctas);
+        st = gemm_launch(ta_mn, tb_w, to_dh, ta_k, tb_h, to_dw, p_dh, p_dw, s);
         if (st != LA_OK) return st;
         const int sum_blocks = (int)std::min<long long>(8LL * sms, ((long long)nc * d / 4 + 255) / 256);
         st = launch_pdl(la::la_gemm_sum_slices_kernel, sum_blocks, 256, 0, s, static_cast<const float*>(dhp), nsplit,
                         cs, d, nc, static_cast<__nv_bfloat16*>(dh) + (size_t)c0 * d);
-        if (st != LA_OK) return st;
-        st = gemm_launch<false>(ta_k, tb_h, to_dw, 0, c0, V, d, (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK, 1,
-                                (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK, c0 > 0 ? 1 : 0, sms, s);
         if (st != LA_OK) return st;
     }
     return LA_OK;
@@ -1078,8 +1104,6 @@ size_t ws_layout(size_t n_x, size_t n_S, size_t n_z, size_t off[16])
     return at;
 }
 
-// The device mapping of page-locked host memory at p, or nullptr when p is not page-locked
-// or not 16-byte aligned (that memory goes through cudaMemcpyAsync instead).
 // The device mapping of a page-locked host buffer [p, p + bytes), or nullptr when the SM
 // copy may not use it: the address and length must be multiples of 16 bytes, and the first
 // and the last byte must both be page-locked with device mappings bytes - 1 apart (a buffer

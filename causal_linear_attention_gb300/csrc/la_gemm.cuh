@@ -7,7 +7,10 @@
 // GT[j][i] = G[i][j] (bf16, row stride cs, tokens contiguous):
 //     dh[i][p] = sum_j G[i][j] W[j][p]      (M = tokens, N = d, K = the vocabulary)
 //     dW[j][p] += sum_i G[i][j] h[i][p]     (M = the vocabulary, N = d, K = the chunk's tokens)
-// One persistent kernel computes D[m][n] = sum_k A[m][k] B[n][k] in 128 x 256 fp32 tiles:
+// One persistent kernel computes D[m][n] = sum_k A[m][k] B[n][k] in 128 x 256 fp32 tiles,
+// for one or two such problems at once (the grid's first CTAs take the first problem, the
+// rest the second: dh is bound by its MMAs, dW by the stream of its fp32 output, and run side
+// by side the two overlap):
 //   - B is read N-major (h and W are row-major with d contiguous): 64-wide atoms of n, one
 //     TMA box each, four per 64-deep slice of K;
 //   - A is read K-major (dW: rows j of GT) or M-major (dh: the tokens of GT are contiguous);
@@ -46,17 +49,22 @@ struct GemmLayout {
     static_assert(STAGE_BYTES % 1024 == 0 && BYTES <= 227 * 1024, "shared memory");
 };
 
-// ta: A as K-major boxes [64 k][128 m] (A_MN false) or M-major boxes [64 m][64 k] (A_MN true);
-// tb: B as N-major boxes [64 n][64 k]; tout: the fp32 output [slices][rows][ncols] as boxes
-// [32 n][32 m][1].  a_k0 / b_k0: K coordinates of the first slice in A / B; mtiles x ntiles
-// output tiles; KB 64-deep slices of K cut into nsplit ranges of kbs slices; unit (split s,
-// tile) writes output slice s.  reduce: TMA reduce-add instead of store.  Boxes that start
-// at or past nrows or ncols are not written (no store starts outside the output).
-template <bool A_MN>
+// One GEMM of a launch.  ta: A as K-major boxes [64 k][128 m] (a_mn 0) or M-major boxes
+// [64 m][64 k] (a_mn 1); tb: B as N-major boxes [64 n][64 k]; tout: the fp32 output
+// [slices][rows][ncols] as boxes [32 n][32 m][1].  a_k0 / b_k0: K coordinates of the first
+// slice in A / B; mtiles x ntiles output tiles; KB 64-deep slices of K cut into nsplit ranges
+// of kbs slices; unit (split s, tile) writes output slice s.  reduce: TMA reduce-add instead
+// of store.  Boxes that start at or past nrows or ncols are not written (no store starts
+// outside the output).  ctas: the CTAs of the grid that work on this problem.
+struct GemmProblem {
+    int a_k0, b_k0, mtiles, ntiles, KB, nsplit, kbs, nrows, ncols, reduce, a_mn, ctas;
+};
+
 __global__ void __launch_bounds__(192, 1)
-la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-               const __grid_constant__ CUtensorMap tout, int a_k0, int b_k0, int mtiles, int ntiles, int KB, int nsplit,
-               int kbs, int nrows, int ncols, int reduce)
+la_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
+               const __grid_constant__ CUtensorMap tout0, const __grid_constant__ CUtensorMap ta1,
+               const __grid_constant__ CUtensorMap tb1, const __grid_constant__ CUtensorMap tout1,
+               const GemmProblem p0, const GemmProblem p1)
 {
     using L = GemmLayout;
     using namespace tc;
@@ -73,7 +81,15 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     uint64_t* tempty = tfull + 2;             // [2] the epilogue has read an accumulator
     uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ntot = mtiles * ntiles, nunits = ntot * nsplit;
+    const bool second = (int)blockIdx.x >= p0.ctas;
+    const GemmProblem& P = second ? p1 : p0;
+    const CUtensorMap* ta = second ? &ta1 : &ta0;
+    const CUtensorMap* tb = second ? &tb1 : &tb0;
+    const CUtensorMap* tout = second ? &tout1 : &tout0;
+    const int first = second ? (int)blockIdx.x - p0.ctas : (int)blockIdx.x, stride = P.ctas;
+    const bool a_mn = P.a_mn != 0;
+    const int mtiles = P.mtiles, ntiles = P.ntiles, KB = P.KB, kbs = P.kbs, nrows = P.nrows, ncols = P.ncols;
+    const int ntot = mtiles * ntiles, nunits = ntot * P.nsplit;
 
     if (tid == 0) {
         for (int s = 0; s < L::STAGES; ++s) {
@@ -103,19 +119,19 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     auto unit = [&](int u, int& m0, int& n0, int& kb0, int& kb1, int& s) {
         s = u / ntot;
         const int T = u % ntot;
-        m0 = (A_MN ? T % mtiles : T / ntiles) * L::BM;
-        n0 = (A_MN ? T / mtiles : T % ntiles) * L::BN;
+        m0 = (a_mn ? T % mtiles : T / ntiles) * L::BM;
+        n0 = (a_mn ? T / mtiles : T % ntiles) * L::BN;
         kb0 = s * kbs;
         kb1 = min(KB, kb0 + kbs);
     };
 
     if (warp == 4) {
         if (lane == 0) {  // TMA producer: every (unit, K slice) of this CTA, in order
-            prefetch_tmap(&ta);
-            prefetch_tmap(&tb);
+            prefetch_tmap(ta);
+            prefetch_tmap(tb);
             int g = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            for (int u = first; u < nunits && ok; u += stride) {
                 int m0, n0, kb0, kb1, s;
                 unit(u, m0, n0, kb0, kb1, s);
                 for (int kb = kb0; kb < kb1; ++kb, ++g) {
@@ -123,23 +139,23 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                     if (r > 0 && !(ok = mbar_wait(empty + st, (r - 1) & 1, ERR_TIMEOUT_MMA))) break;
                     unsigned char* p = sm + st * L::STAGE_BYTES;
                     mbar_expect_tx(full + st, L::STAGE_BYTES);
-                    if (A_MN) {
-                        tma_load_3d(p, &ta, full + st, m0, a_k0 + kb * L::BK, 0);
-                        tma_load_3d(p + 8192, &ta, full + st, m0 + 64, a_k0 + kb * L::BK, 0);
+                    if (a_mn) {
+                        tma_load_3d(p, ta, full + st, m0, P.a_k0 + kb * L::BK, 0);
+                        tma_load_3d(p + 8192, ta, full + st, m0 + 64, P.a_k0 + kb * L::BK, 0);
                     } else {
-                        tma_load_3d(p, &ta, full + st, a_k0 + kb * L::BK, m0, 0);
+                        tma_load_3d(p, ta, full + st, P.a_k0 + kb * L::BK, m0, 0);
                     }
 #pragma unroll
                     for (int b = 0; b < L::BN / 64; ++b)
-                        tma_load_3d(p + L::A_BYTES + b * 8192, &tb, full + st, n0 + 64 * b, b_k0 + kb * L::BK, 0);
+                        tma_load_3d(p + L::A_BYTES + b * 8192, tb, full + st, n0 + 64 * b, P.b_k0 + kb * L::BK, 0);
                 }
             }
         }
     } else if (warp == 5) {  // UMMA issuer: the whole warp waits, one elected lane issues
-        const uint32_t id = idesc_bf16(L::BM, L::BN, A_MN, true);
+        const uint32_t id = idesc_bf16(L::BM, L::BN, a_mn, true);
         int g = 0, lt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++lt) {
+        for (int u = first; u < nunits && ok; u += stride, ++lt) {
             int m0, n0, kb0, kb1, s;
             unit(u, m0, n0, kb0, kb1, s);
             const int acc = lt & 1, ua = lt >> 1;
@@ -153,11 +169,11 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                     const uint32_t a = sbase + st * L::STAGE_BYTES;
                     // K-major A: +32 B per K = 16 step; M-major A and N-major B: +16 rows (2048 B);
                     // M-major atoms 8 KB apart (the LBO field), 8-row K groups 1 KB apart
-                    const uint64_t dA = A_MN ? smem_desc(a, 8192, 1024) : smem_desc(a, 16, 1024);
+                    const uint64_t dA = a_mn ? smem_desc(a, 8192, 1024) : smem_desc(a, 16, 1024);
                     const uint64_t dB = smem_desc(a + L::A_BYTES, 8192, 1024);
 #pragma unroll
                     for (int kk = 0; kk < L::BK / 16; ++kk)
-                        umma_bf16(tmem + acc * L::ACC_COLS, dA + (A_MN ? kk * 128 : kk * 2), dB + kk * 128, id,
+                        umma_bf16(tmem + acc * L::ACC_COLS, dA + (a_mn ? kk * 128 : kk * 2), dB + kk * 128, id,
                                   kb > kb0 || kk > 0);
                     umma_commit(empty + st);
                 }
@@ -174,7 +190,7 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         unsigned char* wst = sm + L::OSTAGE + warp * 2 * L::WBOX;
         int lt = 0, nbox = 0;
-        for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lt) {
+        for (int u = first; u < nunits; u += stride, ++lt) {
             int m0, n0, kb0, kb1, s;
             unit(u, m0, n0, kb0, kb1, s);
             const int acc = lt & 1;
@@ -200,10 +216,10 @@ la_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0) {
                     if (n0 + 32 * c < ncols && m0 + 32 * warp < nrows) {
-                        if (reduce)
-                            tma_reduce_add_3d(&tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
+                        if (P.reduce)
+                            tma_reduce_add_3d(tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
                         else
-                            tma_store_3d(&tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
+                            tma_store_3d(tout, ob, n0 + 32 * c, m0 + 32 * warp, s);
                     }
                     tma_store_commit();  // (an empty group when nothing was written)
                 }
