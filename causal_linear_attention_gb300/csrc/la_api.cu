@@ -768,7 +768,9 @@ namespace {
 
 constexpr size_t kCeAlign = 256;
 constexpr int kGemmMaxSplit = 8;  // vocabulary ranges of the dh GEMM (its fp32 slices live in the workspace)
-constexpr double kDhShare = 0.4;  // the share of the SMs that the dh GEMM gets beside dW (measured best of 0.4, 0.5, 0.6)
+// The share of the GEMM kernel's CTA pairs that dh gets beside dW: measured best at chunks of
+// 512 and of 128 tokens among 0.3 - 0.5 and against a split by estimated cost.
+constexpr double kDhShare = 0.4;
 
 size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 
@@ -929,15 +931,15 @@ bool tmap_f32_out(CUtensorMap* map, float* base, int slices, int rows, int cols)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The cross-entropy backward's GEMM kernel (la_gemm.cuh): persistent, one CTA per SM, the
-// grid cut between one or two problems (p.ctas CTAs each).
+// The cross-entropy backward's GEMM kernel (la_gemm.cuh): persistent, one CTA per SM in pairs
+// (clusters of two), the grid cut between one or two problems (p.ctas CTAs each, even).
 la::GemmProblem gemm_problem(int a_k0, int b_k0, int M, int N, int KB, int nsplit, int kbs, int reduce, bool a_mn)
 {
     using L = la::GemmLayout;
     la::GemmProblem p{};
     p.a_k0 = a_k0;
     p.b_k0 = b_k0;
-    p.mtiles = (M + L::BM - 1) / L::BM;
+    p.mtiles = (M + L::PM - 1) / L::PM;
     p.ntiles = (N + L::BN - 1) / L::BN;
     p.KB = KB;
     p.nsplit = nsplit;
@@ -952,15 +954,37 @@ la::GemmProblem gemm_problem(int a_k0, int b_k0, int M, int N, int KB, int nspli
 
 int gemm_units(const la::GemmProblem& p) { return p.mtiles * p.ntiles * p.nsplit; }
 
+// How many CTA pairs of the GEMM kernel the device holds at once (cached per device), or 0.
+int gemm_max_pairs()
+{
+    using L = la::GemmLayout;
+    static std::atomic<int> cached[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2u * (unsigned)std::max(1, sm_count()));
+        cfg.blockDim = dim3((unsigned)L::THREADS);
+        cfg.dynamicSmemBytes = L::BYTES;
+        if (cudaOccupancyMaxActiveClusters(&n, la::la_gemm_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 la_status gemm_launch(const CUtensorMap& ta0, const CUtensorMap& tb0, const CUtensorMap& to0, const CUtensorMap& ta1,
                       const CUtensorMap& tb1, const CUtensorMap& to1, const la::GemmProblem& p0,
                       const la::GemmProblem& p1, cudaStream_t s)
 {
     using L = la::GemmLayout;
-    static OptIn flag;
-    const la_status st = prepare(la::la_gemm_kernel, flag, L::BYTES);
-    if (st != LA_OK) return st;
-    if (p0.ctas <= 0 || p1.ctas < 0) return LA_ERR_INVALID;
+    if (p0.ctas <= 0 || p1.ctas < 0 || p0.ctas % 2 || p1.ctas % 2) return LA_ERR_INVALID;
     return launch_pdl(la::la_gemm_kernel, p0.ctas + p1.ctas, L::THREADS, L::BYTES, s, ta0, tb0, to0, ta1, tb1, to1,
                       p0, p1);
 }
@@ -1047,11 +1071,18 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     // dh = G W: M = the chunk's tokens (A = GT read token-major), N = d, K = the vocabulary,
     // cut into nsplit ranges (one fp32 slice each, summed in a fixed order);
     // dW += G^T h: M = the vocabulary (A = GT rows), N = d, K = the chunk's tokens.
-    // Both in one launch: dh gets about kDhShare of the SMs, one unit each (dh is bound by its
-    // MMAs, dW by the write of its fp32 output; side by side they overlap).
+    // Both in one launch, on CTA pairs: dh gets about kDhShare of the pairs, one unit each (dh is
+    // bound by its MMAs, dW by the write of its fp32 output; side by side they overlap).
+    {
+        static OptIn flag;
+        st = prepare(la::la_gemm_kernel, flag, la::GemmLayout::BYTES);
+        if (st != LA_OK) return st;
+    }
+    const int pairs = gemm_max_pairs();
+    if (pairs < 2) return LA_ERR_UNSUPPORTED;
     const int kbv = (V + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
-    const int ntot_dh = ((cs + la::GemmLayout::BM - 1) / la::GemmLayout::BM) * ((d + la::GemmLayout::BN - 1) / la::GemmLayout::BN);
-    const int dh_target = std::max(1, (int)(kDhShare * sms + 0.5));
+    const int ntot_dh = ((cs + la::GemmLayout::PM - 1) / la::GemmLayout::PM) * ((d + la::GemmLayout::BN - 1) / la::GemmLayout::BN);
+    const int dh_target = std::max(1, (int)(kDhShare * pairs + 0.5));
     int nsplit = std::max(1, std::min(kGemmMaxSplit, std::min(kbv, (dh_target + ntot_dh / 2) / ntot_dh)));
     const int kbs = (kbv + nsplit - 1) / nsplit;
     nsplit = (kbv + kbs - 1) / kbs;
@@ -1071,9 +1102,10 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
         const int kbc = (nc + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
         la::GemmProblem p_dh = gemm_problem(0, 0, cs, d, kbv, nsplit, kbs, 0, true);
         la::GemmProblem p_dw = gemm_problem(0, c0, V, d, kbc, 1, kbc, c0 > 0 ? 1 : 0, false);
-        // one CTA per dh unit while that leaves dW at least a quarter of the SMs, else dh_target CTAs
-        p_dh.ctas = gemm_units(p_dh) <= sms - sms / 4 ? gemm_units(p_dh) : std::min(dh_target, sms - 1);
-        p_dw.ctas = std::min(gemm_units(p_dw), sms - p_dh.ctas);
+        // one pair per dh unit while that leaves dW at least a quarter of the pairs, else dh_target pairs
+        const int dh_pairs = gemm_units(p_dh) <= pairs - pairs / 4 ? gemm_units(p_dh) : std::min(dh_target, pairs - 1);
+        p_dh.ctas = 2 * dh_pairs;
+        p_dw.ctas = 2 * std::min(gemm_units(p_dw), pairs - dh_pairs);
         st = gemm_launch(ta_mn, tb_w, to_dh, ta_k, tb_h, to_dw, p_dh, p_dw, s);
         if (st != LA_OK) return st;
         const int sum_blocks = (int)std::min<long long>(8LL * sms, ((long long)nc * d / 4 + 255) / 256);
