@@ -81,7 +81,7 @@ def chunked_fwd(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float = 1e-6
 
 def chunked_fwd_split(q, k, v, S0=None, z0=None, *, block: int = 64, eps: float = 1e-6, o=None, S_out=None,
                       z_out=None, workspace=None, stream=None):
-    """chunked_fwd cut along the tokens for few groups of long chunks (bf16, D = 64): the
+    """chunked_fwd cut along the tokens for few groups of long chunks (bf16, D = 64 or 128): the
     pieces of every group run on separate CTAs from carries computed by a prefix over the
     pieces' own sums.  `workspace` (a CUDA tensor of at least la_fwd_split_workspace_bytes
     bytes) is allocated here when not given.  Returns (o, S_out, z_out)."""

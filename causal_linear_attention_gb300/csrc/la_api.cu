@@ -202,8 +202,11 @@ la_status fwd_tile_launch(const void* q, const void* k, const void* v, const flo
                       S_out, z_out, C, eps);
 }
 
+// The bf16 head-size-128 forward; with piece_carry != nullptr, the G * P pieces of the
+// chunk-parallel forward (la_chunked_fwd_split).
 la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
-                           float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+                           float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream, int P = 1,
+                           int PL = 0, const float* piece_carry = nullptr)
 {
     static OptIn flag;
     auto kern = la::la_fwd_tc128_kernel;
@@ -216,8 +219,8 @@ la_status fwd_tc128_launch(const void* q, const void* k, const void* v, const fl
             !tmap_bf16(&to, o, G, C, 128, R))
             return LA_ERR_CUDA;
     }
-    return launch_pdl(kern, G, la::FwdTc128Layout::THREADS, la::FwdTc128Layout::BYTES, stream, tq, tk, tv, to, S0,
-                      z0, S_out, z_out, C, eps);
+    return launch_pdl(kern, piece_carry ? G * P : G, la::FwdTc128Layout::THREADS, la::FwdTc128Layout::BYTES, stream,
+                      tq, tk, tv, to, S0, z0, S_out, z_out, C, eps, P, PL, piece_carry);
 }
 
 // The bf16 head-size-64 backward of a chunk that fits one 128-token tile (0 <= C <= 128).
@@ -433,59 +436,75 @@ int sm_count()
 }
 
 // How a chunk is cut: P pieces of PL tokens (the last one ragged, none empty) so that
-// G * P CTAs about fill the GPU at `per_sm` per SM (the forward's kernel fits two on an
-// SM, the backward's one); P = 1 when that does not help or does not apply.
+// G * P CTAs about fill the GPU at the forward kernel's CTAs per SM (two at head size 64,
+// one at 128; the backward's kernel fits one); P = 1 when that does not help or does not
+// apply.  max_cells > 0 caps the workspace at that many cells.
 struct SplitPlan {
     int P = 1, PL = 0;
     size_t bytes = 0;  // workspace: `cells` cells per piece
 };
 
-bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan, int per_sm = 2, int cells = 1)
+size_t cell_bytes(int D) { return (size_t)(D * D + D) * 4; }
+
+bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan, bool backward = false, int max_cells = 0)
 {
     *plan = SplitPlan{};
     plan->PL = C;
-    if (dtype != LA_BF16 || D != 64 || G <= 0 || C <= 128) return true;
+    if (dtype != LA_BF16 || (D != 64 && (D != 128 || backward)) || G <= 0 || C <= 128) return true;
+    const int per_sm = backward || D == 128 ? 1 : 2, cells = backward ? 2 : 1;
     const int sms = sm_count();
     if (sms == 0) return false;
     const int nsb = (C + 127) / 128;
-    const int want = std::min(nsb, std::max(1, per_sm * sms / G));
+    int want = std::min(nsb, std::max(1, per_sm * sms / G));
+    if (max_cells > 0) want = std::min(want, std::max(1, max_cells / (cells * G)));
     if (want <= 1) return true;
     const int bpp = (nsb + want - 1) / want;  // 128-token blocks per piece
     plan->P = (nsb + bpp - 1) / bpp;
     plan->PL = bpp * 128;
-    plan->bytes = plan->P > 1 ? (size_t)cells * G * plan->P * la::DeltaLayout::CELL * 4 : 0;
+    plan->bytes = plan->P > 1 ? (size_t)cells * G * plan->P * cell_bytes(D) : 0;
     if (plan->P == 1) plan->PL = C;
     return true;
 }
 
 bool bwd_split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
 {
-    return split_plan(G, C, D, dtype, plan, 1, 2);
+    return split_plan(G, C, D, dtype, plan, true);
 }
 
 // Every piece's forward carry into ws: the pieces' sums of k v^T and k, then their
 // exclusive prefix from S0, z0.
-la_status piece_carries(const void* k, const void* v, const float* S0, const float* z0, int G, int C,
+la_status piece_carries(const void* k, const void* v, const float* S0, const float* z0, int G, int C, int D,
                         const SplitPlan& plan, float* ws, cudaStream_t stream)
 {
-    static OptIn dflag;
-    auto dkern = la::la_state_delta_kernel;
-    la_status st = prepare(dkern, dflag, la::DeltaLayout::BYTES);
-    if (st != LA_OK) return st;
     CUtensorMap tk{}, tv{};
-    if (!tmap_bf16(&tk, k, G, C, 64, 128) || !tmap_bf16(&tv, v, G, C, 64, 128)) return LA_ERR_CUDA;
-    st = launch_pdl(dkern, G * plan.P, la::DeltaLayout::THREADS, la::DeltaLayout::BYTES, stream, tk, tv, C, plan.P,
-                    plan.PL, ws);
+    if (!tmap_bf16(&tk, k, G, C, D, 128) || !tmap_bf16(&tv, v, G, C, D, 128)) return LA_ERR_CUDA;
+    la_status st;
+    if (D == 64) {
+        static OptIn dflag;
+        st = prepare(la::la_state_delta_kernel, dflag, la::DeltaLayout::BYTES);
+        if (st == LA_OK)
+            st = launch_pdl(la::la_state_delta_kernel, G * plan.P, la::DeltaLayout::THREADS, la::DeltaLayout::BYTES,
+                            stream, tk, tv, C, plan.P, plan.PL, ws);
+        if (st != LA_OK) return st;
+        return launch_pdl(la::la_state_scan_kernel<64>, G * la::scan_blocks(64), 256, 0, stream, S0, z0, ws, plan.P);
+    }
+    static OptIn dflag128;
+    st = prepare(la::la_state_delta128_kernel, dflag128, la::Delta128Layout::BYTES);
+    if (st == LA_OK)
+        st = launch_pdl(la::la_state_delta128_kernel, G * plan.P, la::Delta128Layout::THREADS,
+                        la::Delta128Layout::BYTES, stream, tk, tv, C, plan.P, plan.PL, ws);
     if (st != LA_OK) return st;
-    return launch_pdl(la::la_state_scan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, S0, z0, ws, plan.P);
+    return launch_pdl(la::la_state_scan_kernel<128>, G * la::scan_blocks(128), 256, 0, stream, S0, z0, ws, plan.P);
 }
 
 la_status fwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
-                           float* S_out, float* z_out, int G, int C, float eps, const SplitPlan& plan, float* ws,
-                           cudaStream_t stream)
+                           float* S_out, float* z_out, int G, int C, int D, float eps, const SplitPlan& plan,
+                           float* ws, cudaStream_t stream)
 {
-    const la_status st = piece_carries(k, v, S0, z0, G, C, plan, ws, stream);
+    const la_status st = piece_carries(k, v, S0, z0, G, C, D, plan, ws, stream);
     if (st != LA_OK) return st;
+    if (D == 128)
+        return fwd_tc128_launch(q, k, v, nullptr, nullptr, o, S_out, z_out, G, C, eps, stream, plan.P, plan.PL, ws);
     return fwd_tc_launch(q, k, v, nullptr, nullptr, o, S_out, z_out, G, C, eps, stream, plan.P, plan.PL, ws);
 }
 
@@ -499,7 +518,7 @@ la_status bwd_split_launch(const void* q, const void* k, const void* v, const fl
 {
     float* fcell = ws;
     float* rcell = ws + (size_t)G * plan.P * la::DeltaLayout::CELL;
-    la_status st = piece_carries(k, v, S0, z0, G, C, plan, fcell, stream);
+    la_status st = piece_carries(k, v, S0, z0, G, C, 64, plan, fcell, stream);
     if (st != LA_OK) return st;
     st = bwd_tcm_launch<64>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
                             stream, plan.P, plan.PL, 1, fcell, rcell);
@@ -540,7 +559,7 @@ extern "C" la_status la_chunked_fwd_split(const void* q, const void* k, const vo
     const Buf all[] = {{q, n_x}, {k, n_x}, {v, n_x}, {S0, n_S}, {z0, n_z}, {o, n_x}, {S_out, n_S}, {z_out, n_z}};
     for (const Buf& b : all)
         if (overlaps(wsb, b)) return LA_ERR_INVALID;
-    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, plan, static_cast<float*>(workspace),
+    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, D, eps, plan, static_cast<float*>(workspace),
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -588,12 +607,12 @@ extern "C" la_status la_chunked_fwd_split_static(const void* q, const void* k, c
     if (st != LA_OK) return st;
     if (G == 0) return LA_OK;
     SplitPlan plan;
-    if (!split_plan(G, C, D, dtype, &plan)) return LA_ERR_CUDA;
+    if (!split_plan(G, C, D, dtype, &plan, false, (int)(kStaticScratchBytes / cell_bytes(D)))) return LA_ERR_CUDA;
     if (plan.P == 1) return la_chunked_fwd(q, k, v, S0, z0, o, S_out, z_out, G, C, D, block, dtype, eps, stream);
     if (plan.bytes > kStaticScratchBytes) return LA_ERR_UNSUPPORTED;
     void* ws = static_split_scratch();
     if (!ws) return LA_ERR_CUDA;
-    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, plan, static_cast<float*>(ws),
+    return fwd_split_launch(q, k, v, S0, z0, o, S_out, z_out, G, C, D, eps, plan, static_cast<float*>(ws),
                             static_cast<cudaStream_t>(stream));
 }
 

@@ -12,7 +12,8 @@
 // fill the GPU.  The result equals the sequential one up to the order of the fp32 sums.
 //
 // The per-piece sums live in a caller-provided device workspace: for piece p of group g,
-// the D x D fp32 sum [p][c] followed by the D fp32 key sums (4160 floats at D = 64).
+// the D x D fp32 sum [p][c] followed by the D fp32 key sums (4160 floats at D = 64, 16512
+// at D = 128).  The forward runs at head size 64 and 128; the backward at 64.
 //
 // The backward runs the same way in reverse ("the derivative of a cumsum is a reverse
 // cumsum", section 1): with every piece's forward carry known, the pass-1 launch of the
@@ -179,19 +180,167 @@ la_state_delta_kernel(const __grid_constant__ CUtensorMap tk, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
+// The head-size-128 piece sums: the same work as la_state_delta_kernel on 128-row tiles of
+// two 64-column atoms each; the transposed sum is an M = 128 accumulator (TMEM lane c holds
+// column c of the sum), written straight to the cell (the 32 lanes of a warp cover 128
+// contiguous bytes of a row).
+struct Delta128Layout {
+    static constexpr int D = 128;
+    static constexpr uint32_t ATOM = 16384;           // 128 rows x 64 bf16 columns
+    static constexpr uint32_t KT0 = 0, KT1 = 32768;   // K tiles, two stages of two atoms
+    static constexpr uint32_t VT0 = 65536, VT1 = 98304;
+    static constexpr uint32_t ZPART = 131072;         // float[4][128]
+    static constexpr uint32_t BARS = 133120;
+    static constexpr uint32_t END = 133248;
+    static constexpr uint32_t BYTES = END;
+    static constexpr uint32_t TMEM_COLS = 128;
+    static constexpr int THREADS = 160;
+    static constexpr uint32_t CELL = D * D + D;
+};
+
+__global__ void __launch_bounds__(160, 1)
+la_state_delta128_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, int C,
+                         int P, int PL, float* delta)
+{
+    using L = Delta128Layout;
+    using namespace tc;
+    constexpr int D = L::D;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t sbase = smem_addr(sm);
+    float* zpart = reinterpret_cast<float*>(sm + L::ZPART);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* full = bars + 0;   // [2] K, V of a stage landed (TMA)
+    uint64_t* empty = bars + 2;  // [2] a stage's MMA and column sums are done (MMA commit + 128)
+    uint64_t* done = bars + 4;   // every MMA of the piece is done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 40);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = (int)blockIdx.x / P, piece = (int)blockIdx.x % P;
+    const int rbase = piece * PL;
+    const int nblk = (min(PL, C - rbase) + 127) / 128;
+
+    if (tid == 0) {
+        mbar_init(full + 0, 1);
+        mbar_init(full + 1, 1);
+        mbar_init(empty + 0, 129);
+        mbar_init(empty + 1, 129);
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            auto load = [&](int blk) {
+                const int s = blk & 1;
+                unsigned char* kt = sm + (s ? L::KT1 : L::KT0);
+                unsigned char* vt = sm + (s ? L::VT1 : L::VT0);
+                mbar_expect_tx(full + s, 4 * L::ATOM);
+                tma_load_3d(kt, &tk, full + s, 0, rbase + blk * 128, g);
+                tma_load_3d(kt + L::ATOM, &tk, full + s, 64, rbase + blk * 128, g);
+                tma_load_3d(vt, &tv, full + s, 0, rbase + blk * 128, g);
+                tma_load_3d(vt + L::ATOM, &tv, full + s, 64, rbase + blk * 128, g);
+            };
+            for (int blk = 0; blk < min(2, nblk); ++blk) load(blk);
+            pdl_launch_dependents();
+            const uint32_t id_state = idesc_bf16(128, 128, true, true);
+            bool ok = true;
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int s = blk & 1;
+                const uint32_t ph = (blk >> 1) & 1;
+                ok = mbar_wait(full + s, ph, ERR_TIMEOUT_TMA);
+                if (!ok) break;
+                tc_fence_after();
+                // MN-major operands of two 64-wide atoms (LBO = one atom), 16 rows per K = 16 step
+                const uint64_t dK = smem_desc(sbase + (s ? L::KT1 : L::KT0), L::ATOM, 1024);
+                const uint64_t dV = smem_desc(sbase + (s ? L::VT1 : L::VT0), L::ATOM, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // sum^T += V^T K  (M = c, N = p, K = j)
+                    umma_bf16(tmem, dV + kk * 128, dK + kk * 128, id_state, blk > 0 || kk > 0);
+                umma_commit(empty + s);
+                if (blk + 2 < nblk) {
+                    ok = mbar_wait(empty + s, ph, ERR_TIMEOUT_MMA);
+                    if (ok) load(blk + 2);
+                }
+            }
+            umma_commit(done);
+        }
+    } else {
+        // ---- column sums of K: thread (cc, rg) sums 16 rows x 8 columns of every block
+        const int t = tid, cc = t & 15, rg = t >> 4;
+        float zs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zs[e] = 0.f;
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int s = blk & 1;
+            mbar_wait(full + s, (blk >> 1) & 1, ERR_TIMEOUT_TMA);
+            const uint32_t kt = (s ? L::KT1 : L::KT0) + (uint32_t)(cc >> 3) * L::ATOM;
+#pragma unroll 4
+            for (int r = 0; r < 16; ++r) {
+                const uint4 u = *reinterpret_cast<const uint4*>(sm + kt + sw_chunk(rg * 16 + r, cc & 7));
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    zs[2 * e] += f.x;
+                    zs[2 * e + 1] += f.y;
+                }
+            }
+            mbar_arrive(empty + s);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zs[e] += __shfl_xor_sync(0xffffffffu, zs[e], 16);
+        if (lane < 16)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zpart[warp * D + 8 * cc + e] = zs[e];
+        // ---- the sum of outer products: TMEM lane c holds column c of the sum
+        mbar_wait(done, 0, ERR_TIMEOUT_MMA);
+        tc_fence_after();
+        float* cell = delta + (size_t)blockIdx.x * L::CELL;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[64];
+            tmem_ld32x64(tmem + ((uint32_t)(32 * warp) << 16) + 64 * h, r);
+#pragma unroll
+            for (int p = 0; p < 64; ++p) cell[(size_t)(64 * h + p) * D + t] = __uint_as_float(r[p]);
+        }
+        epi_sync();
+        cell[D * D + t] = zpart[t] + zpart[D + t] + zpart[2 * D + t] + zpart[3 * D + t];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
 // Exclusive prefix over each group's pieces, in place: piece p's cell becomes the state
-// before it (S0 plus the sums of pieces 0..p-1).  SCAN_BLOCKS blocks of 256 threads per
+// before it (S0 plus the sums of pieces 0..p-1).  scan_blocks(D) blocks of 256 threads per
 // group, one element of the cell per thread.
 constexpr int SCAN_BLOCKS = (DeltaLayout::CELL + 255) / 256;
+__host__ __device__ constexpr int scan_blocks(int D) { return (D * D + D + 255) / 256; }
 
+template <int D>
 __global__ void __launch_bounds__(256)
 la_state_scan_kernel(const float* S0, const float* z0, float* delta, int P)
 {
-    constexpr int D = DeltaLayout::D;
-    constexpr uint32_t CELL = DeltaLayout::CELL;
+    constexpr uint32_t CELL = D * D + D;
+    constexpr int NB = scan_blocks(D);
     pdl_wait();
-    const int e = ((int)blockIdx.x % SCAN_BLOCKS) * 256 + threadIdx.x;
-    const size_t g = blockIdx.x / SCAN_BLOCKS;
+    const int e = ((int)blockIdx.x % NB) * 256 + threadIdx.x;
+    const size_t g = blockIdx.x / NB;
     if (e >= (int)CELL) return;
     float run = e < D * D ? (S0 ? S0[g * D * D + e] : 0.f) : (z0 ? z0[g * D + (e - D * D)] : 0.f);
     float* cell = delta + g * P * CELL + e;

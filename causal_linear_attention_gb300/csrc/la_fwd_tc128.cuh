@@ -8,7 +8,8 @@
 // As in the head-size-64 kernel, the tensor core walks the chunk in blocks of 128 tokens
 // whatever block the caller names (the block size changes only the rounding).
 //
-// One CTA per group (one per SM: 227 KB of shared memory, 512 TMEM columns), warp-
+// One CTA per group, or per piece of a group's chunk in the chunk-parallel forward (piece
+// mode, below); one per SM: 227 KB of shared memory, 512 TMEM columns.  Warp-
 // specialised: warps 0-3 own the rows of a block (thread t <-> TMEM lane t), warp 4 is
 // the producer (TMA loads; one lane issues every tcgen05.mma).  Per block:
 //   I1a    A = Q K^T                (M=128, N=128, K=128: 8 instructions)
@@ -71,8 +72,13 @@ __device__ __forceinline__ uint32_t sw_chunk2(int row, int chunk)
 __global__ void __launch_bounds__(160, 1)
 la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                    const float* S0, const float* z0, float* S_out, float* z_out, int C, float eps)
+                    const float* S0, const float* z0, float* S_out, float* z_out, int C, float eps, int P = 1,
+                    int PL = 0, const float* piece_carry = nullptr)
 {
+    // Piece mode (piece_carry != nullptr): the chunk of each group is cut into P pieces of PL
+    // tokens (a multiple of 128; the last piece ragged); CTA b runs piece b % P of group b / P
+    // from the carry piece_carry[b] (S [D][D] then z [D], fp32) and writes S_out, z_out only
+    // for the last piece, whose final state is the group's.
     using L = FwdTc128Layout;
     using namespace tc;
     constexpr int D = 128;
@@ -98,8 +104,18 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 96);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x;
-    const int nsb = (C + 127) / 128;
+    const int g = piece_carry ? (int)blockIdx.x / P : (int)blockIdx.x;  // group
+    const int piece = piece_carry ? (int)blockIdx.x % P : 0;
+    const int rbase = piece * PL;                                          // first token of the piece
+    const int nsb = ((piece_carry ? min(PL, C - rbase) : C) + 127) / 128;
+    // this CTA's incoming carry: the group's S0 / z0, or the piece's cell
+    const float* S0g = S0 ? S0 + (size_t)g * D * D : nullptr;
+    const float* z0g = z0 ? z0 + (size_t)g * D : nullptr;
+    if (piece_carry) {
+        S0g = piece_carry + (size_t)blockIdx.x * (D * D + D);
+        z0g = S0g + D * D;
+        if (piece + 1 < P) S_out = z_out = nullptr;
+    }
 
     if (tid == 0) {
         mbar_init(bar_s0, 1);
@@ -118,9 +134,9 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         tmem_relinquish();
     }
     if (warp < 4) {  // S0 / z0 absent: zero carry
-        if (!S0)
+        if (!S0g)
             for (int i = tid; i < 65536 / 16; i += 128) reinterpret_cast<uint4*>(sm + L::S0F)[i] = make_uint4(0, 0, 0, 0);
-        if (!z0) zin[tid] = 0.f;
+        if (!z0g) zin[tid] = 0.f;
     }
     fence_async_smem();
     tc_fence_before();
@@ -136,12 +152,12 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         prefetch_tmap(&tv);
         prefetch_tmap(&to);
         for (int a = 0; a < 2; ++a) {
-            tma_prefetch_3d(&tq, 64 * a, 0, g);
-            tma_prefetch_3d(&tk, 64 * a, 0, g);
-            tma_prefetch_3d(&tv, 64 * a, 0, g);
+            tma_prefetch_3d(&tq, 64 * a, rbase, g);
+            tma_prefetch_3d(&tk, 64 * a, rbase, g);
+            tma_prefetch_3d(&tv, 64 * a, rbase, g);
         }
-        if (S0) prefetch_l2(S0 + (size_t)g * D * D, 65536);
-        if (z0) prefetch_l2(z0 + (size_t)g * D, 512);
+        if (S0g) prefetch_l2(S0g, 65536);
+        if (z0g) prefetch_l2(z0g, 512);
     }
     pdl_wait();  // inputs may have been written by the previous kernel in the stream
 
@@ -150,22 +166,22 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         if (lane == 0) {
             auto issue_qk = [&](int sb) {
                 mbar_expect_tx(bar_qk, L::QK_BYTES);
-                tma_load_3d(sm + L::QT, &tq, bar_qk, 0, sb * 128, g);
-                tma_load_3d(sm + L::QT + L::ATOM, &tq, bar_qk, 64, sb * 128, g);
-                tma_load_3d(sm + L::KT, &tk, bar_qk, 0, sb * 128, g);
-                tma_load_3d(sm + L::KT + L::ATOM, &tk, bar_qk, 64, sb * 128, g);
+                tma_load_3d(sm + L::QT, &tq, bar_qk, 0, rbase + sb * 128, g);
+                tma_load_3d(sm + L::QT + L::ATOM, &tq, bar_qk, 64, rbase + sb * 128, g);
+                tma_load_3d(sm + L::KT, &tk, bar_qk, 0, rbase + sb * 128, g);
+                tma_load_3d(sm + L::KT + L::ATOM, &tk, bar_qk, 64, rbase + sb * 128, g);
             };
             auto issue_v = [&](int sb) {
                 mbar_expect_tx(bar_v, L::V_BYTES);
-                tma_load_3d(sm + L::VT, &tv, bar_v, 0, sb * 128, g);
-                tma_load_3d(sm + L::VT + L::ATOM, &tv, bar_v, 64, sb * 128, g);
+                tma_load_3d(sm + L::VT, &tv, bar_v, 0, rbase + sb * 128, g);
+                tma_load_3d(sm + L::VT + L::ATOM, &tv, bar_v, 64, rbase + sb * 128, g);
             };
             if (nsb > 0) {  // Q, K first (I1a), then the carry (after the score epilogue), then V
                 issue_qk(0);
                 // (with neither S0 nor z0 this arrival alone completes the phase)
-                mbar_expect_tx(bar_s0, (S0 ? 65536u : 0u) + (z0 ? 512u : 0u));
-                if (S0) bulk_load(sm + L::S0F, S0 + (size_t)g * D * D, 65536, bar_s0);
-                if (z0) bulk_load(sm + L::ZIN, z0 + (size_t)g * D, 512, bar_s0);
+                mbar_expect_tx(bar_s0, (S0g ? 65536u : 0u) + (z0g ? 512u : 0u));
+                if (S0g) bulk_load(sm + L::S0F, S0g, 65536, bar_s0);
+                if (z0g) bulk_load(sm + L::ZIN, z0g, 512, bar_s0);
                 issue_v(0);
             }
             pdl_launch_dependents();
@@ -194,9 +210,9 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 umma_commit(bar_mma1);
                 if (sb + 1 < nsb)  // the next tile towards L2 while this one computes
                     for (int a = 0; a < 2; ++a) {
-                        tma_prefetch_3d(&tq, 64 * a, (sb + 1) * 128, g);
-                        tma_prefetch_3d(&tk, 64 * a, (sb + 1) * 128, g);
-                        tma_prefetch_3d(&tv, 64 * a, (sb + 1) * 128, g);
+                        tma_prefetch_3d(&tq, 64 * a, rbase + (sb + 1) * 128, g);
+                        tma_prefetch_3d(&tk, 64 * a, rbase + (sb + 1) * 128, g);
+                        tma_prefetch_3d(&tv, 64 * a, rbase + (sb + 1) * 128, g);
                     }
                 // the block's incoming state (first block: the carry-in; later: the previous EPI2)
                 ok = mbar_wait(bar_sst, par, ERR_TIMEOUT_MMA);
@@ -230,7 +246,7 @@ la_fwd_tc128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         for (int sb = 0; sb < nsb; ++sb) {
             const uint32_t par = sb & 1;
-            const int row0 = sb * 128;
+            const int row0 = rbase + sb * 128;
             const bool last = sb + 1 == nsb;
             // ---- masked score row -> bf16 A operand in TMEM (keys [64h, 64h+64) of row t land
             //      in columns [32h, 32h+32) of lane t, over scores already read); fp32 row sum

@@ -119,7 +119,7 @@ int la_bwd_max_c(int D, int block, la_dtype dtype);
 la_status la_device_status(int clear);
 
 /*
- * Chunk-parallel forward for few groups of long chunks (bf16, head size 64).
+ * Chunk-parallel forward for few groups of long chunks (bf16, head size 64 or 128).
  * The state after a run of tokens is the state before it plus the run's own sums
  * (section 2, "Opt 2", read run by run), so each group's chunk is cut into P pieces
  * that run on P CTAs: the pieces' sums of k v^T and k, an exclusive prefix over them
@@ -127,9 +127,10 @@ la_status la_device_status(int clear);
  * Results equal la_chunked_fwd's up to the order of the fp32 state sums.
  *
  * la_fwd_split_workspace_bytes: device workspace the call needs on the current device
- * (one 16,640-byte cell per piece); 0 when no split applies (other dtypes or head
- * sizes, C <= 128, or G already large enough to fill the GPU) -- then la_chunked_fwd_split
- * simply runs la_chunked_fwd and needs no workspace.
+ * (one cell of (D*D + D) floats per piece: 16,640 bytes at head size 64, 66,048 at 128);
+ * 0 when no split applies (fp32, C <= 128, or G already large enough to fill the GPU:
+ * two groups per SM at head size 64, one at 128) -- then la_chunked_fwd_split simply runs
+ * la_chunked_fwd and needs no workspace.
  *
  * la_chunked_fwd_split: arguments, layouts, in-place carries and errors as
  * la_chunked_fwd; workspace is caller-owned DEVICE memory, 256-byte aligned, at least
@@ -149,8 +150,10 @@ la_status la_chunked_fwd_split(const void* q, const void* k, const void* v,
  * la_chunked_fwd_split without a workspace argument, for callers that cannot allocate
  * device memory.  The page has no counterpart: it is this library's way of running the
  * chunk-parallel forward above from a fixed, module-level device array of 8 MiB (room for
- * 504 piece cells; a plan asking for more -- more than about 250 SMs' worth of pieces --
- * returns LA_ERR_UNSUPPORTED).  Arguments, results and errors otherwise as
+ * 504 piece cells at head size 64, 127 at 128: at head size 128 the plan is cut to at most
+ * 127 pieces in all, so its fp32 sums may be grouped differently from
+ * la_chunked_fwd_split's; at head size 64 a plan asking for more than 504 cells -- more
+ * than about 250 SMs' worth of pieces -- returns LA_ERR_UNSUPPORTED).  Arguments, results and errors otherwise as
  * la_chunked_fwd_split; with no split to make it runs la_chunked_fwd.
  *   - Every call on a device uses the same array: calls that may overlap in time (on
  *     different streams, or from different host threads) race and must be ordered by the

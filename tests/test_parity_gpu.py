@@ -279,12 +279,14 @@ def test_bounded_wait_gives_up_and_the_device_stays_usable():
     assert la.la_device_status() == 0
 
 
-@pytest.mark.parametrize("G,C", [(2, 4096), (8, 1000), (1, 300), (3, 2048)])
-def test_chunk_parallel_forward(G, C):
+@pytest.mark.parametrize("G,C,D", [(2, 4096, 64), (8, 1000, 64), (1, 300, 64), (3, 2048, 64),
+                                   (2, 4096, 128), (8, 1000, 128), (1, 300, 128), (1, 8192, 128), (3, 2000, 128)])
+def test_chunk_parallel_forward(G, C, D):
     """la_chunked_fwd_split (pieces on separate CTAs, carries from a prefix over the
     pieces' sums) matches the oracle, and the sequential kernel within the bf16 bounds."""
-    x = make_inputs(G, C, 64, dtype="bf16", seed=G * C, carry=True)
-    assert la.la_fwd_split_workspace_bytes(G, C, 64, la.LA_BF16) > 0
+    x = make_inputs(G, C, D, dtype="bf16", seed=G * C + D, carry=True)
+    ws = la.la_fwd_split_workspace_bytes(G, C, D, la.LA_BF16)
+    assert ws > 0 and ws % (4 * (D * D + D)) == 0 and ws // (4 * (D * D + D)) % G == 0
     d = x.to(DEV)
     got = la.chunked_fwd_split(d.q, d.k, d.v, d.S0, d.z0, block=64, eps=EPS)
     seq = la.chunked_fwd(d.q, d.k, d.v, d.S0, d.z0, block=64, eps=EPS)
@@ -305,12 +307,13 @@ def test_chunk_parallel_forward_falls_back_and_threads_carry_in_place():
     torch.cuda.synchronize()
     check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
     # a split with in-place carry: the scan reads S0 before the last piece writes S_out
-    x = make_inputs(2, 2000, 64, dtype="bf16", seed=6, carry=True)
-    d = x.to(DEV)
-    S, z = d.S0.clone(), d.z0.clone()
-    got = la.chunked_fwd_split(d.q, d.k, d.v, S, z, block=64, eps=EPS, S_out=S, z_out=z)
-    torch.cuda.synchronize()
-    check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
+    for D in (64, 128):
+        x = make_inputs(2, 2000, D, dtype="bf16", seed=6, carry=True)
+        d = x.to(DEV)
+        S, z = d.S0.clone(), d.z0.clone()
+        got = la.chunked_fwd_split(d.q, d.k, d.v, S, z, block=64, eps=EPS, S_out=S, z_out=z)
+        torch.cuda.synchronize()
+        check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
 
 
 @pytest.mark.parametrize("G,C", [(2, 4096), (8, 1000), (1, 300), (3, 2048), (1, 16384)])
