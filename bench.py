@@ -474,10 +474,10 @@ OTHER_CONFIGS = (
      "chunked"),
     ("cumsum_form_fwdbwd: G=160, C=128, D=64, bf16, token-by-token scan", 160, 128, 64, 64, ("fwd", "bwd"),
      "cumsum"),
-    ("few_groups_wide_heads_fwd: G=8, C=8192, D=128, bf16, one CTA per group", 8, 8192, 128, 64, ("fwd",),
-     "chunked"),
-    ("few_groups_wide_heads_split_fwd: G=8, C=8192, D=128, bf16, chunk-parallel (la_chunked_fwd_split)", 8, 8192,
-     128, 64, ("fwd",), "split"),
+    ("few_groups_wide_heads_fwdbwd: G=8, C=8192, D=128, bf16, one CTA per group", 8, 8192, 128, 64,
+     ("fwd", "bwd"), "chunked"),
+    ("few_groups_wide_heads_split_fwdbwd: G=8, C=8192, D=128, bf16, chunk-parallel (la_chunked_fwd_split, "
+     "la_chunked_bwd_split)", 8, 8192, 128, 64, ("fwd", "bwd"), "split"),
 )
 
 # The cumsum form runs on the CUDA cores: its bound is fp32 FMA issue, 128 FMA lanes per
@@ -523,8 +523,9 @@ def measure_other_configs(stream, eps, hbm):
             ws = None
             if impl == "cumsum" and "bwd" in dirs:
                 ws = torch.empty(la.la_cumsum_bwd_workspace_bytes(G, C, D, la.LA_BF16), dtype=torch.uint8, device=dev)
-            if impl == "split":
-                ws = torch.empty(max(1, la.la_fwd_split_workspace_bytes(G, C, D, la.LA_BF16)), dtype=torch.uint8,
+            if impl == "split":  # one workspace serves both directions (the calls are stream-ordered)
+                ws = torch.empty(max(1, la.la_fwd_split_workspace_bytes(G, C, D, la.LA_BF16),
+                                     la.la_bwd_split_workspace_bytes(G, C, D, la.LA_BF16)), dtype=torch.uint8,
                                  device=dev)
             if impl == "threaded":  # contiguous [G][128][D] pieces of q, k, v; o as 64 pieces
                 for key in ("q", "k", "v"):
@@ -541,9 +542,12 @@ def measure_other_configs(stream, eps, hbm):
                     for c, (qc, kc, vc, oc) in enumerate(zip(d["q"], d["k"], d["v"], o[0])):
                         S_in, z_in = (d["S0"], d["z0"]) if c == 0 else (o[1], o[2])
                         la.chunked_fwd(qc, kc, vc, S_in, z_in, block=block, eps=eps, o=oc, S_out=o[1], z_out=o[2])
-                elif impl == "split":
+                elif impl == "split" and direction == "fwd":
                     la.chunked_fwd_split(d["q"], d["k"], d["v"], d["S0"], d["z0"], block=block, eps=eps, o=o[0],
                                          S_out=o[1], z_out=o[2], workspace=ws)
+                elif impl == "split":
+                    la.chunked_bwd_split(d["q"], d["k"], d["v"], d["S0"], d["z0"], d["dO"], d["dS_out"], d["dz_out"],
+                                         block=block, eps=eps, out=gr, workspace=ws)
                 elif impl == "cumsum":
                     la.cumsum_bwd(d["q"], d["k"], d["v"], d["S0"], d["z0"], d["dO"], d["dS_out"], d["dz_out"],
                                   eps=eps, out=gr, workspace=ws)

@@ -204,7 +204,7 @@ def cumsum_bwd(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, eps: float = 1e
 
 def chunked_bwd_split(q, k, v, S0, z0, dO, dS_out=None, dz_out=None, *, block: int = 64, eps: float = 1e-6,
                       out: Optional[tuple] = None, workspace=None, stream=None):
-    """chunked_bwd cut along the tokens for few groups of long chunks (bf16, D = 64): the
+    """chunked_bwd cut along the tokens for few groups of long chunks (bf16, D = 64 or 128): the
     pieces of every group run on separate CTAs, between prefix sums over the pieces in
     token order (the forward carries) and in reverse (the carry gradients).  `workspace`
     (a CUDA tensor of at least la_bwd_split_workspace_bytes bytes) is allocated here when

@@ -450,7 +450,7 @@ bool split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan, bool backw
 {
     *plan = SplitPlan{};
     plan->PL = C;
-    if (dtype != LA_BF16 || (D != 64 && (D != 128 || backward)) || G <= 0 || C <= 128) return true;
+    if (dtype != LA_BF16 || (D != 64 && D != 128) || G <= 0 || C <= 128) return true;
     const int per_sm = backward || D == 128 ? 1 : 2, cells = backward ? 2 : 1;
     const int sms = sm_count();
     if (sms == 0) return false;
@@ -511,23 +511,34 @@ la_status fwd_split_launch(const void* q, const void* k, const void* v, const fl
 // The chunk-parallel backward: forward carries, pass 1 of every piece (dq, the parked
 // 1/den and dd, each piece's own reverse sums), their reverse prefix (and dS0, dz0), pass 2
 // of every piece (dk, dv).  ws holds the forward cells, then the reverse cells.
+template <int D>
 la_status bwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0,
                            const void* dO, const float* dS_out, const float* dz_out, void* dq, void* dk, void* dv,
                            float* dS0, float* dz0, int G, int C, float eps, const SplitPlan& plan, float* ws,
                            cudaStream_t stream)
 {
     float* fcell = ws;
-    float* rcell = ws + (size_t)G * plan.P * la::DeltaLayout::CELL;
-    la_status st = piece_carries(k, v, S0, z0, G, C, 64, plan, fcell, stream);
+    float* rcell = ws + (size_t)G * plan.P * (D * D + D);
+    la_status st = piece_carries(k, v, S0, z0, G, C, D, plan, fcell, stream);
     if (st != LA_OK) return st;
-    st = bwd_tcm_launch<64>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
-                            stream, plan.P, plan.PL, 1, fcell, rcell);
+    st = bwd_tcm_launch<D>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
+                           stream, plan.P, plan.PL, 1, fcell, rcell);
     if (st != LA_OK) return st;
-    st = launch_pdl(la::la_state_rscan_kernel, G * la::SCAN_BLOCKS, 256, 0, stream, dS_out, dz_out, rcell, dS0, dz0,
-                    plan.P);
+    if constexpr (D == 128) {  // the pieces' own sums of q dN^T (head size 64: formed by the pass-1 launch)
+        static OptIn qflag;
+        st = prepare(la::la_piece_qdn128_kernel, qflag, la::Qdn128Layout::BYTES);
+        if (st != LA_OK) return st;
+        CUtensorMap tq{}, tg{};
+        if (!tmap_bf16(&tq, q, G, C, 128, 128) || !tmap_bf16(&tg, dO, G, C, 128, 128)) return LA_ERR_CUDA;
+        st = launch_pdl(la::la_piece_qdn128_kernel, G * plan.P, la::Qdn128Layout::THREADS, la::Qdn128Layout::BYTES,
+                        stream, tq, tg, static_cast<const __nv_bfloat16*>(dk), C, plan.P, plan.PL, rcell);
+        if (st != LA_OK) return st;
+    }
+    st = launch_pdl(la::la_state_rscan_kernel<D>, G * la::scan_blocks(D), 256, 0, stream, dS_out, dz_out, rcell, dS0,
+                    dz0, plan.P);
     if (st != LA_OK) return st;
-    return bwd_tcm_launch<64>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
-                              stream, plan.P, plan.PL, 2, fcell, rcell);
+    return bwd_tcm_launch<D>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
+                             stream, plan.P, plan.PL, 2, fcell, rcell);
 }
 
 }  // namespace
@@ -678,8 +689,12 @@ extern "C" la_status la_chunked_bwd_split(const void* q, const void* k, const vo
                        {dz_out, n_z}, {dq, n_x},     {dk, n_x},  {dv, n_x},  {dS0, n_S}, {dz0, n_z}};
     for (const Buf& b : all)
         if (overlaps(wsb, b)) return LA_ERR_INVALID;
-    return bwd_split_launch(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, plan,
-                            static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
+    float* ws = static_cast<float*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return D == 64 ? bwd_split_launch<64>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, plan,
+                                          ws, s)
+                   : bwd_split_launch<128>(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, eps, plan,
+                                           ws, s);
 }
 
 // ---------------------------------------------------------------- cumsum form

@@ -34,12 +34,13 @@
 // except the first, which is the tile pass 1 ended with: pass 1 leaves Q, K, V and dN in
 // place (dq is staged over dA), so it is not loaded again.
 //
-// Piece mode (head size 64; the chunk-parallel backward): the grid has P CTAs per group,
-// CTA (g, p) owning tokens [p PL, (p+1) PL) of group g, and each launch runs ONE pass:
+// Piece mode (the chunk-parallel backward): the grid has P CTAs per group, CTA (g, p)
+// owning tokens [p PL, (p+1) PL) of group g, and each launch runs ONE pass:
 //   mode 1 runs pass 1 over the piece from its forward carry (S, z before the piece: a
 //          cell of D*D + D floats, S as [p][c] then z) and also sums the piece's own
-//          Q^T dN (a fourth TMEM accumulator) and Q^T dd, written to the piece's cell of
-//          `rcell` -- what pass 2 adds to R and r over the piece;
+//          Q^T dN (head size 64: a fourth TMEM accumulator; 128: la_piece_qdn128_kernel
+//          after this launch) and Q^T dd, written to the piece's cell of `rcell` -- what
+//          pass 2 adds to R and r over the piece;
 //   mode 2 runs pass 2 over the piece from its reverse carry (R, r after the piece, read
 //          from the same cell once a reverse scan has turned the sums into carries).
 // Between them the parked (1/den, dd) wait in dk as usual.  Mode 0 is the whole chunk,
@@ -719,10 +720,10 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (tid == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
             mbar_arrive(bar_e3);
         }
-        if constexpr (D == 64) {
-            if (mode == 1) {
-                // the piece's sums -> its cell: Q^T dN from TMEM (its last MMA completed before the
-                // last bar_m3), then Q^T dd
+        if (mode == 1) {
+            // the piece's sums -> its cell: Q^T dN from TMEM (its last MMA completed before the
+            // last bar_m3; at head size 128 a separate kernel forms it), then Q^T dd
+            if constexpr (D == 64) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + L::T_RL + hh * HC, r);
                 if (srow) {
@@ -732,8 +733,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                 }
-                if (tid < D) cellR[D * D + tid] = rzl[tid];
             }
+            if (tid < D) cellR[D * D + tid] = rzl[tid];
         }
     }
     if (tid == 0) tma_store_wait_read();  // shared memory stays valid until the stores have read it

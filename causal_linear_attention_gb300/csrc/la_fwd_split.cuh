@@ -326,10 +326,156 @@ la_state_delta128_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
+// The head-size-128 backward split's own sums of q dN^T per piece.  At head size 64 the
+// pass-1 launch forms them in a fourth TMEM accumulator; at 128 its 512 columns are taken, so
+// this kernel forms them after pass 1, from Q, dO and the 1/den that pass 1 parks in the first
+// 8 bytes of each token's dk row: dN = bf16(dO / den) row by row (the rounding pass 1 uses),
+// then sum_i q_i dN_i^T on the tensor core (M = p, N = c, K = i; both operands read
+// MN-major), into [0, D*D) of the piece's reverse cell.  (The sum of dd q, [D*D, D*D + D),
+// comes from pass 1.)
+struct Qdn128Layout {
+    static constexpr int D = 128;
+    static constexpr uint32_t ATOM = 16384;           // 128 rows x 64 bf16 columns
+    static constexpr uint32_t QT0 = 0, QT1 = 32768;   // Q tiles, two stages of two atoms
+    static constexpr uint32_t GT0 = 65536, GT1 = 98304;  // dO -> dN tiles
+    static constexpr uint32_t BARS = 131072;
+    static constexpr uint32_t END = 131200;
+    static constexpr uint32_t BYTES = END;
+    static constexpr uint32_t TMEM_COLS = 128;
+    static constexpr int THREADS = 160;
+    static constexpr uint32_t CELL = D * D + D;
+};
+
+__global__ void __launch_bounds__(160, 1)
+la_piece_qdn128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
+                       const __nv_bfloat16* dk, int C, int P, int PL, float* rcell)
+{
+    using L = Qdn128Layout;
+    using namespace tc;
+    constexpr int D = L::D;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    if (smem_addr(sm) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_status, ERR_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t sbase = smem_addr(sm);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* full = bars + 0;    // [2] Q, dO of a stage landed (TMA)
+    uint64_t* scaled = bars + 2;  // [2] every row of the stage's dO is now dN (128 epilogue threads)
+    uint64_t* empty = bars + 4;   // [2] the stage's MMAs are done (MMA commit)
+    uint64_t* done = bars + 6;    // every MMA of the piece is done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 64);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = (int)blockIdx.x / P, piece = (int)blockIdx.x % P;
+    const int rbase = piece * PL;
+    const int rend = min(C, rbase + PL);
+    const int nblk = (rend - rbase + 127) / 128;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(scaled + s, 128);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();  // pass 1 has parked 1/den in dk
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tg);
+            auto load = [&](int blk) {
+                const int s = blk & 1;
+                unsigned char* qt = sm + (s ? L::QT1 : L::QT0);
+                unsigned char* gt = sm + (s ? L::GT1 : L::GT0);
+                mbar_expect_tx(full + s, 4 * L::ATOM);
+                tma_load_3d(qt, &tq, full + s, 0, rbase + blk * 128, g);
+                tma_load_3d(qt + L::ATOM, &tq, full + s, 64, rbase + blk * 128, g);
+                tma_load_3d(gt, &tg, full + s, 0, rbase + blk * 128, g);
+                tma_load_3d(gt + L::ATOM, &tg, full + s, 64, rbase + blk * 128, g);
+            };
+            for (int blk = 0; blk < min(2, nblk); ++blk) load(blk);
+            pdl_launch_dependents();
+            const uint32_t id = idesc_bf16(128, 128, true, true);
+            bool ok = true;
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int s = blk & 1;
+                const uint32_t ph = (blk >> 1) & 1;
+                ok = mbar_wait(full + s, ph, ERR_TIMEOUT_TMA) && mbar_wait(scaled + s, ph, ERR_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                // MN-major operands of two 64-wide atoms (LBO = one atom), 16 rows per K = 16 step
+                const uint64_t dQ = smem_desc(sbase + (s ? L::QT1 : L::QT0), L::ATOM, 1024);
+                const uint64_t dG = smem_desc(sbase + (s ? L::GT1 : L::GT0), L::ATOM, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // sum += Q^T dN  (M = p, N = c, K = i)
+                    umma_bf16(tmem, dQ + kk * 128, dG + kk * 128, id, blk > 0 || kk > 0);
+                umma_commit(empty + s);
+                if (blk + 2 < nblk) {
+                    ok = mbar_wait(empty + s, ph, ERR_TIMEOUT_MMA);
+                    if (ok) load(blk + 2);
+                }
+            }
+            umma_commit(done);
+        }
+    } else {
+        // ---- row t of every tile: dO -> dN = dO / den in place (rows past the piece: zero)
+        const int t = tid;
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int s = blk & 1;
+            const int grow = rbase + blk * 128 + t;
+            const float inv =
+                grow < rend ? reinterpret_cast<const float2*>(dk + ((size_t)g * C + grow) * D)->x : 0.f;
+            mbar_wait(full + s, (blk >> 1) & 1, ERR_TIMEOUT_TMA);
+            unsigned char* gt = sm + (s ? L::GT1 : L::GT0);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                uint4* p4 = reinterpret_cast<uint4*>(gt + (uint32_t)(c >> 3) * L::ATOM + sw_chunk(t, c & 7));
+                uint4 u = *p4;
+                __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    h2[e] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                }
+                *p4 = u;
+            }
+            fence_async_smem();
+            mbar_arrive(scaled + s);
+        }
+        // ---- the sum: TMEM lane p holds row p of sum_i q_i dN_i^T ([p][c], as the cell wants)
+        mbar_wait(done, 0, ERR_TIMEOUT_MMA);
+        tc_fence_after();
+        float4* cell = reinterpret_cast<float4*>(rcell + (size_t)blockIdx.x * L::CELL + (size_t)t * D);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[64];
+            tmem_ld32x64(tmem + ((uint32_t)(32 * warp) << 16) + 64 * h, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                cell[16 * h + j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
 // Exclusive prefix over each group's pieces, in place: piece p's cell becomes the state
 // before it (S0 plus the sums of pieces 0..p-1).  scan_blocks(D) blocks of 256 threads per
 // group, one element of the cell per thread.
-constexpr int SCAN_BLOCKS = (DeltaLayout::CELL + 255) / 256;
 __host__ __device__ constexpr int scan_blocks(int D) { return (D * D + D + 255) / 256; }
 
 template <int D>
@@ -356,15 +502,16 @@ la_state_scan_kernel(const float* S0, const float* z0, float* delta, int P)
 // dS_out (dz_out) plus the sums of pieces p+1 .. P-1; the total over all pieces is the
 // gradient of the incoming carry, written to dS0 (dz0).  dS0 may be dS_out (dz0 dz_out):
 // each element is read and then written by the same thread.  NULL dS_out / dz_out = zero;
-// NULL dS0 / dz0 are skipped.  Launch as la_state_scan_kernel.
+// NULL dS0 / dz0 are skipped.  Launch as la_state_scan_kernel<D>.
+template <int D>
 __global__ void __launch_bounds__(256)
 la_state_rscan_kernel(const float* dS_out, const float* dz_out, float* delta, float* dS0, float* dz0, int P)
 {
-    constexpr int D = DeltaLayout::D;
-    constexpr uint32_t CELL = DeltaLayout::CELL;
+    constexpr uint32_t CELL = D * D + D;
+    constexpr int NB = scan_blocks(D);
     pdl_wait();
-    const int e = ((int)blockIdx.x % SCAN_BLOCKS) * 256 + threadIdx.x;
-    const size_t g = blockIdx.x / SCAN_BLOCKS;
+    const int e = ((int)blockIdx.x % NB) * 256 + threadIdx.x;
+    const size_t g = blockIdx.x / NB;
     if (e >= (int)CELL) return;
     const bool is_S = e < D * D;
     float run = is_S ? (dS_out ? dS_out[g * D * D + e] : 0.f) : (dz_out ? dz_out[g * D + (e - D * D)] : 0.f);

@@ -171,7 +171,7 @@ la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* 
                                       void* stream);
 
 /*
- * Chunk-parallel backward for few groups of long chunks (bf16, head size 64): the
+ * Chunk-parallel backward for few groups of long chunks (bf16, head size 64 or 128): the
  * reverse cumsum of section 1 cut into pieces like la_chunked_fwd_split's forward.
  * Every piece's forward carry comes from the pieces' sums and their exclusive prefix; a
  * first pass over every piece (token order) writes dq and each piece's own sums of
@@ -181,15 +181,16 @@ la_status la_chunked_fwd_split_static(const void* q, const void* k, const void* 
  * the order of the fp32 sums.
  *
  * la_bwd_split_workspace_bytes: device workspace the call needs on the current device
- * (two 16,640-byte cells per piece); 0 when no split applies (other dtypes or head sizes,
- * C <= 128, or G already large enough to fill the GPU at one group per SM) -- then
+ * (two cells of (D*D + D) floats per piece); 0 when no split applies (fp32, C <= 128, or
+ * G already large enough to fill the GPU at one group per SM) -- then
  * la_chunked_bwd_split simply runs la_chunked_bwd and needs no workspace.
  *
  * la_chunked_bwd_split: arguments, layouts, in-place carry gradients and errors as
  * la_chunked_bwd; workspace is caller-owned DEVICE memory, 256-byte aligned, at least
  * la_bwd_split_workspace_bytes(G, C, D, dtype) bytes, disjoint from every tensor and not
  * used by anything else until the stream has completed (LA_ERR_INVALID otherwise).  The
- * library allocates nothing.  Five kernels are enqueued on `stream`.
+ * library allocates nothing.  Five kernels are enqueued on `stream` (six at head size 128,
+ * where the pieces' own sums of q dN^T take a kernel of their own).
  */
 size_t la_bwd_split_workspace_bytes(int G, int C, int D, la_dtype dtype);
 

@@ -316,13 +316,15 @@ def test_chunk_parallel_forward_falls_back_and_threads_carry_in_place():
         check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
 
 
-@pytest.mark.parametrize("G,C", [(2, 4096), (8, 1000), (1, 300), (3, 2048), (1, 16384)])
-def test_chunk_parallel_backward(G, C):
+@pytest.mark.parametrize("G,C,D", [(2, 4096, 64), (8, 1000, 64), (1, 300, 64), (3, 2048, 64), (1, 16384, 64),
+                                   (2, 4096, 128), (8, 1000, 128), (1, 300, 128), (3, 2000, 128), (1, 8192, 128)])
+def test_chunk_parallel_backward(G, C, D):
     """la_chunked_bwd_split (forward carries from a prefix over the pieces, carry gradients
     from a reverse prefix) matches the oracle, and the sequential kernel within the bf16
     bounds."""
-    x = make_inputs(G, C, 64, dtype="bf16", seed=G * C + 1, carry=True, grads=True)
-    assert la.la_bwd_split_workspace_bytes(G, C, 64, la.LA_BF16) > 0
+    x = make_inputs(G, C, D, dtype="bf16", seed=G * C + 1 + D, carry=True, grads=True)
+    ws = la.la_bwd_split_workspace_bytes(G, C, D, la.LA_BF16)
+    assert ws > 0 and ws % (8 * (D * D + D)) == 0
     d = x.to(DEV)
     got = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
     seq = la.chunked_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
@@ -334,9 +336,10 @@ def test_chunk_parallel_backward(G, C):
         assert max_rel(a, b.cpu().double().numpy()) < (2e-2 if n in ("dq", "dk", "dv") else 1e-4), n
 
 
-def test_chunk_parallel_backward_carry_cases():
+@pytest.mark.parametrize("D", [64, 128])
+def test_chunk_parallel_backward_carry_cases(D):
     # no upstream carry gradient, no carry
-    x = make_inputs(2, 1500, 64, dtype="bf16", seed=31, carry=False, grads=True)
+    x = make_inputs(2, 1500, D, dtype="bf16", seed=31, carry=False, grads=True)
     x.dS_out = x.dz_out = None
     d = x.to(DEV)
     got = la.chunked_bwd_split(d.q, d.k, d.v, None, None, d.dO, None, None, block=64, eps=EPS)
@@ -344,7 +347,7 @@ def test_chunk_parallel_backward_carry_cases():
     check(got, oracle.bwd(x.q, x.k, x.v, None, None, x.dO, None, None, eps=EPS), "bf16", BWD_NAMES)
     # in place: dS0 over dS_out and dz0 over dz_out (the reverse scan reads each element
     # before it writes it)
-    x = make_inputs(2, 2000, 64, dtype="bf16", seed=32, carry=True, grads=True)
+    x = make_inputs(2, 2000, D, dtype="bf16", seed=32, carry=True, grads=True)
     d = x.to(DEV)
     dS, dz = d.dS_out.clone(), d.dz_out.clone()
     out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), dS, dz)
