@@ -802,9 +802,14 @@ namespace {
 
 constexpr size_t kCeAlign = 256;
 constexpr int kGemmMaxSplit = 8;  // vocabulary ranges of the dh GEMM (its fp32 slices live in the workspace)
-// The share of the GEMM kernel's CTA pairs that dh gets beside dW: measured best at chunks of
-// 512 and of 128 tokens among 0.3 - 0.5 and against a split by estimated cost.
+// The share of the GEMM kernel's CTA pairs that dh gets beside dW when dW is stored (one
+// chunk): measured best at one chunk of 512 tokens among 0.3 - 0.5 and against a split by
+// estimated cost.
 constexpr double kDhShare = 0.4;
+// The same when dW adds into itself (chunks after the first): its read-modify-write of the
+// fp32 output makes it the longer side, so dh gets fewer pairs (best of 0.18 - 0.4 at chunks
+// of 128 tokens).
+constexpr double kDhShareReduce = 0.32;
 
 size_t ce_round(size_t n) { return (n + kCeAlign - 1) / kCeAlign * kCeAlign; }
 
@@ -1116,7 +1121,7 @@ extern "C" la_status la_ce_bwd(const void* h, const void* W, const int* targets,
     if (pairs < 2) return LA_ERR_UNSUPPORTED;
     const int kbv = (V + la::GemmLayout::BK - 1) / la::GemmLayout::BK;
     const int ntot_dh = ((cs + la::GemmLayout::PM - 1) / la::GemmLayout::PM) * ((d + la::GemmLayout::BN - 1) / la::GemmLayout::BN);
-    const int dh_target = std::max(1, (int)(kDhShare * pairs + 0.5));
+    const int dh_target = std::max(1, (int)((N > cc ? kDhShareReduce : kDhShare) * pairs + 0.5));
     int nsplit = std::max(1, std::min(kGemmMaxSplit, std::min(kbv, (dh_target + ntot_dh / 2) / ntot_dh)));
     const int kbs = (kbv + nsplit - 1) / nsplit;
     nsplit = (kbv + kbs - 1) / kbs;
