@@ -406,6 +406,7 @@ def run_ours(args, rank, world, local):
     out = None
     if rank == 0:
         cpu = cpu_baseline(host, G, C, D, eps)
+        cpu_torch = cpu_torch_fp32(host, G, C, D, block, eps)
         out = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
@@ -416,7 +417,7 @@ def run_ours(args, rank, world, local):
                              f"{l2 / 2**20:.0f} MiB)", "timing": "CUDA graphs, CUDA events, max over ranks"},
             "fwd_only": {"value": fwd_only, "unit": UNIT, "us_per_launch": kernels["la_fwd"]["avg_us"]},
             "roofline": roof, "kernels": kernels, "e2e": e2e, "gpu_launches": 2 * args.steps,
-            "clocks": clock_info, "cpu_baseline": cpu, "other_configs": others,
+            "clocks": clock_info, "cpu_baseline": cpu, "cpu_torch_fp32": cpu_torch, "other_configs": others,
         }
     if world > 1:
         import torch.distributed as dist
@@ -691,6 +692,38 @@ def cpu_baseline(host, G, C, D, eps, budget_s=10.0):
     return {"value": G * C * reps / el, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
             "cpu": cpu_model(),
             "sample": f"{reps} x full fwd+bwd of the workload (G={G}, C={C}, D={D}) in fp64, {el:.1f} s"}
+
+
+def cpu_torch_fp32(host, G, C, D, block, eps, reps=5):
+    """The page's chunked form as plain PyTorch CPU ops in fp32 (oracle/torch_chunked.py; the
+    backward by autograd), the way the page's own CPU micro-benchmark runs it: median of
+    `reps` runs of the forward and of forward + backward on the same workload."""
+    import statistics
+
+    import torch
+
+    from oracle import torch_chunked
+    x = [None if t is None else t.float() for t in (host.q, host.k, host.v, host.S0, host.z0, host.dO,
+                                                     host.dS_out, host.dz_out)]
+    res = {}
+    for name, fn in (("fwd", lambda: torch_chunked.chunked_fwd(*x[:5], block=block, eps=eps)),
+                     ("fwdbwd", lambda: torch_chunked.chunked_fwd_bwd(*x, block=block, eps=eps))):
+        with torch.no_grad() if name == "fwd" else torch.enable_grad():
+            fn()
+            times = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                fn()
+                times.append(time.perf_counter() - t0)
+        ms = statistics.median(times) * 1e3
+        res[name] = {"value": G * C / (ms / 1e3), "unit": UNIT, "ms": round(ms, 2)}
+    res.update({"kind": "torch-CPU fp32 restatement of the chunked form (oracle/torch_chunked.py), autograd backward",
+                "threads": torch.get_num_threads(), "cpu": cpu_model(), "torch": torch.__version__,
+                "sample": f"median of {reps} runs of the workload (G={G}, C={C}, D={D}, block {block})",
+                "page_cpu_table": {"fwd_ms": 23.0, "fwdbwd_ms": 72.4,
+                                   "note": "the page's chunked CPU micro-benchmark at G = 160 (torch on a CPU "
+                                           "of unstated model and core count): context, not a target"}})
+    return res
 
 
 def run_reference(args, rank, world):

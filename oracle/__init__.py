@@ -28,6 +28,9 @@ z: [G, D]; ``None`` carries / upstream carry grads mean zeros):
 * ``fwd_chunked``    the page's chunked form with a block size (C).
 * ``bwd_chunked``    the chunked backward (forward sweep + reverse sweep) (C).
 * ``fwd_einsum``     the page's masked-einsum form, O(C^2 D^2) memory; tiny inputs.
+* ``torch_chunked``  (submodule) the chunked form as PyTorch CPU ops, fp32 or fp64, the backward
+                   by autograd: the bench's like-for-like CPU number (the page times its own
+                   chunked form this way).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (hand-derived golden values, closed forms, invariants, finite differences and
