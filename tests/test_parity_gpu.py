@@ -297,6 +297,24 @@ def test_chunk_parallel_forward(G, C, D):
         assert max_rel(a, b.cpu().double().numpy()) < (2e-2 if n == "o" else 1e-5), n
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("C", [129, 257, 1025])
+def test_chunk_parallel_one_token_past_a_tile(D, C):
+    """Chunks one token past a tile boundary: the last piece of each group holds a single
+    token (forward and backward split, one group and three)."""
+    for G in (1, 3):
+        x = make_inputs(G, C, D, dtype="bf16", seed=C + D + G, carry=True, grads=True)
+        assert la.la_fwd_split_workspace_bytes(G, C, D, la.LA_BF16) > 0
+        assert la.la_bwd_split_workspace_bytes(G, C, D, la.LA_BF16) > 0
+        d = x.to(DEV)
+        fwd = la.chunked_fwd_split(d.q, d.k, d.v, d.S0, d.z0, block=64, eps=EPS)
+        bwd = la.chunked_bwd_split(d.q, d.k, d.v, d.S0, d.z0, d.dO, d.dS_out, d.dz_out, block=64, eps=EPS)
+        torch.cuda.synchronize()
+        assert la.la_device_status() == 0
+        check(fwd, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
+        check(bwd, oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS), "bf16", BWD_NAMES)
+
+
 def test_chunk_parallel_forward_falls_back_and_threads_carry_in_place():
     # many groups: no split, no workspace needed; in-place carry threading still works
     x = make_inputs(300, 256, 64, dtype="bf16", seed=5, carry=True)
