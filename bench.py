@@ -42,8 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 # L2 when it ends (they are written back to DRAM later), so the write counter of one launch
 # reads ~0: the line carries both counters and says so.
 NCU_TRAFFIC = {
-    "la_fwd": {"read": 10562688, "write": 0, "l2_write": 7968320, "src": "ddc22d99b01eae4d"},
-    "la_bwd": {"read": 15875968, "write": 0, "l2_write": 15808256, "src": "d1c27f29834ec188"},
+    "la_fwd": {"read": 10562560, "write": 0, "l2_write": 7974080, "src": "bb92639dca406800"},
+    "la_bwd": {"read": 15877760, "write": 0, "l2_write": 15799488, "src": "82c52753b6c829a2"},
 }
 
 
