@@ -49,7 +49,7 @@ struct GemmLayout {
     static constexpr int STAGES = 5;
     static constexpr uint32_t OSTAGE = STAGES * STAGE_BYTES;        // output staging: NBOX boxes per epilogue warp
     static constexpr uint32_t WBOX = 32 * 32 * 4;                   // 32 rows x 32 fp32
-    static constexpr int NBOX = 4;  // (the output stream binds dW: 4 boxes in flight per warp beat 2, a 6th stage did not)
+    static constexpr int NBOX = 4;  // (dW's output stream binds: 4 boxes per warp with 5 stages beat 2 with 6)
     static constexpr uint32_t BARS = OSTAGE + 4 * NBOX * WBOX;
     static constexpr uint32_t BYTES = BARS + 256;
     static constexpr uint32_t ACC_COLS = 256;                       // accumulator a at TMEM column 256 a
