@@ -74,6 +74,12 @@ def test_fractus1b_block_forward():
     fwd_case(160, 128, 64, 64, "bf16")
 
 
+def test_fractus1b_block_backward():
+    """The bench step's backward at its own size and on its own inputs (rank 0's seed):
+    G=160, C=128, D=64, block=64, bf16."""
+    bwd_case(160, 128, 64, 64, "bf16", seed=1000)
+
+
 def test_fractus1b_forward_backward_b16():
     """B=16 -> G=640, C=128, D=64, block=64, bf16 forward + backward."""
     fwd_case(640, 128, 64, 64, "bf16", seed=2)
