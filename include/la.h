@@ -246,7 +246,9 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
  * Everything runs on this library's tensor-core kernels: the logits of a chunk with the
  * log-sum-exp (forward) or the softmax gradient G = (softmax - one-hot) dloss / N
  * (backward) taken straight from the accumulator, so the logits never reach memory; then
- * dh = G W and dW = G^T h on its persistent GEMM.  d must be a multiple of 64
+ * dh = G W and dW = G^T h in one launch of its persistent GEMM, which runs on CTA pairs
+ * (clusters of two CTAs sharing each tcgen05 MMA; the backward returns LA_ERR_UNSUPPORTED
+ * on a device that cannot hold two such pairs at once).  d must be a multiple of 64
  * (LA_ERR_UNSUPPORTED otherwise).
  *
  * la_ce_workspace_bytes: the device workspace both calls need: the chunk's bf16 gradient,
@@ -267,7 +269,8 @@ la_status la_cumsum_bwd(const void* q, const void* k, const void* v,
  * disjoint from every tensor; outputs disjoint from inputs (LA_ERR_INVALID otherwise).
  * N = 0 writes loss = 0 (forward) or dW = 0 (backward).  A target outside [0, V) gives its
  * row a NaN loss and makes la_device_status report LA_ERR_DEVICE.  Asynchronous on
- * `stream`; the library allocates nothing and keeps no state between calls.
+ * `stream`; the library allocates nothing and keeps no state between calls (beyond
+ * per-device facts it looks up once: the SM count, how many CTA pairs fit).
  */
 size_t la_ce_workspace_bytes(int N, int V, int d, int ce_chunk);
 
