@@ -476,6 +476,7 @@ bool bwd_split_plan(int G, int C, int D, la_dtype dtype, SplitPlan* plan)
 la_status piece_carries(const void* k, const void* v, const float* S0, const float* z0, int G, int C, int D,
                         const SplitPlan& plan, float* ws, cudaStream_t stream)
 {
+    if (plan.P > 32 * la::SCAN_MAXW) return LA_ERR_UNSUPPORTED;  // (plans stay near two pieces per SM)
     CUtensorMap tk{}, tv{};
     if (!tmap_bf16(&tk, k, G, C, D, 128) || !tmap_bf16(&tv, v, G, C, D, 128)) return LA_ERR_CUDA;
     la_status st;
@@ -486,7 +487,8 @@ la_status piece_carries(const void* k, const void* v, const float* S0, const flo
             st = launch_pdl(la::la_state_delta_kernel, G * plan.P, la::DeltaLayout::THREADS, la::DeltaLayout::BYTES,
                             stream, tk, tv, C, plan.P, plan.PL, ws);
         if (st != LA_OK) return st;
-        return launch_pdl(la::la_state_scan_kernel<64>, G * la::scan_blocks(64), 256, 0, stream, S0, z0, ws, plan.P);
+        return launch_pdl(la::la_state_scan_kernel<64, false>, G * la::scan_blocks(64), 32 * la::scan_warps(plan.P), 0,
+                          stream, S0, z0, ws, nullptr, nullptr, plan.P);
     }
     static OptIn dflag128;
     st = prepare(la::la_state_delta128_kernel, dflag128, la::Delta128Layout::BYTES);
@@ -494,7 +496,8 @@ la_status piece_carries(const void* k, const void* v, const float* S0, const flo
         st = launch_pdl(la::la_state_delta128_kernel, G * plan.P, la::Delta128Layout::THREADS,
                         la::Delta128Layout::BYTES, stream, tk, tv, C, plan.P, plan.PL, ws);
     if (st != LA_OK) return st;
-    return launch_pdl(la::la_state_scan_kernel<128>, G * la::scan_blocks(128), 256, 0, stream, S0, z0, ws, plan.P);
+    return launch_pdl(la::la_state_scan_kernel<128, false>, G * la::scan_blocks(128), 32 * la::scan_warps(plan.P), 0,
+                      stream, S0, z0, ws, nullptr, nullptr, plan.P);
 }
 
 la_status fwd_split_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
@@ -534,8 +537,8 @@ la_status bwd_split_launch(const void* q, const void* k, const void* v, const fl
                         stream, tq, tg, static_cast<const __nv_bfloat16*>(dk), C, plan.P, plan.PL, rcell);
         if (st != LA_OK) return st;
     }
-    st = launch_pdl(la::la_state_rscan_kernel<D>, G * la::scan_blocks(D), 256, 0, stream, dS_out, dz_out, rcell, dS0,
-                    dz0, plan.P);
+    st = launch_pdl(la::la_state_scan_kernel<D, true>, G * la::scan_blocks(D), 32 * la::scan_warps(plan.P), 0, stream,
+                    dS_out, dz_out, rcell, dS0, dz0, plan.P);
     if (st != LA_OK) return st;
     return bwd_tcm_launch<D>(q, k, v, nullptr, nullptr, dO, nullptr, nullptr, dq, dk, dv, nullptr, nullptr, G, C, eps,
                              stream, plan.P, plan.PL, 2, fcell, rcell);

@@ -13,13 +13,13 @@
 //
 // The per-piece sums live in a caller-provided device workspace: for piece p of group g,
 // the D x D fp32 sum [p][c] followed by the D fp32 key sums (4160 floats at D = 64, 16512
-// at D = 128).  The forward runs at head size 64 and 128; the backward at 64.
+// at D = 128).  Both directions run at head size 64 and 128.
 //
 // The backward runs the same way in reverse ("the derivative of a cumsum is a reverse
 // cumsum", section 1): with every piece's forward carry known, the pass-1 launch of the
 // multi-tile backward (la_bwd_tcm_kernel, mode 1) also leaves each piece's own sums of
 // q dN^T and dd q in a second set of cells; a reverse exclusive prefix
-// (la_state_rscan_kernel) turns them into the gradient reaching each piece's end, and the
+// (la_state_scan_kernel in reverse) turns them into the gradient reaching each piece's end, and the
 // pass-2 launch (mode 2) finishes every piece from there.
 #pragma once
 #include <cuda_bf16.h>
@@ -473,68 +473,69 @@ la_piece_qdn128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
-// Exclusive prefix over each group's pieces, in place: piece p's cell becomes the state
-// before it (S0 plus the sums of pieces 0..p-1).  scan_blocks(D) blocks of 256 threads per
-// group, one element of the cell per thread.
-__host__ __device__ constexpr int scan_blocks(int D) { return (D * D + D + 255) / 256; }
-constexpr int SCAN_U = 8;  // pieces a reverse-scan thread loads at once
+// Exclusive prefix over each group's pieces, in place.  Forward (REV false): piece p's cell
+// becomes the state before it, S0 (z0) plus the sums of pieces 0 .. p-1.  Reverse (REV
+// true): piece p's cell (its own sums of q dN^T [p][c] and of dd q) becomes the gradient
+// reaching the state after it, dS_out (dz_out) plus the sums of pieces p+1 .. P-1, and the
+// total over all pieces, the gradient of the incoming carry, goes to dS0 (dz0).  NULL
+// init pointers mean zero; NULL outputs are skipped.
+// Two levels, so that no thread walks the pieces one dependent load after another: block b
+// of group g covers 32 cell elements (lane), its warp w the pieces at positions
+// [32 w, 32 w + 32) of the scan order (REV: counted from the last piece), all loaded at once
+// (each warp load a coalesced row of one cell); the warps' totals meet in shared memory and
+// each warp writes its pieces' prefixes starting from the initial value plus the totals of
+// the warps before it, in warp order: a fixed order, the same bits every run.  Every thread
+// reads its initial value before the block's barrier, so dS0 may be dS_out (z likewise).
+// Launch: G * scan_blocks(D) blocks of 32 * scan_warps(P) threads; P <= 32 * SCAN_MAXW.
+constexpr int SCAN_MAXW = 32;
+__host__ __device__ constexpr int scan_blocks(int D) { return (D * D + D + 31) / 32; }
+inline int scan_warps(int P) { return (P + 31) / 32; }
 
-template <int D>
-__global__ void __launch_bounds__(256)
-la_state_scan_kernel(const float* S0, const float* z0, float* delta, int P)
+template <int D, bool REV>
+__global__ void __launch_bounds__(1024)
+la_state_scan_kernel(const float* init_S, const float* init_z, float* delta, float* out_S, float* out_z, int P)
 {
     constexpr uint32_t CELL = D * D + D;
     constexpr int NB = scan_blocks(D);
+    __shared__ float tot[SCAN_MAXW][32];
     pdl_wait();
-    const int e = ((int)blockIdx.x % NB) * 256 + threadIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int e = ((int)blockIdx.x % NB) * 32 + lane;
     const size_t g = blockIdx.x / NB;
-    if (e >= (int)CELL) return;
-    float run = e < D * D ? (S0 ? S0[g * D * D + e] : 0.f) : (z0 ? z0[g * D + (e - D * D)] : 0.f);
-    float* cell = delta + g * P * CELL + e;
-    for (int p = 0; p < P; ++p, cell += CELL) {
-        const float d = *cell;
-        *cell = run;
-        run += d;
+    const bool live = e < (int)CELL, is_S = e < D * D;
+    float run = 0.f;
+    if (live) {
+        if (is_S)
+            run = init_S ? init_S[g * D * D + e] : 0.f;
+        else
+            run = init_z ? init_z[g * D + (e - D * D)] : 0.f;
     }
-}
-
-// Reverse exclusive prefix over each group's pieces, in place: piece p's cell (its own sums
-// of q dN^T [p][c] and of dd q) becomes the gradient reaching the state after the piece,
-// dS_out (dz_out) plus the sums of pieces p+1 .. P-1; the total over all pieces is the
-// gradient of the incoming carry, written to dS0 (dz0).  dS0 may be dS_out (dz0 dz_out):
-// each element is read and then written by the same thread.  NULL dS_out / dz_out = zero;
-// NULL dS0 / dz0 are skipped.  Launch as la_state_scan_kernel<D>.
-template <int D>
-__global__ void __launch_bounds__(256)
-la_state_rscan_kernel(const float* dS_out, const float* dz_out, float* delta, float* dS0, float* dz0, int P)
-{
-    constexpr uint32_t CELL = D * D + D;
-    constexpr int NB = scan_blocks(D);
-    pdl_wait();
-    const int e = ((int)blockIdx.x % NB) * 256 + threadIdx.x;
-    const size_t g = blockIdx.x / NB;
-    if (e >= (int)CELL) return;
-    const bool is_S = e < D * D;
-    float run = is_S ? (dS_out ? dS_out[g * D * D + e] : 0.f) : (dz_out ? dz_out[g * D + (e - D * D)] : 0.f);
-    float* cells = delta + g * P * CELL + e;
-    // from the last piece, SCAN_U pieces' loads in flight at once (one load, store and add
-    // per piece in a dependent chain took 4-18 % of the split backward; the forward scan's
-    // plain loop is already as fast as this, measured)
-    for (int p0 = 0; p0 < P; p0 += SCAN_U) {
-        float d[SCAN_U];
+    // The warp's first piece in scan order, and a constant step to the next one.
+    constexpr long STEP = REV ? -(long)CELL : (long)CELL;
+    const int q0 = 32 * w, n = live ? min(32, P - q0) : 0;
+    float* cell = delta + g * P * CELL + (size_t)(REV ? P - 1 - q0 : q0) * CELL + e;
+    float d[32];
+    float t = 0.f;
 #pragma unroll
-        for (int u = 0; u < SCAN_U; ++u) d[u] = p0 + u < P ? cells[(size_t)(P - 1 - p0 - u) * CELL] : 0.f;
+    for (int u = 0; u < 32; ++u) d[u] = u < n ? cell[u * STEP] : 0.f;
 #pragma unroll
-        for (int u = 0; u < SCAN_U; ++u)
-            if (p0 + u < P) {
-                cells[(size_t)(P - 1 - p0 - u) * CELL] = run;
-                run += d[u];
-            }
+    for (int u = 0; u < 32; ++u) t += d[u];
+    tot[w][lane] = t;
+    __syncthreads();
+    for (int c = 0; c < w; ++c) run += tot[c][lane];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+        if (u < n) {
+            cell[u * STEP] = run;
+            run += d[u];
+        }
     }
-    if (is_S) {
-        if (dS0) dS0[g * D * D + e] = run;
-    } else if (dz0) {
-        dz0[g * D + (e - D * D)] = run;
+    if (REV && live && w == nw - 1) {  // the last warp ends with the initial value plus every piece
+        if (is_S) {
+            if (out_S) out_S[g * D * D + e] = run;
+        } else if (out_z) {
+            out_z[g * D + (e - D * D)] = run;
+        }
     }
 }
 
