@@ -33,6 +33,7 @@
 #include <stdint.h>
 
 #include "la_device.cuh"
+#include "la_tc.cuh"
 
 namespace la {
 
@@ -83,30 +84,82 @@ template <> struct Elem<__nv_bfloat16> {
     }
 };
 
-// Rows t0 .. t0 + nt - 1 of one group's [C][D] tensor -> dst[TB][D] fp32, row i times
-// scale[i] when `scale` is given; rows nt .. ntp - 1 are zero (all threads of the CTA).
+// One thread's share of a staged block: elements [E tid, E tid + E) of the TB x D values
+// of rows t0 .. t0 + TB - 1 (contiguous in the group's [C][D] tensor), held as loaded, so
+// that a load issued for the next block passes under the current block's work.
 template <int D, typename T>
-__device__ __forceinline__ void cs_stage(float* dst, const T* src, int t0, int nt, int ntp, const float* scale)
+struct CsShare {
+    static constexpr int E = CumsumCfg<D>::TB * D / CumsumCfg<D>::THREADS;  // 8 at D = 64, 2 at D = 128
+    static constexpr int WORDS = E * (int)sizeof(T) / 4;
+    static_assert(E * CumsumCfg<D>::THREADS == CumsumCfg<D>::TB * D && D % E == 0, "whole rows per block");
+    uint32_t w[WORDS];
+};
+
+// Issue the loads of this thread's share of rows t0 .. t0 + nt - 1; elements of rows >= nt
+// are zero.  The row of this thread's elements is E tid / D.
+template <int D, typename T>
+__device__ __forceinline__ void cs_fetch(CsShare<D, T>& r, const T* src, int t0, int nt)
 {
-    constexpr int PER_ROW = D / 8;
-    for (int i = threadIdx.x; i < ntp * PER_ROW; i += CumsumCfg<D>::THREADS) {
-        const int row = i / PER_ROW, c8 = i % PER_ROW;
-        float f[8];
-        if (row < nt) {
-            Elem<T>::load8(src + (size_t)(t0 + row) * D + 8 * c8, f);
-            if (scale) {
-                const float sc = scale[row];
+    using Sh = CsShare<D, T>;
+    const int i = Sh::E * (int)threadIdx.x;
+    const bool in = i < nt * D;
+    const T* p = src + (size_t)t0 * D + i;
+    if constexpr (Sh::WORDS % 4 == 0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] *= sc;
-            }
-        } else {  // padding (its scale slot is never read)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        for (int n = 0; n < Sh::WORDS / 4; ++n) {
+            const uint4 u = in ? reinterpret_cast<const uint4*>(p)[n] : make_uint4(0u, 0u, 0u, 0u);
+            r.w[4 * n] = u.x;
+            r.w[4 * n + 1] = u.y;
+            r.w[4 * n + 2] = u.z;
+            r.w[4 * n + 3] = u.w;
         }
-        float4* d4 = reinterpret_cast<float4*>(dst + row * D + 8 * c8);
-        d4[0] = make_float4(f[0], f[1], f[2], f[3]);
-        d4[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else if constexpr (Sh::WORDS == 2) {
+        const uint2 u = in ? *reinterpret_cast<const uint2*>(p) : make_uint2(0u, 0u);
+        r.w[0] = u.x;
+        r.w[1] = u.y;
+    } else {
+        static_assert(Sh::WORDS == 1, "share sizes");
+        r.w[0] = in ? *reinterpret_cast<const uint32_t*>(p) : 0u;
     }
+}
+
+// This thread's share -> dst[TB][D] fp32, times `scale` (bf16 is the upper half of an fp32
+// word, so widening is a shift).
+template <int D, typename T>
+__device__ __forceinline__ void cs_put(float* dst, const CsShare<D, T>& r, float scale)
+{
+    using Sh = CsShare<D, T>;
+    float f[Sh::E];
+#pragma unroll
+    for (int n = 0; n < Sh::WORDS; ++n) {
+        if constexpr (sizeof(T) == 4) {
+            f[n] = __uint_as_float(r.w[n]) * scale;
+        } else {
+            f[2 * n] = __uint_as_float(r.w[n] << 16) * scale;
+            f[2 * n + 1] = __uint_as_float(r.w[n] & 0xffff0000u) * scale;
+        }
+    }
+    float* d = dst + Sh::E * threadIdx.x;
+    if constexpr (Sh::E == 8) {
+        reinterpret_cast<float4*>(d)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(d)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+        static_assert(Sh::E == 2, "share sizes");
+        *reinterpret_cast<float2*>(d) = make_float2(f[0], f[1]);
+    }
+}
+
+// The row of a block this thread's share lies in.
+template <int D, typename T>
+__device__ __forceinline__ int cs_row() { return CsShare<D, T>::E * (int)threadIdx.x / D; }
+
+// Start the first rows of a group's tensor towards L2 (before the wait for the previous
+// kernel: a prefetch hands nothing to this kernel, and the loads after the wait read L2).
+template <int D, typename T>
+__device__ __forceinline__ void cs_prefetch(const T* src, int C)
+{
+    const uint32_t rows = (uint32_t)min(C, 128);
+    if (rows > 0) tc::prefetch_l2(src, rows * D * (uint32_t)sizeof(T));
 }
 
 // src[TB][D] fp32 rows 0 .. nt - 1 -> rows t0 .. of one group's [C][D] output tensor.
@@ -231,20 +284,35 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int own = 32 * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     const size_t g = blockIdx.x;
+    const T* qg = q + g * (size_t)C * D;
+    const T* kg = k + g * (size_t)C * D;
+    const T* vg = v + g * (size_t)C * D;
+    if (tid == 0) {
+        cs_prefetch<D>(kg, C);
+        cs_prefetch<D>(qg, C);
+        cs_prefetch<D>(vg, C);
+    }
     pdl_wait();
     float s[CL];
 #pragma unroll
     for (int i = 0; i < CL; ++i) s[i] = S0 ? S0[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
-    const T* qg = q + g * (size_t)C * D;
-    const T* kg = k + g * (size_t)C * D;
-    const T* vg = v + g * (size_t)C * D;
+    CsShare<D, T> rk, rq, rv;  // the block about to be staged
+    cs_fetch<D>(rk, kg, 0, min(TB, C));
+    cs_fetch<D>(rq, qg, 0, min(TB, C));
+    cs_fetch<D>(rv, vg, 0, min(TB, C));
     for (int t0 = 0; t0 < C; t0 += TB) {
         const int nt = min(TB, C - t0);
-        cs_stage<D>(sK, kg, t0, nt, nt, nullptr);
-        cs_stage<D>(sQ, qg, t0, nt, nt, nullptr);
-        cs_stage<D>(sV, vg, t0, nt, nt, nullptr);
+        cs_put<D>(sK, rk, 1.f);
+        cs_put<D>(sQ, rq, 1.f);
+        cs_put<D>(sV, rv, 1.f);
         __syncthreads();
+        if (t0 + TB < C) {  // the next block's loads pass under this block's work
+            const int nn = min(TB, C - t0 - TB);
+            cs_fetch<D>(rk, kg, t0 + TB, nn);
+            cs_fetch<D>(rq, qg, t0 + TB, nn);
+            cs_fetch<D>(rv, vg, t0 + TB, nn);
+        }
         cs_denominators<D>(sK, sQ, sO, sInv, nt, zl, eps);
         cs_sweep<D, false>(s, sK, sQ, sV, sY, nt, own, cw);
         __syncthreads();
@@ -286,22 +354,40 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
     const T* gg = dO + g * (size_t)C * D;
     float* winv = ws_inv + g * (size_t)C;
     float* wdd = ws_dd + g * (size_t)C;
+    if (tid == 0) {
+        cs_prefetch<D>(kg, C);
+        cs_prefetch<D>(qg, C);
+        cs_prefetch<D>(vg, C);
+        cs_prefetch<D>(gg, C);
+    }
     pdl_wait();
     float s[CL];
 #pragma unroll
     for (int i = 0; i < CL; ++i) s[i] = S0 ? S0[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
+    const int nblk = (C + TB - 1) / TB;
     // ---- forward sweep
+    CsShare<D, T> ra, rx, rb, rg;  // k, q, v of the block about to be staged; dO of the current one
+    cs_fetch<D>(ra, kg, 0, min(TB, C));
+    cs_fetch<D>(rx, qg, 0, min(TB, C));
+    cs_fetch<D>(rb, vg, 0, min(TB, C));
     for (int t0 = 0; t0 < C; t0 += TB) {
         const int nt = min(TB, C - t0);
-        cs_stage<D>(sA, kg, t0, nt, nt, nullptr);
-        cs_stage<D>(sX, qg, t0, nt, nt, nullptr);
-        cs_stage<D>(sB, vg, t0, nt, nt, nullptr);
+        cs_put<D>(sA, ra, 1.f);
+        cs_put<D>(sX, rx, 1.f);
+        cs_put<D>(sB, rb, 1.f);
         __syncthreads();
+        cs_fetch<D>(rg, gg, t0, nt);
+        if (t0 + TB < C) {  // the next block's loads pass under this block's work
+            const int nn = min(TB, C - t0 - TB);
+            cs_fetch<D>(ra, kg, t0 + TB, nn);
+            cs_fetch<D>(rx, qg, t0 + TB, nn);
+            cs_fetch<D>(rb, vg, t0 + TB, nn);
+        }
         cs_denominators<D>(sA, sX, sO, sInv, nt, zl, eps);
         cs_sweep<D, false>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();  // every slice of every owner has read v
-        cs_stage<D>(sB, gg, t0, nt, nt, nullptr);  // dO
+        cs_put<D>(sB, rg, 1.f);  // dO
         __syncthreads();
         for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = sB[i] * cs_parts<D>(sY, i / D, i % D);
         __syncthreads();
@@ -322,21 +408,34 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
     // ---- reverse sweep: R += q_t dn_t^T (inclusive), dv_t = R^T k_t
 #pragma unroll
     for (int i = 0; i < CL; ++i) s[i] = dS_out ? dS_out[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
-    const int nblk = (C + TB - 1) / TB;
+    // q, k, dO and 1/den of this thread's row, for the block about to be staged (1/den was
+    // written above by another thread of this CTA, before the barriers since)
+    const int row = cs_row<D, T>();
+    float inv = 0.f;
+    if (nblk > 0) {
+        const int t0 = (nblk - 1) * TB, nt = C - t0;
+        cs_fetch<D>(ra, qg, t0, nt);
+        cs_fetch<D>(rx, kg, t0, nt);
+        cs_fetch<D>(rg, gg, t0, nt);
+        inv = row < nt ? winv[t0 + row] : 0.f;
+    }
     for (int bi = nblk - 1; bi >= 0; --bi) {
         const int t0 = bi * TB, nt = min(TB, C - t0);
-        if (tid < nt) sInv[tid] = winv[t0 + tid];
+        cs_put<D>(sA, ra, 1.f);
+        cs_put<D>(sX, rx, 1.f);
+        cs_put<D>(sB, rg, inv);  // dn = dO / den
         __syncthreads();
-        cs_stage<D>(sA, qg, t0, nt, nt, nullptr);
-        cs_stage<D>(sX, kg, t0, nt, nt, nullptr);
-        cs_stage<D>(sB, gg, t0, nt, nt, sInv);  // dn = dO / den
-        __syncthreads();
+        if (bi > 0) {  // the previous block (a whole one) passes under this block's work
+            cs_fetch<D>(ra, qg, t0 - TB, TB);
+            cs_fetch<D>(rx, kg, t0 - TB, TB);
+            cs_fetch<D>(rg, gg, t0 - TB, TB);
+            inv = winv[t0 - TB + row];
+        }
         cs_sweep<D, true>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
         for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = cs_parts<D>(sY, i / D, i % D);
         __syncthreads();
         cs_write<D>(dv + g * (size_t)C * D, sO, t0, nt);
-        __syncthreads();
     }
 }
 
@@ -371,6 +470,11 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
     const T* gg = dO + g * (size_t)C * D;
     const float* winv = ws_inv + g * (size_t)C;
     const float* wdd = ws_dd + g * (size_t)C;
+    if (tid == 0) {
+        cs_prefetch<D>(vg, C);
+        cs_prefetch<D>(gg, C);
+        cs_prefetch<D>(kg, C);
+    }
     pdl_wait();
     float s[CL];
 #pragma unroll
@@ -380,18 +484,29 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
         s[i] = f.x; s[i + 1] = f.y; s[i + 2] = f.z; s[i + 3] = f.w;
     }
     float zr = (tid < D && z0) ? z0[g * D + tid] : 0.f;  // z[p = tid] (forward), then r[p] (reverse)
+    // v, dO, k, this thread's row's 1/den and (threads t < TB) dd of token t, for the block
+    // about to be staged
+    const int row = cs_row<D, T>();
+    const int nblk = (C + TB - 1) / TB;
+    CsShare<D, T> ra, rx, rb;
+    float inv = 0.f, dd = 0.f;
+    auto fetch = [&](const T* a, const T* x, const T* b, int t0, int nt) {
+        cs_fetch<D>(ra, a, t0, nt);
+        cs_fetch<D>(rx, x, t0, nt);
+        cs_fetch<D>(rb, b, t0, nt);
+        inv = row < nt ? winv[t0 + row] : 0.f;
+        dd = tid < nt ? wdd[t0 + tid] : 0.f;
+    };
     // ---- forward sweep: S += k v^T, z += k (inclusive); dq = S dn + dd z
+    if (nblk > 0) fetch(vg, gg, kg, 0, min(TB, C));
     for (int t0 = 0; t0 < C; t0 += TB) {
         const int nt = min(TB, C - t0);
-        if (tid < nt) {
-            sInv[tid] = winv[t0 + tid];
-            sDD[tid] = wdd[t0 + tid];
-        }
+        cs_put<D>(sA, ra, 1.f);
+        cs_put<D>(sX, rx, inv);  // dn = dO / den
+        cs_put<D>(sB, rb, 1.f);
+        if (tid < TB) sDD[tid] = dd;
         __syncthreads();
-        cs_stage<D>(sA, vg, t0, nt, nt, nullptr);
-        cs_stage<D>(sX, gg, t0, nt, nt, sInv);
-        cs_stage<D>(sB, kg, t0, nt, nt, nullptr);
-        __syncthreads();
+        if (t0 + TB < C) fetch(vg, gg, kg, t0 + TB, min(TB, C - t0 - TB));  // passes under this block's work
         cs_sweep<D, false>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
         if (tid < D)
@@ -400,8 +515,7 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
                 sO[tt * D + tid] = fmaf(sDD[tt], zr, cs_parts<D>(sY, tt, tid));
             }
         __syncthreads();
-        cs_write<D>(dq + g * (size_t)C * D, sO, t0, nt);
-        __syncthreads();
+        cs_write<D>(dq + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
     // ---- reverse sweep: R += q dn^T, r += dd q (inclusive); dk = R v + r
 #pragma unroll
@@ -411,18 +525,15 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
         s[i] = f.x; s[i + 1] = f.y; s[i + 2] = f.z; s[i + 3] = f.w;
     }
     zr = (tid < D && dz_out) ? dz_out[g * D + tid] : 0.f;
-    const int nblk = (C + TB - 1) / TB;
+    if (nblk > 0) fetch(gg, vg, qg, (nblk - 1) * TB, C - (nblk - 1) * TB);
     for (int bi = nblk - 1; bi >= 0; --bi) {
         const int t0 = bi * TB, nt = min(TB, C - t0);
-        if (tid < nt) {
-            sInv[tid] = winv[t0 + tid];
-            sDD[tid] = wdd[t0 + tid];
-        }
+        cs_put<D>(sA, ra, inv);  // dn = dO / den
+        cs_put<D>(sX, rx, 1.f);
+        cs_put<D>(sB, rb, 1.f);
+        if (tid < TB) sDD[tid] = dd;
         __syncthreads();
-        cs_stage<D>(sA, gg, t0, nt, nt, sInv);
-        cs_stage<D>(sX, vg, t0, nt, nt, nullptr);
-        cs_stage<D>(sB, qg, t0, nt, nt, nullptr);
-        __syncthreads();
+        if (bi > 0) fetch(gg, vg, qg, t0 - TB, TB);  // passes under this block's work
         cs_sweep<D, true>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
         if (tid < D)
@@ -431,8 +542,7 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
                 sO[tt * D + tid] = cs_parts<D>(sY, tt, tid) + zr;
             }
         __syncthreads();
-        cs_write<D>(dk + g * (size_t)C * D, sO, t0, nt);
-        __syncthreads();
+        cs_write<D>(dk + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
     __syncthreads();
     if (dS0)
