@@ -13,13 +13,15 @@
 //     R_t = dS_out + sum_{i >= t} q_i dn_i^T,  r_t = dz_out + sum_{i >= t} dd_i q_i
 //     dk_t = R_t v_t + r_t,  dv_t = R_t^T k_t,  dS0 = R_0,  dz0 = r_0
 //
-// One CTA per group.  A D x D state is spread over the CTA as (owner, slice): lane l of
-// warp (ow, cw) owns o = 32 ow + l and holds the CL = D / NC entries whose contracted
-// index lies in slice cw.  "Column layout" (owner = value index c, contracted = key index
-// p) serves o = S^T q and dv = R^T k; "row layout" (owner = p, contracted = c) serves
-// dq = S dn and dk = R v.  Per token every lane reads the same CL contracted values (one
-// broadcast per 16 bytes), updates its CL entries and sums its slice of the readout; the
-// NC slice partials meet in shared memory once per block of TB tokens, where the parts
+// One CTA per group.  A D x D state is spread over the CTA as (owners, slice): lane l of
+// warp (ow, cw) owns o = 64 ow + l and o + 32 and holds, for each, the CL = D / NC entries
+// whose contracted index lies in slice cw.  "Column layout" (owner = value index c,
+// contracted = key index p) serves o = S^T q and dv = R^T k; "row layout" (owner = p,
+// contracted = c) serves dq = S dn and dk = R v.  Per token every lane reads the same CL
+// contracted values (one broadcast per 16 bytes, each serving both owners: the sweep is
+// bound by shared-memory loads, so two owners per lane halve them per FMA), updates its
+// 2 CL entries and sums its slice of both readouts; the NC slice partials meet in shared
+// memory once per block of TB tokens, where the parts
 // that are sequential in the token but not in the state (the denominators, the z and r
 // prefixes, the dO . n dots) are also formed.  Tokens are staged TB at a time as fp32
 // (bf16 inputs are widened there), so the scan runs in fp32 in token order.
@@ -39,10 +41,11 @@ namespace la {
 
 template <int D>
 struct CumsumCfg {
-    static constexpr int NOW = D / 32;                // owner warps
-    static constexpr int CL = 16;                     // contracted entries per lane
+    static constexpr int OW = 2;                      // owners per lane: o and o + 32
+    static constexpr int NOW = D / (32 * OW);         // owner warps
+    static constexpr int CL = D == 64 ? 8 : 16;       // contracted entries per lane and owner
     static constexpr int NC = D / CL;                 // contracted slices
-    static constexpr int THREADS = 32 * NOW * NC;     // 256 at D = 64, 1024 at D = 128
+    static constexpr int THREADS = 32 * NOW * NC;     // 256 at D = 64, 512 at D = 128
     static constexpr int TB = D == 64 ? 32 : 16;      // tokens per staging block
     // shared memory (floats): A, X, B, O [TB][D] + Y [NC][TB][D] + inv, dd [TB]
     static constexpr size_t SMEM = ((size_t)(4 + NC) * TB * D + 2 * TB) * 4;
@@ -89,7 +92,7 @@ template <> struct Elem<__nv_bfloat16> {
 // that a load issued for the next block passes under the current block's work.
 template <int D, typename T>
 struct CsShare {
-    static constexpr int E = CumsumCfg<D>::TB * D / CumsumCfg<D>::THREADS;  // 8 at D = 64, 2 at D = 128
+    static constexpr int E = CumsumCfg<D>::TB * D / CumsumCfg<D>::THREADS;  // 8 at D = 64, 4 at D = 128
     static constexpr int WORDS = E * (int)sizeof(T) / 4;
     static_assert(E * CumsumCfg<D>::THREADS == CumsumCfg<D>::TB * D && D % E == 0, "whole rows per block");
     uint32_t w[WORDS];
@@ -143,6 +146,8 @@ __device__ __forceinline__ void cs_put(float* dst, const CsShare<D, T>& r, float
     if constexpr (Sh::E == 8) {
         reinterpret_cast<float4*>(d)[0] = make_float4(f[0], f[1], f[2], f[3]);
         reinterpret_cast<float4*>(d)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else if constexpr (Sh::E == 4) {
+        *reinterpret_cast<float4*>(d) = make_float4(f[0], f[1], f[2], f[3]);
     } else {
         static_assert(Sh::E == 2, "share sizes");
         *reinterpret_cast<float2*>(d) = make_float2(f[0], f[1]);
@@ -178,47 +183,110 @@ __device__ __forceinline__ void cs_write(T* dst, const float* src, int t0, int n
 }
 
 
-// One token of a sweep for this lane: s += a b (a: the slice's contracted values, b: the
-// owner's value), then this slice's part of the readout sum_i x_i s_i.
-template <int CL>
-__device__ __forceinline__ float cs_token(float (&s)[CL], const float* a, const float* x, float b)
+// One token of a sweep for this lane's owners: s[u] += a b[u] (a: the slice's contracted
+// values, b[u]: owner u's value), then this slice's part of the readout y[u] = sum_i x_i
+// s[u]_i.  Each contracted value loaded from shared memory serves both owners.
+template <int CL, int OW>
+__device__ __forceinline__ void cs_token(float (&s)[OW][CL], const float* a, const float* x, const float (&b)[OW],
+                                         float (&y)[OW])
 {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[OW][2];
+#pragma unroll
+    for (int u = 0; u < OW; ++u) acc[u][0] = acc[u][1] = 0.f;
 #pragma unroll
     for (int i = 0; i < CL; i += 4) {
         const float4 a4 = *reinterpret_cast<const float4*>(a + i);
         const float4 x4 = *reinterpret_cast<const float4*>(x + i);
-        s[i] = fmaf(a4.x, b, s[i]);
-        s[i + 1] = fmaf(a4.y, b, s[i + 1]);
-        s[i + 2] = fmaf(a4.z, b, s[i + 2]);
-        s[i + 3] = fmaf(a4.w, b, s[i + 3]);
-        acc[0] = fmaf(x4.x, s[i], acc[0]);
-        acc[1] = fmaf(x4.y, s[i + 1], acc[1]);
-        acc[2] = fmaf(x4.z, s[i + 2], acc[2]);
-        acc[3] = fmaf(x4.w, s[i + 3], acc[3]);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+        for (int u = 0; u < OW; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[u][i + e] = fmaf(av[e], b[u], s[u][i + e]);
+                acc[u][e & 1] = fmaf(xv[e], s[u][i + e], acc[u][e & 1]);
+            }
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int u = 0; u < OW; ++u) y[u] = acc[u][0] + acc[u][1];
 }
 
-// The block's tokens through this lane's state, in order (REV: from the last), each
-// readout part -> sY[cw][tt][o].
+// The block's tokens through this lane's state, in order (REV: from the last); owner u is
+// own + 32 u, its readout part -> sY[cw][tt][own + 32 u].
 template <int D, bool REV>
-__device__ __forceinline__ void cs_sweep(float (&s)[CumsumCfg<D>::CL], const float* sA, const float* sX,
-                                         const float* sB, float* sY, int nt, int o, int cw)
+__device__ __forceinline__ void cs_sweep(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* sA,
+                                         const float* sX, const float* sB, float* sY, int nt, int own, int cw)
 {
     using Cf = CumsumCfg<D>;
-    constexpr int CL = Cf::CL, TB = Cf::TB;
-    float* y = sY + cw * TB * D + o;
+    constexpr int CL = Cf::CL, TB = Cf::TB, OW = Cf::OW;
+    float* y = sY + cw * TB * D + own;
     const float* a = sA + cw * CL;
     const float* x = sX + cw * CL;
-    const float* b = sB + o;
+    const float* b = sB + own;
+    auto token = [&](int tt) {
+        float bv[OW], yv[OW];
+#pragma unroll
+        for (int u = 0; u < OW; ++u) bv[u] = b[tt * D + 32 * u];
+        cs_token<CL, OW>(s, a + tt * D, x + tt * D, bv, yv);
+#pragma unroll
+        for (int u = 0; u < OW; ++u) y[tt * D + 32 * u] = yv[u];
+    };
     if (!REV) {
 #pragma unroll 2
-        for (int tt = 0; tt < nt; ++tt) y[tt * D] = cs_token<CL>(s, a + tt * D, x + tt * D, b[tt * D]);
+        for (int tt = 0; tt < nt; ++tt) token(tt);
     } else {
 #pragma unroll 2
-        for (int tt = nt - 1; tt >= 0; --tt) y[tt * D] = cs_token<CL>(s, a + tt * D, x + tt * D, b[tt * D]);
+        for (int tt = nt - 1; tt >= 0; --tt) token(tt);
     }
+}
+
+// A D x D matrix <-> this lane's state.  Column layout: s[u][i] = M[p = cw CL + i][own + 32 u]
+// (lanes read consecutive columns); row layout: s[u][i] = M[own + 32 u][c = cw CL + i]
+// (16-byte pieces of a row).  A NULL source is zero.
+template <int D>
+__device__ __forceinline__ void cs_load_col(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* M, int own,
+                                            int cw)
+{
+    using Cf = CumsumCfg<D>;
+#pragma unroll
+    for (int u = 0; u < Cf::OW; ++u)
+#pragma unroll
+        for (int i = 0; i < Cf::CL; ++i) s[u][i] = M ? M[(size_t)(cw * Cf::CL + i) * D + own + 32 * u] : 0.f;
+}
+template <int D>
+__device__ __forceinline__ void cs_store_col(const float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], float* M, int own,
+                                             int cw)
+{
+    using Cf = CumsumCfg<D>;
+#pragma unroll
+    for (int u = 0; u < Cf::OW; ++u)
+#pragma unroll
+        for (int i = 0; i < Cf::CL; ++i) M[(size_t)(cw * Cf::CL + i) * D + own + 32 * u] = s[u][i];
+}
+template <int D>
+__device__ __forceinline__ void cs_load_row(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* M, int own,
+                                            int cw)
+{
+    using Cf = CumsumCfg<D>;
+#pragma unroll
+    for (int u = 0; u < Cf::OW; ++u)
+#pragma unroll
+        for (int i = 0; i < Cf::CL; i += 4) {
+            const float4 f = M ? *reinterpret_cast<const float4*>(M + (size_t)(own + 32 * u) * D + cw * Cf::CL + i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[u][i] = f.x; s[u][i + 1] = f.y; s[u][i + 2] = f.z; s[u][i + 3] = f.w;
+        }
+}
+template <int D>
+__device__ __forceinline__ void cs_store_row(const float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], float* M, int own,
+                                             int cw)
+{
+    using Cf = CumsumCfg<D>;
+#pragma unroll
+    for (int u = 0; u < Cf::OW; ++u)
+#pragma unroll
+        for (int i = 0; i < Cf::CL; i += 4)
+            *reinterpret_cast<float4*>(M + (size_t)(own + 32 * u) * D + cw * Cf::CL + i) =
+                make_float4(s[u][i], s[u][i + 1], s[u][i + 2], s[u][i + 3]);
 }
 
 // sum of the NC slice parts of token tt, owner o
@@ -233,8 +301,8 @@ __device__ __forceinline__ float cs_parts(const float* sY, int tt, int o)
 }
 
 // 1/den of the block's tokens -> sInv[0 .. nt): threads p < D carry z[p] (zl) across blocks
-// and write q_t[p] z_t[p] into scratch[TB][D]; thread t < nt then sums row t.  Ends with
-// the CTA synchronised.
+// and write q_t[p] z_t[p] into scratch[TB][D]; eight threads per token then sum its row.
+// Ends with the CTA synchronised.
 template <int D>
 __device__ __forceinline__ void cs_denominators(const float* sK, const float* sQ, float* scratch, float* sInv, int nt,
                                                 float& zl, float eps)
@@ -251,21 +319,29 @@ __device__ __forceinline__ void cs_denominators(const float* sK, const float* sQ
         }
     }
     __syncthreads();
-    if (tid < nt) {
+    // row sums, eight threads per token: thread j of token t adds the float4s at 4 j + 32 m
+    // (a quarter warp reads 128 contiguous bytes), then the eight meet by shuffles
+    constexpr int TB = CumsumCfg<D>::TB;
+    static_assert(8 * TB % 32 == 0 && 8 * TB <= CumsumCfg<D>::THREADS, "whole warps of eight threads per token");
+    if (tid < 8 * TB) {
+        const int t = tid >> 3, j = tid & 7;
+        const float* r = scratch + t * D + 4 * j;
         float acc = 0.f;
-        const float4* r = reinterpret_cast<const float4*>(scratch + tid * D);
-#pragma unroll 4
-        for (int j = 0; j < D / 4; ++j) {
-            const float4 f = r[j];
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) {
+            const float4 f = *reinterpret_cast<const float4*>(r + 32 * m);
             acc += (f.x + f.y) + (f.z + f.w);
         }
-        sInv[tid] = 1.f / (acc + eps);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (j == 0 && t < nt) sInv[t] = 1.f / (acc + eps);
     }
     __syncthreads();
 }
 
 // ---------------------------------------------------------------- forward
-// Column layout: s[i] = S[p = cw CL + i][c = o].  S_out may be S0 and z_out z0: every entry
+// Column layout: s[u][i] = S[p = cw CL + i][c = own + 32 u].  S_out may be S0 and z_out z0: every entry
 // is read and written back by the same thread, after a barrier.
 template <int D, typename T>
 __global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
@@ -282,7 +358,7 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
     float* sY = sO + TB * D;       // [NC][TB][D]
     float* sInv = sY + Cf::NC * TB * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int own = 32 * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
+    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     const size_t g = blockIdx.x;
     const T* qg = q + g * (size_t)C * D;
     const T* kg = k + g * (size_t)C * D;
@@ -293,9 +369,8 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
         cs_prefetch<D>(vg, C);
     }
     pdl_wait();
-    float s[CL];
-#pragma unroll
-    for (int i = 0; i < CL; ++i) s[i] = S0 ? S0[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
+    float s[Cf::OW][CL];
+    cs_load_col<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
     CsShare<D, T> rk, rq, rv;  // the block about to be staged
     cs_fetch<D>(rk, kg, 0, min(TB, C));
@@ -321,9 +396,7 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
         cs_write<D>(o + g * (size_t)C * D, sO, t0, nt);
     }
     __syncthreads();  // every thread has read its S0 / z0 entries before any is overwritten
-    if (S_out)
-#pragma unroll
-        for (int i = 0; i < CL; ++i) S_out[g * D * D + (size_t)(cw * CL + i) * D + own] = s[i];
+    if (S_out) cs_store_col<D>(s, S_out + g * D * D, own, cw);
     if (z_out && tid < D) z_out[g * D + tid] = zl;
 }
 
@@ -346,7 +419,7 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
     float* sY = sO + TB * D;       // [NC][TB][D]
     float* sInv = sY + Cf::NC * TB * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int own = 32 * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
+    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     const size_t g = blockIdx.x;
     const T* qg = q + g * (size_t)C * D;
     const T* kg = k + g * (size_t)C * D;
@@ -361,9 +434,8 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
         cs_prefetch<D>(gg, C);
     }
     pdl_wait();
-    float s[CL];
-#pragma unroll
-    for (int i = 0; i < CL; ++i) s[i] = S0 ? S0[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
+    float s[Cf::OW][CL];
+    cs_load_col<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
     const int nblk = (C + TB - 1) / TB;
     // ---- forward sweep
@@ -406,8 +478,7 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
         __syncthreads();
     }
     // ---- reverse sweep: R += q_t dn_t^T (inclusive), dv_t = R^T k_t
-#pragma unroll
-    for (int i = 0; i < CL; ++i) s[i] = dS_out ? dS_out[g * D * D + (size_t)(cw * CL + i) * D + own] : 0.f;
+    cs_load_col<D>(s, dS_out ? dS_out + g * D * D : nullptr, own, cw);
     // q, k, dO and 1/den of this thread's row, for the block about to be staged (1/den was
     // written above by another thread of this CTA, before the barriers since)
     const int row = cs_row<D, T>();
@@ -440,7 +511,7 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
 }
 
 // ---------------------------------------------------------------- backward, row layout
-// s[i] = S[p = o][c = cw CL + i] (then R).  Forward sweep: dq_t[p] = sum_c S_t[p][c] dn_t[c]
+// s[u][i] = S[p = own + 32 u][c = cw CL + i] (then R).  Forward sweep: dq_t[p] = sum_c S_t[p][c] dn_t[c]
 // + dd_t z_t[p]; reverse sweep: dk_t[p] = sum_c R_t[p][c] v_t[c] + r_t[p], dS0 = R_0,
 // dz0 = r_0 (each thread writes back only the dS_out / dz_out entries it read itself).
 // z and r run as prefixes in threads p < D.  1/den and dd come from
@@ -462,7 +533,7 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
     float* sInv = sY + Cf::NC * TB * D;
     float* sDD = sInv + TB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int own = 32 * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
+    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     const size_t g = blockIdx.x;
     const T* qg = q + g * (size_t)C * D;
     const T* kg = k + g * (size_t)C * D;
@@ -476,13 +547,8 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
         cs_prefetch<D>(kg, C);
     }
     pdl_wait();
-    float s[CL];
-#pragma unroll
-    for (int i = 0; i < CL; i += 4) {
-        const float4 f = S0 ? *reinterpret_cast<const float4*>(S0 + g * D * D + (size_t)own * D + cw * CL + i)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        s[i] = f.x; s[i + 1] = f.y; s[i + 2] = f.z; s[i + 3] = f.w;
-    }
+    float s[Cf::OW][CL];
+    cs_load_row<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
     float zr = (tid < D && z0) ? z0[g * D + tid] : 0.f;  // z[p = tid] (forward), then r[p] (reverse)
     // v, dO, k, this thread's row's 1/den and (threads t < TB) dd of token t, for the block
     // about to be staged
@@ -518,12 +584,7 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
         cs_write<D>(dq + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
     // ---- reverse sweep: R += q dn^T, r += dd q (inclusive); dk = R v + r
-#pragma unroll
-    for (int i = 0; i < CL; i += 4) {
-        const float4 f = dS_out ? *reinterpret_cast<const float4*>(dS_out + g * D * D + (size_t)own * D + cw * CL + i)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        s[i] = f.x; s[i + 1] = f.y; s[i + 2] = f.z; s[i + 3] = f.w;
-    }
+    cs_load_row<D>(s, dS_out ? dS_out + g * D * D : nullptr, own, cw);
     zr = (tid < D && dz_out) ? dz_out[g * D + tid] : 0.f;
     if (nblk > 0) fetch(gg, vg, qg, (nblk - 1) * TB, C - (nblk - 1) * TB);
     for (int bi = nblk - 1; bi >= 0; --bi) {
@@ -545,11 +606,7 @@ la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, co
         cs_write<D>(dk + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
     __syncthreads();
-    if (dS0)
-#pragma unroll
-        for (int i = 0; i < CL; i += 4)
-            *reinterpret_cast<float4*>(dS0 + g * D * D + (size_t)own * D + cw * CL + i) =
-                make_float4(s[i], s[i + 1], s[i + 2], s[i + 3]);
+    if (dS0) cs_store_row<D>(s, dS0 + g * D * D, own, cw);
     if (dz0 && tid < D) dz0[g * D + tid] = zr;
 }
 
