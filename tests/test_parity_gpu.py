@@ -300,8 +300,11 @@ def test_chunk_parallel_forward(G, C, D):
     torch.cuda.synchronize()
     ref = oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS)
     check(got, ref, "bf16", FWD_NAMES)
+    # the split sums each piece's k v^T and then prefixes the pieces: the carry's fp32 sums
+    # are grouped differently from the sequential kernel's, by more as the chunk grows
+    # (1.7e-5 at 12,800 tokens; 1e-2 is the carry's bound against the oracle)
     for a, b, n in zip(got, seq, FWD_NAMES):
-        assert max_rel(a, b.cpu().double().numpy()) < (2e-2 if n == "o" else 1e-5), n
+        assert max_rel(a, b.cpu().double().numpy()) < (2e-2 if n == "o" else 5e-5), n
 
 
 @pytest.mark.parametrize("D", [64, 128])
