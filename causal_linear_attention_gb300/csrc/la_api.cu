@@ -703,6 +703,14 @@ extern "C" la_status la_chunked_bwd_split(const void* q, const void* k, const vo
 // ---------------------------------------------------------------- cumsum form
 namespace {
 
+// 1/den and dd per token, then (from a 16-byte boundary) room for one D x D copy of dS_out
+// per group, used when dS0 is dS_out; nothing for an empty chunk.  Offsets in floats.
+size_t cumsum_bwd_copy_offset(int G, int C) { return ((size_t)2 * G * C + 3) & ~(size_t)3; }
+size_t cumsum_bwd_ws_bytes(int G, int C, int D)
+{
+    return C > 0 ? (cumsum_bwd_copy_offset(G, C) + (size_t)G * D * D) * 4 : 0;
+}
+
 template <int D, typename T>
 la_status cumsum_fwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
                             float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
@@ -722,25 +730,28 @@ la_status cumsum_bwd_launch(const void* q, const void* k, const void* v, const f
                             float* dS0, float* dz0, int G, int C, float eps, float* ws, cudaStream_t stream)
 {
     using Cf = la::CumsumCfg<D>;
-    static OptIn fc, fr;
-    auto kc = la::la_cumsum_bwd_col_kernel<D, T>;
-    auto kr = la::la_cumsum_bwd_row_kernel<D, T>;
-    la_status st = prepare(kc, fc, Cf::SMEM);
-    if (st == LA_OK) st = prepare(kr, fr, Cf::SMEM);
+    static OptIn fa, fb;
+    auto ka = la::la_cumsum_bwd_scan_kernel<D, T>;
+    auto kb = la::la_cumsum_bwd_sweeps_kernel<D, T>;
+    la_status st = prepare(ka, fa, Cf::SMEM);
+    if (st == LA_OK) st = prepare(kb, fb, Cf::SMEM);
     if (st != LA_OK) return st;
     float* ws_inv = ws;
     float* ws_dd = ws + (size_t)G * C;
+    // dS0 written in place over dS_out: the reverse column sweep reads a copy (see the kernels)
+    const bool alias = C > 0 && dS0 && dS0 == dS_out;
+    float* R0copy = alias ? ws + cumsum_bwd_copy_offset(G, C) : nullptr;
+    const float* R0 = C == 0 ? nullptr : alias ? R0copy : dS_out;
     const T* tq = static_cast<const T*>(q);
     const T* tk = static_cast<const T*>(k);
     const T* tv = static_cast<const T*>(v);
     const T* tg = static_cast<const T*>(dO);
-    st = launch_pdl(kc, G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, static_cast<T*>(dv),
-                    ws_inv, ws_dd, C, eps);
+    st = launch_pdl(ka, G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, R0copy, ws_inv, ws_dd, C,
+                    eps);
     if (st != LA_OK) return st;
-    // both kernels start R from dS_out; only the second writes dS0 (which may be dS_out)
-    return launch_pdl(kr, G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, dz_out,
-                      static_cast<T*>(dq), static_cast<T*>(dk), dS0, dz0, static_cast<const float*>(ws_inv),
-                      static_cast<const float*>(ws_dd), C);
+    return launch_pdl(kb, 3 * G, Cf::THREADS, Cf::SMEM, stream, tq, tk, tv, S0, z0, tg, dS_out, dz_out, R0,
+                      static_cast<T*>(dq), static_cast<T*>(dk), static_cast<T*>(dv), dS0, dz0,
+                      static_cast<const float*>(ws_inv), static_cast<const float*>(ws_dd), C);
 }
 
 }  // namespace
@@ -764,7 +775,7 @@ extern "C" size_t la_cumsum_bwd_workspace_bytes(int G, int C, int D, la_dtype dt
 {
     size_t esz = 0;
     if (check_common(G, C, D, 64, dtype, 0.f, &esz) != LA_OK) return 0;
-    return (size_t)2 * G * C * 4;
+    return cumsum_bwd_ws_bytes(G, C, D);
 }
 
 extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, const float* S0, const float* z0,
@@ -775,7 +786,7 @@ extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, 
     la_status st = check_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, 64, dtype, eps);
     if (st != LA_OK) return st;
     if (G == 0) return LA_OK;
-    const size_t need = (size_t)2 * G * C * 4;
+    const size_t need = cumsum_bwd_ws_bytes(G, C, D);
     if (need > 0) {
         if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0 || workspace_bytes < need)
             return LA_ERR_INVALID;

@@ -26,10 +26,9 @@
 // prefixes, the dO . n dots) are also formed.  Tokens are staged TB at a time as fp32
 // (bf16 inputs are widened there), so the scan runs in fp32 in token order.
 //
-// The backward runs in two launches: la_cumsum_bwd_col_kernel (forward sweep: 1/den and
-// dd of every token -> workspace; reverse sweep: dv) and la_cumsum_bwd_row_kernel
-// (forward sweep: dq; reverse sweep: dk, dS0, dz0), which reads 1/den and dd back.  Both
-// start R from dS_out, so only the second writes dS0: it may then be dS_out itself.
+// The backward runs in two launches: la_cumsum_bwd_scan_kernel (the forward sweep: 1/den
+// and dd of every token -> workspace), then la_cumsum_bwd_sweeps_kernel, whose three CTAs per
+// group run the three sweeps that need only those, side by side (dv; dq; dk, dS0, dz0).
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -158,13 +157,14 @@ __device__ __forceinline__ void cs_put(float* dst, const CsShare<D, T>& r, float
 template <int D, typename T>
 __device__ __forceinline__ int cs_row() { return CsShare<D, T>::E * (int)threadIdx.x / D; }
 
-// Start the first rows of a group's tensor towards L2 (before the wait for the previous
-// kernel: a prefetch hands nothing to this kernel, and the loads after the wait read L2).
+// Start rows r0 .. of a group's tensor (up to 128 of them, not past C) towards L2 (before
+// the wait for the previous kernel: a prefetch hands nothing to this kernel, and the loads
+// after the wait read L2).
 template <int D, typename T>
-__device__ __forceinline__ void cs_prefetch(const T* src, int C)
+__device__ __forceinline__ void cs_prefetch(const T* src, int r0, int C)
 {
-    const uint32_t rows = (uint32_t)min(C, 128);
-    if (rows > 0) tc::prefetch_l2(src, rows * D * (uint32_t)sizeof(T));
+    const uint32_t rows = (uint32_t)min(C - r0, 128);
+    if (r0 >= 0 && C - r0 > 0) tc::prefetch_l2(src + (size_t)r0 * D, rows * D * (uint32_t)sizeof(T));
 }
 
 // src[TB][D] fp32 rows 0 .. nt - 1 -> rows t0 .. of one group's [C][D] output tensor.
@@ -364,9 +364,9 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
     const T* kg = k + g * (size_t)C * D;
     const T* vg = v + g * (size_t)C * D;
     if (tid == 0) {
-        cs_prefetch<D>(kg, C);
-        cs_prefetch<D>(qg, C);
-        cs_prefetch<D>(vg, C);
+        cs_prefetch<D>(kg, 0, C);
+        cs_prefetch<D>(qg, 0, C);
+        cs_prefetch<D>(vg, 0, C);
     }
     pdl_wait();
     float s[Cf::OW][CL];
@@ -400,22 +400,49 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
     if (z_out && tid < D) z_out[g * D + tid] = zl;
 }
 
-// ---------------------------------------------------------------- backward, column layout
-// Forward sweep: n_t = S_t^T q_t and den_t -> 1/den_t and dd_t = -(dO_t . n_t) / den_t^2 of
-// every token in ws_inv / ws_dd ([G][C] fp32); reverse sweep: R (column layout) from
-// dS_out, dv_t = R_t^T k_t.
+// ---------------------------------------------------------------- backward
+// la_cumsum_bwd_scan_kernel (one CTA per group, column layout) runs the forward sweep:
+// n_t = S_t^T q_t and den_t -> 1/den_t and dd_t = -(dO_t . n_t) / den_t^2 of every token into
+// ws_inv / ws_dd ([G][C] fp32).  The three sweeps left need only those and nothing from one
+// another, so la_cumsum_bwd_sweeps_kernel runs them side by side, three CTAs per group:
+//   part 0, column layout, reverse: R from dS_out, dv_t = R_t^T k_t;
+//   part 1, row layout, forward: dq_t = S_t dn_t + dd_t z_t (z from z0);
+//   part 2, row layout, reverse: dk_t = R_t v_t + r_t, dS0 = R_0, dz0 = r_0 (r from dz_out).
+// dS0 may be dS_out itself: part 2 writes dS0 when it ends, and part 0 of the same group
+// need not have read dS_out by then, so the scan kernel first copies dS_out into the
+// workspace (R0copy) and part 0 reads the copy.
+
+// Sum of row t = tid / 8 of rows[TB][D] (shared memory) by threads 8 t .. 8 t + 7 (whole
+// warps, threads < 8 TB): thread j adds the float4s at 4 j + 32 m (a quarter warp reads 128
+// contiguous bytes), then the eight meet by shuffles; each of the eight returns the sum.
+template <int D>
+__device__ __forceinline__ float cs_row_sum8(const float* rows)
+{
+    const float* r = rows + (threadIdx.x >> 3) * D + 4 * (threadIdx.x & 7);
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < D / 32; ++m) {
+        const float4 f = *reinterpret_cast<const float4*>(r + 32 * m);
+        acc += (f.x + f.y) + (f.z + f.w);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    return acc;
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
-la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, const T* dO,
-                         const float* dS_out, T* dv, float* ws_inv, float* ws_dd, int C, float eps)
+la_cumsum_bwd_scan_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, const T* dO,
+                          const float* dS_out, float* R0copy, float* ws_inv, float* ws_dd, int C, float eps)
 {
     using Cf = CumsumCfg<D>;
     constexpr int TB = Cf::TB, CL = Cf::CL;
     extern __shared__ __align__(16) float smf[];
-    float* sA = smf;               // k (forward) / q (reverse): the update's contracted vector
-    float* sX = sA + TB * D;       // q (forward) / k (reverse): the readout vector
-    float* sB = sX + TB * D;       // v (forward) / dn (reverse): the owner vector
-    float* sO = sB + TB * D;       // q z, then dO n products (forward) / dv out (reverse)
+    float* sA = smf;               // k: the update's contracted vector
+    float* sX = sA + TB * D;       // q: the readout vector
+    float* sB = sX + TB * D;       // v: the owner vector, then dO
+    float* sO = sB + TB * D;       // q z, then dO n products
     float* sY = sO + TB * D;       // [NC][TB][D]
     float* sInv = sY + Cf::NC * TB * D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -428,17 +455,20 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
     float* winv = ws_inv + g * (size_t)C;
     float* wdd = ws_dd + g * (size_t)C;
     if (tid == 0) {
-        cs_prefetch<D>(kg, C);
-        cs_prefetch<D>(qg, C);
-        cs_prefetch<D>(vg, C);
-        cs_prefetch<D>(gg, C);
+        cs_prefetch<D>(kg, 0, C);
+        cs_prefetch<D>(qg, 0, C);
+        cs_prefetch<D>(vg, 0, C);
+        cs_prefetch<D>(gg, 0, C);
     }
     pdl_wait();
+    if (R0copy) {  // dS0 is dS_out: the reverse column sweep reads this copy
+        const float4* src = reinterpret_cast<const float4*>(dS_out + g * D * D);
+        float4* dst = reinterpret_cast<float4*>(R0copy + g * D * D);
+        for (int i = tid; i < D * D / 4; i += Cf::THREADS) dst[i] = src[i];
+    }
     float s[Cf::OW][CL];
     cs_load_col<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
-    const int nblk = (C + TB - 1) / TB;
-    // ---- forward sweep
     CsShare<D, T> ra, rx, rb, rg;  // k, q, v of the block about to be staged; dO of the current one
     cs_fetch<D>(ra, kg, 0, min(TB, C));
     cs_fetch<D>(rx, qg, 0, min(TB, C));
@@ -463,151 +493,162 @@ la_cumsum_bwd_col_kernel(const T* q, const T* k, const T* v, const float* S0, co
         __syncthreads();
         for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = sB[i] * cs_parts<D>(sY, i / D, i % D);
         __syncthreads();
-        if (tid < nt) {
-            float dot = 0.f;
-            const float4* r = reinterpret_cast<const float4*>(sO + tid * D);
-#pragma unroll 4
-            for (int j = 0; j < D / 4; ++j) {
-                const float4 f = r[j];
-                dot += (f.x + f.y) + (f.z + f.w);
+        if (tid < 8 * TB) {
+            const float dot = cs_row_sum8<D>(sO);
+            const int t = tid >> 3;
+            if ((tid & 7) == 0 && t < nt) {
+                const float inv = sInv[t];
+                winv[t0 + t] = inv;
+                wdd[t0 + t] = -dot * inv * inv;
             }
-            const float inv = sInv[tid];
-            winv[t0 + tid] = inv;
-            wdd[t0 + tid] = -dot * inv * inv;
         }
         __syncthreads();
     }
-    // ---- reverse sweep: R += q_t dn_t^T (inclusive), dv_t = R^T k_t
-    cs_load_col<D>(s, dS_out ? dS_out + g * D * D : nullptr, own, cw);
-    // q, k, dO and 1/den of this thread's row, for the block about to be staged (1/den was
-    // written above by another thread of this CTA, before the barriers since)
-    const int row = cs_row<D, T>();
+}
+
+// Part 0: column layout, reverse from R0 (dS_out or its copy): R += q_t dn_t^T (inclusive),
+// dv_t = R_t^T k_t.  Pointers are the group's.
+template <int D, typename T>
+__device__ __forceinline__ void cs_bwd_dv(float* smf, const T* qg, const T* kg, const T* gg, const float* R0,
+                                          const float* winv, T* dvg, int C)
+{
+    using Cf = CumsumCfg<D>;
+    constexpr int TB = Cf::TB, CL = Cf::CL;
+    float* sA = smf;          // q
+    float* sX = sA + TB * D;  // k
+    float* sB = sX + TB * D;  // dn
+    float* sO = sB + TB * D;  // dv out
+    float* sY = sO + TB * D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
+    float s[Cf::OW][CL];
+    cs_load_col<D>(s, R0, own, cw);
+    const int row = cs_row<D, T>(), nblk = (C + TB - 1) / TB;
+    CsShare<D, T> ra, rx, rg;  // q, k, dO of the block about to be staged, and its row's 1/den
     float inv = 0.f;
-    if (nblk > 0) {
-        const int t0 = (nblk - 1) * TB, nt = C - t0;
+    auto fetch = [&](int t0, int nt) {
         cs_fetch<D>(ra, qg, t0, nt);
         cs_fetch<D>(rx, kg, t0, nt);
         cs_fetch<D>(rg, gg, t0, nt);
         inv = row < nt ? winv[t0 + row] : 0.f;
-    }
+    };
+    if (nblk > 0) fetch((nblk - 1) * TB, C - (nblk - 1) * TB);
     for (int bi = nblk - 1; bi >= 0; --bi) {
         const int t0 = bi * TB, nt = min(TB, C - t0);
         cs_put<D>(sA, ra, 1.f);
         cs_put<D>(sX, rx, 1.f);
         cs_put<D>(sB, rg, inv);  // dn = dO / den
         __syncthreads();
-        if (bi > 0) {  // the previous block (a whole one) passes under this block's work
-            cs_fetch<D>(ra, qg, t0 - TB, TB);
-            cs_fetch<D>(rx, kg, t0 - TB, TB);
-            cs_fetch<D>(rg, gg, t0 - TB, TB);
-            inv = winv[t0 - TB + row];
-        }
+        if (bi > 0) fetch(t0 - TB, TB);  // the previous (whole) block passes under this one's work
         cs_sweep<D, true>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
         for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = cs_parts<D>(sY, i / D, i % D);
         __syncthreads();
-        cs_write<D>(dv + g * (size_t)C * D, sO, t0, nt);
+        cs_write<D>(dvg, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
 }
 
-// ---------------------------------------------------------------- backward, row layout
-// s[u][i] = S[p = own + 32 u][c = cw CL + i] (then R).  Forward sweep: dq_t[p] = sum_c S_t[p][c] dn_t[c]
-// + dd_t z_t[p]; reverse sweep: dk_t[p] = sum_c R_t[p][c] v_t[c] + r_t[p], dS0 = R_0,
+// Parts 1 and 2: row layout, s[u][i] = S[p = own + 32 u][c = cw CL + i] (then R).  REV false:
+// S += k v^T, z += k (inclusive; S, z from S0, z0), out = dq = S dn + dd z.  REV true: R +=
+// q dn^T, r += dd q (inclusive; from dS_out, dz_out), out = dk = R v + r, then dS0 = R_0,
 // dz0 = r_0 (each thread writes back only the dS_out / dz_out entries it read itself).
-// z and r run as prefixes in threads p < D.  1/den and dd come from
-// la_cumsum_bwd_col_kernel.
-template <int D, typename T>
-__global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
-la_cumsum_bwd_row_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, const T* dO,
-                         const float* dS_out, const float* dz_out, T* dq, T* dk, float* dS0, float* dz0,
-                         const float* ws_inv, const float* ws_dd, int C)
+// z and r run as prefixes in threads p < D.
+template <int D, typename T, bool REV>
+__device__ __forceinline__ void cs_bwd_row(float* smf, const T* qg, const T* kg, const T* vg, const T* gg,
+                                           const float* M0, const float* m0, const float* winv, const float* wdd,
+                                           T* outg, float* Mend, float* mend, int C)
 {
     using Cf = CumsumCfg<D>;
     constexpr int TB = Cf::TB, CL = Cf::CL;
-    extern __shared__ __align__(16) float smf[];
-    float* sA = smf;               // v (forward) / dn (reverse): the update's contracted vector
-    float* sX = sA + TB * D;       // dn (forward) / v (reverse): the readout vector
-    float* sB = sX + TB * D;       // k (forward) / q (reverse): the owner vector
-    float* sO = sB + TB * D;       // dq / dk out
-    float* sY = sO + TB * D;       // [NC][TB][D]
-    float* sInv = sY + Cf::NC * TB * D;
-    float* sDD = sInv + TB;
+    float* sA = smf;          // v (forward) / dn (reverse): the update's contracted vector
+    float* sX = sA + TB * D;  // dn (forward) / v (reverse): the readout vector
+    float* sB = sX + TB * D;  // k (forward) / q (reverse): the owner vector
+    float* sO = sB + TB * D;  // dq / dk out
+    float* sY = sO + TB * D;
+    float* sDD = sY + Cf::NC * TB * D + TB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
-    const size_t g = blockIdx.x;
+    float s[Cf::OW][CL];
+    cs_load_row<D>(s, M0, own, cw);
+    float zr = (tid < D && m0) ? m0[tid] : 0.f;
+    const int row = cs_row<D, T>(), nblk = (C + TB - 1) / TB;
+    CsShare<D, T> ra, rx, rb;  // the block about to be staged, its row's 1/den, dd of token tid
+    float inv = 0.f, dd = 0.f;
+    auto fetch = [&](int t0, int nt) {
+        cs_fetch<D>(ra, REV ? gg : vg, t0, nt);
+        cs_fetch<D>(rx, REV ? vg : gg, t0, nt);
+        cs_fetch<D>(rb, REV ? qg : kg, t0, nt);
+        inv = row < nt ? winv[t0 + row] : 0.f;
+        dd = tid < nt ? wdd[t0 + tid] : 0.f;
+    };
+    if (nblk > 0) fetch(REV ? (nblk - 1) * TB : 0, REV ? C - (nblk - 1) * TB : min(TB, C));
+    for (int n = 0; n < nblk; ++n) {
+        const int bi = REV ? nblk - 1 - n : n;
+        const int t0 = bi * TB, nt = min(TB, C - t0);
+        cs_put<D>(sA, ra, REV ? inv : 1.f);  // dn = dO / den
+        cs_put<D>(sX, rx, REV ? 1.f : inv);
+        cs_put<D>(sB, rb, 1.f);
+        if (tid < TB) sDD[tid] = dd;
+        __syncthreads();
+        if (n + 1 < nblk) {  // the next block in sweep order passes under this one's work
+            const int tn = REV ? t0 - TB : t0 + TB;
+            fetch(tn, min(TB, C - tn));
+        }
+        cs_sweep<D, REV>(s, sA, sX, sB, sY, nt, own, cw);
+        __syncthreads();
+        if (tid < D) {
+            if (!REV) {
+                for (int tt = 0; tt < nt; ++tt) {
+                    zr += sB[tt * D + tid];
+                    sO[tt * D + tid] = fmaf(sDD[tt], zr, cs_parts<D>(sY, tt, tid));
+                }
+            } else {
+                for (int tt = nt - 1; tt >= 0; --tt) {
+                    zr = fmaf(sDD[tt], sB[tt * D + tid], zr);
+                    sO[tt * D + tid] = cs_parts<D>(sY, tt, tid) + zr;
+                }
+            }
+        }
+        __syncthreads();
+        cs_write<D>(outg, sO, t0, nt);  // (the next block's staging leaves sO alone)
+    }
+    if (REV) {
+        if (Mend) cs_store_row<D>(s, Mend, own, cw);
+        if (mend && tid < D) mend[tid] = zr;
+    }
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
+la_cumsum_bwd_sweeps_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, const T* dO,
+                            const float* dS_out, const float* dz_out, const float* R0, T* dq, T* dk, T* dv,
+                            float* dS0, float* dz0, const float* ws_inv, const float* ws_dd, int C)
+{
+    extern __shared__ __align__(16) float smf[];
+    const size_t g = blockIdx.x / 3;
+    const int part = (int)(blockIdx.x % 3);
     const T* qg = q + g * (size_t)C * D;
     const T* kg = k + g * (size_t)C * D;
     const T* vg = v + g * (size_t)C * D;
     const T* gg = dO + g * (size_t)C * D;
-    const float* winv = ws_inv + g * (size_t)C;
-    const float* wdd = ws_dd + g * (size_t)C;
-    if (tid == 0) {
-        cs_prefetch<D>(vg, C);
-        cs_prefetch<D>(gg, C);
-        cs_prefetch<D>(kg, C);
+    const size_t gx = g * (size_t)C * D, gS = g * D * D, gz = g * D;
+    if (threadIdx.x == 0) {  // the first block of the sweep (the last one for parts 0 and 2)
+        const int r0 = part == 1 ? 0 : max(0, C - 128);
+        cs_prefetch<D>(gg, r0, C);
+        cs_prefetch<D>(part == 0 ? kg : vg, r0, C);
+        cs_prefetch<D>(part == 1 ? kg : qg, r0, C);
     }
     pdl_wait();
-    float s[Cf::OW][CL];
-    cs_load_row<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
-    float zr = (tid < D && z0) ? z0[g * D + tid] : 0.f;  // z[p = tid] (forward), then r[p] (reverse)
-    // v, dO, k, this thread's row's 1/den and (threads t < TB) dd of token t, for the block
-    // about to be staged
-    const int row = cs_row<D, T>();
-    const int nblk = (C + TB - 1) / TB;
-    CsShare<D, T> ra, rx, rb;
-    float inv = 0.f, dd = 0.f;
-    auto fetch = [&](const T* a, const T* x, const T* b, int t0, int nt) {
-        cs_fetch<D>(ra, a, t0, nt);
-        cs_fetch<D>(rx, x, t0, nt);
-        cs_fetch<D>(rb, b, t0, nt);
-        inv = row < nt ? winv[t0 + row] : 0.f;
-        dd = tid < nt ? wdd[t0 + tid] : 0.f;
-    };
-    // ---- forward sweep: S += k v^T, z += k (inclusive); dq = S dn + dd z
-    if (nblk > 0) fetch(vg, gg, kg, 0, min(TB, C));
-    for (int t0 = 0; t0 < C; t0 += TB) {
-        const int nt = min(TB, C - t0);
-        cs_put<D>(sA, ra, 1.f);
-        cs_put<D>(sX, rx, inv);  // dn = dO / den
-        cs_put<D>(sB, rb, 1.f);
-        if (tid < TB) sDD[tid] = dd;
-        __syncthreads();
-        if (t0 + TB < C) fetch(vg, gg, kg, t0 + TB, min(TB, C - t0 - TB));  // passes under this block's work
-        cs_sweep<D, false>(s, sA, sX, sB, sY, nt, own, cw);
-        __syncthreads();
-        if (tid < D)
-            for (int tt = 0; tt < nt; ++tt) {
-                zr += sB[tt * D + tid];
-                sO[tt * D + tid] = fmaf(sDD[tt], zr, cs_parts<D>(sY, tt, tid));
-            }
-        __syncthreads();
-        cs_write<D>(dq + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
-    }
-    // ---- reverse sweep: R += q dn^T, r += dd q (inclusive); dk = R v + r
-    cs_load_row<D>(s, dS_out ? dS_out + g * D * D : nullptr, own, cw);
-    zr = (tid < D && dz_out) ? dz_out[g * D + tid] : 0.f;
-    if (nblk > 0) fetch(gg, vg, qg, (nblk - 1) * TB, C - (nblk - 1) * TB);
-    for (int bi = nblk - 1; bi >= 0; --bi) {
-        const int t0 = bi * TB, nt = min(TB, C - t0);
-        cs_put<D>(sA, ra, inv);  // dn = dO / den
-        cs_put<D>(sX, rx, 1.f);
-        cs_put<D>(sB, rb, 1.f);
-        if (tid < TB) sDD[tid] = dd;
-        __syncthreads();
-        if (bi > 0) fetch(gg, vg, qg, t0 - TB, TB);  // passes under this block's work
-        cs_sweep<D, true>(s, sA, sX, sB, sY, nt, own, cw);
-        __syncthreads();
-        if (tid < D)
-            for (int tt = nt - 1; tt >= 0; --tt) {
-                zr = fmaf(sDD[tt], sB[tt * D + tid], zr);
-                sO[tt * D + tid] = cs_parts<D>(sY, tt, tid) + zr;
-            }
-        __syncthreads();
-        cs_write<D>(dk + g * (size_t)C * D, sO, t0, nt);  // (the next block's staging leaves sO alone)
-    }
-    __syncthreads();
-    if (dS0) cs_store_row<D>(s, dS0 + g * D * D, own, cw);
-    if (dz0 && tid < D) dz0[g * D + tid] = zr;
+    const float* winv = ws_inv + g * (size_t)C;
+    const float* wdd = ws_dd + g * (size_t)C;
+    if (part == 0)
+        cs_bwd_dv<D, T>(smf, qg, kg, gg, R0 ? R0 + gS : nullptr, winv, dv + gx, C);
+    else if (part == 1)
+        cs_bwd_row<D, T, false>(smf, qg, kg, vg, gg, S0 ? S0 + gS : nullptr, z0 ? z0 + gz : nullptr, winv, wdd,
+                                dq + gx, nullptr, nullptr, C);
+    else
+        cs_bwd_row<D, T, true>(smf, qg, kg, vg, gg, dS_out ? dS_out + gS : nullptr, dz_out ? dz_out + gz : nullptr,
+                               winv, wdd, dk + gx, dS0 ? dS0 + gS : nullptr, dz0 ? dz0 + gz : nullptr, C);
 }
 
 }  // namespace la

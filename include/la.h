@@ -213,8 +213,10 @@ la_status la_chunked_bwd_split(const void* q, const void* k, const void* v,
  * the block size (there are no blocks).  D 64 or 128; float32 or bfloat16; any C >= 0.
  *
  * la_cumsum_bwd_workspace_bytes: the device workspace la_cumsum_bwd needs: two float32
- * values per token (1/den and dd, passed from the first kernel to the second); 0 for an
- * invalid shape.  No CUDA call.
+ * values per token (1/den and dd, passed from the first kernel to the second), rounded up
+ * to a multiple of four, then D * D float32 per group (a copy of dS_out, used when dS0 is
+ * dS_out itself: the second kernel's sweeps run side by side, and the one that reads dS_out
+ * must not see dS0 written); 0 when C = 0 or for an invalid shape.  No CUDA call.
  *
  * la_cumsum_bwd: arguments, layouts, in-place carry gradients and errors as
  * la_chunked_bwd, without the block size; workspace is caller-owned DEVICE memory,

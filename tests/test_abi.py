@@ -253,9 +253,11 @@ def test_cumsum_backward_checks_arguments_first(L, kw, status):
 
 
 def test_cumsum_workspace_bytes_closed_form(L):
-    """Two fp32 values per token: 1/den and dd."""
-    for G, C, D, dt in ((160, 128, 64, 1), (3, 200, 128, 0), (0, 5, 64, 1), (4, 0, 64, 1)):
-        assert la.la_cumsum_bwd_workspace_bytes(G, C, D, dt) == 2 * G * C * 4
+    """Two fp32 values per token (1/den and dd), rounded up to a multiple of four, then one
+    D x D fp32 copy of dS_out per group; nothing for an empty chunk."""
+    for G, C, D, dt in ((160, 128, 64, 1), (3, 200, 128, 0), (0, 5, 64, 1), (4, 0, 64, 1), (3, 33, 64, 1)):
+        want = 0 if C == 0 else ((2 * G * C + 3) // 4 * 4 + G * D * D) * 4
+        assert la.la_cumsum_bwd_workspace_bytes(G, C, D, dt) == want
     assert la.la_cumsum_bwd_workspace_bytes(2, 8, 96, 1) == 0
 
 

@@ -68,9 +68,12 @@ def test_cumsum_empty_chunk_passes_the_carry_through():
     assert torch.equal(dS0.cpu(), x.dS_out) and torch.equal(dz0.cpu(), x.dz_out)
 
 
-def test_cumsum_in_place_carries():
-    """S_out over S0, z_out over z0 (forward); dS0 over dS_out, dz0 over dz_out (backward)."""
-    x = make_inputs(4, 150, 64, dtype="bf16", seed=9, carry=True, grads=True)
+@pytest.mark.parametrize("G,C,D,dtype", [(4, 150, 64, "bf16"), (3, 33, 128, "f32")])
+def test_cumsum_in_place_carries(G, C, D, dtype):
+    """S_out over S0, z_out over z0 (forward); dS0 over dS_out, dz0 over dz_out (backward:
+    the dv sweep then reads the workspace's copy of dS_out, which starts on a 16-byte
+    boundary after the 2 G C per-token values, 198 floats in the second case)."""
+    x = make_inputs(G, C, D, dtype=dtype, seed=9, carry=True, grads=True)
     d = x.to(DEV)
     S, z = d.S0.clone(), d.z0.clone()
     got = la.cumsum_fwd(d.q, d.k, d.v, S, z, eps=EPS, S_out=S, z_out=z)
@@ -78,8 +81,8 @@ def test_cumsum_in_place_carries():
     out = (torch.empty_like(d.q), torch.empty_like(d.q), torch.empty_like(d.q), dS, dz)
     gotb = la.cumsum_bwd(d.q, d.k, d.v, d.S0, d.z0, d.dO, dS, dz, eps=EPS, out=out)
     torch.cuda.synchronize()
-    check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), "bf16", FWD_NAMES)
-    check(gotb, oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS), "bf16", BWD_NAMES)
+    check(got, oracle.fwd(x.q, x.k, x.v, x.S0, x.z0, eps=EPS), dtype, FWD_NAMES)
+    check(gotb, oracle.bwd(x.q, x.k, x.v, x.S0, x.z0, x.dO, x.dS_out, x.dz_out, eps=EPS), dtype, BWD_NAMES)
 
 
 def test_cumsum_agrees_with_the_chunked_kernels():
