@@ -265,13 +265,15 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     } else if (warp == 8) {
         // =================================================== producer (one lane)
         if (lane == 0) {
-            auto load = [&](int b) {
+            auto load_qk = [&](int b) {
                 mbar_expect_tx(bar_qk, L::HALF_BYTES);
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
                     tma_load_3d(sm + L::QT + a * 16384, &tq, bar_qk, 64 * a, rbase + b * 128, (int)g);
                     tma_load_3d(sm + L::KT + a * 16384, &tk, bar_qk, 64 * a, rbase + b * 128, (int)g);
                 }
+            };
+            auto load_vg = [&](int b) {
                 mbar_expect_tx(bar_vg, L::HALF_BYTES);
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
@@ -280,7 +282,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
             };
             auto tile_of = [&](int it) { return it < nsb ? it : 2 * nsb - 1 - it; };
-            load(tile_of(it0));
+            load_qk(tile_of(it0));
+            load_vg(tile_of(it0));
             pdl_launch_dependents();
 
             // K-major operands: +32 B (2 units) per K = 16 step inside a 64-column atom, the
@@ -294,25 +297,15 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t id_dd = idesc_bf16(D, D, true, true);        // D x D, both MN-major
             auto kstep = [](uint64_t d, int kk) { return d + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2); };
 
-            bool ok = true;
-            for (int it = it0; it < it1 && ok; ++it) {
-                const bool p1 = it < nsb;
-                const uint32_t par = (it - it0) & 1;
-                // descriptors derived per tile from an opaque copy of the base address, so the
-                // compiler cannot hoist every unrolled instruction's operands out of the loop
+            // M1 of tile `it` (its Q and K landed with phase `par` of bar_qk): A = Q K^T
+            auto round1 = [&](int it, uint32_t par) {
                 uint32_t b0 = sbase;
                 asm volatile("" : "+r"(b0));
-                const uint64_t dQ = smem_desc(b0 + L::QT, 16, 1024), dQm = smem_desc(b0 + L::QT, 16384, 1024);
-                const uint64_t dK = smem_desc(b0 + L::KT, 16, 1024), dKm = smem_desc(b0 + L::KT, 16384, 1024);
-                const uint64_t dV = smem_desc(b0 + L::VT, 16, 1024), dVm = smem_desc(b0 + L::VT, 16384, 1024);
-                const uint64_t dG = smem_desc(b0 + L::GN, 16, 1024), dGm = smem_desc(b0 + L::GN, 16384, 1024);
-                const uint64_t dAk = smem_desc(b0 + L::AD, 16, 1024), dAm = smem_desc(b0 + L::AD, 16384, 1024);
-                const uint64_t dS = smem_desc(b0 + L::SR, 16, 1024), dRm = smem_desc(b0 + L::SR, L::SR_ATOM, 1024);
-                ok = mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA);
-                if (!ok) break;
+                const uint64_t dQ = smem_desc(b0 + L::QT, 16, 1024), dK = smem_desc(b0 + L::KT, 16, 1024);
+                if (!mbar_wait(bar_qk, par, ERR_TIMEOUT_TMA)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < KD; ++kk)  // M1: A = Q K^T
+                for (int kk = 0; kk < KD; ++kk)
                     umma_bf16(tmem + L::T_SC, kstep(dQ, kk), kstep(dK, kk), id_sq, kk > 0);
                 umma_commit(bar_m1);
                 if constexpr (D == 64) {
@@ -326,6 +319,22 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         tma_prefetch_3d(&tv, 0, rbase + nb * 128, (int)g);
                     }
                 }
+                return true;
+            };
+            bool ok = round1(it0, 0);
+            for (int it = it0; it < it1 && ok; ++it) {
+                const bool p1 = it < nsb;
+                const uint32_t par = (it - it0) & 1;
+                // descriptors derived per tile from an opaque copy of the base address, so the
+                // compiler cannot hoist every unrolled instruction's operands out of the loop
+                uint32_t b0 = sbase;
+                asm volatile("" : "+r"(b0));
+                const uint64_t dQ = smem_desc(b0 + L::QT, 16, 1024), dQm = smem_desc(b0 + L::QT, 16384, 1024);
+                const uint64_t dK = smem_desc(b0 + L::KT, 16, 1024), dKm = smem_desc(b0 + L::KT, 16384, 1024);
+                const uint64_t dV = smem_desc(b0 + L::VT, 16, 1024), dVm = smem_desc(b0 + L::VT, 16384, 1024);
+                const uint64_t dG = smem_desc(b0 + L::GN, 16, 1024), dGm = smem_desc(b0 + L::GN, 16384, 1024);
+                const uint64_t dAk = smem_desc(b0 + L::AD, 16, 1024), dAm = smem_desc(b0 + L::AD, 16384, 1024);
+                const uint64_t dS = smem_desc(b0 + L::SR, 16, 1024), dRm = smem_desc(b0 + L::SR, L::SR_ATOM, 1024);
                 ok = mbar_wait(bar_e1, par, ERR_TIMEOUT_MMA) && mbar_wait(bar_vg, par, ERR_TIMEOUT_TMA);
                 if (!ok) break;
                 tc_fence_after();
@@ -378,14 +387,28 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         umma_bf16(tmem + L::T_ST, dQm + kk * 128, dGm + kk * 128, id_dd, true);
                 }
                 umma_commit(bar_m3);
+                // The next tile's Q and K as soon as this third round has read them (the
+                // epilogue's last reads of Q and K come before bar_e2), and its scores (T_SC:
+                // its P was read before bar_e2) computed under this tile's last epilogue; dO
+                // and V once that epilogue is done (pass 2 stages dk in dN's buffer).  Pass 2 starts on the tile pass 1
+                // ended with: its Q, K, V and dN are still in place.
+                const bool more = it + 1 < it1, keep = it + 1 == nsb && it0 == 0;
+                if (more) {
+                    ok = mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
+                    if (!ok) break;
+                    if (keep)
+                        mbar_arrive(bar_qk);
+                    else
+                        load_qk(tile_of(it + 1));
+                    ok = round1(it + 1, par ^ 1u);  // the next tile's scores, under this epilogue
+                    if (!ok) break;
+                }
                 ok = mbar_wait(bar_e3, par, ERR_TIMEOUT_MMA);
-                if (ok && it + 1 < it1) {
-                    if (it + 1 == nsb && it0 == 0) {  // pass 2 starts on the tile pass 1 ended with:
-                        mbar_arrive(bar_qk);          // its Q, K, V and dN are still in place
+                if (ok && more) {
+                    if (keep)
                         mbar_arrive(bar_vg);
-                    } else {
-                        load(tile_of(it + 1));
-                    }
+                    else
+                        load_vg(tile_of(it + 1));
                 }
             }
         }
@@ -400,6 +423,42 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // layout puts row 16 q + l in lane l < 16 of quarter q
         const bool srow = D == 128 || lane < 16;
         const int prow = D == 128 ? t : 16 * q4 + lane;
+        // per-warp sums over the tile's 128 rows of a bf16 tile's columns, optionally
+        // weighted per row: thread (cc, rg) sums D/16 rows x 8 columns, then the warp's rows
+        auto column_sums = [&](uint32_t tile, const float* wrow, float* part) {
+            constexpr int CH = D / 8, RPG = CH / 2;
+            const int cc = tid % CH, rg = tid / CH;
+            float s[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[e] = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < RPG; ++rr) {
+                const int row = rg * RPG + rr;
+                const float w = wrow ? wrow[row] : 1.f;
+                const uint4 u = *reinterpret_cast<const uint4*>(sm + tile + chunk_at(row, cc, 16384));
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    s[2 * e] = fmaf(w, f.x, s[2 * e]);
+                    s[2 * e + 1] = fmaf(w, f.y, s[2 * e + 1]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (CH == 8) s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
+                s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
+            }
+            if (lane < CH)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[warp * D + 8 * cc + e] = s[e];
+        };
+        auto warp_total = [&](const float* part, int c) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += part[w * D + c];
+            return v;
+        };
         for (int it = it0; it < it1; ++it) {
             const bool p1 = it < nsb;
             const int b = p1 ? it : 2 * nsb - 1 - it;
@@ -509,9 +568,18 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 *p4 = u;
             }
+            if (!p1 && hh == 0) ddt[t] = parked.y;  // (pass 2: dd is known here)
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_e1);
+            // column sums of this tile, under the second round: pass 1, z after the tile =
+            // z + sum_j k_j; pass 2, r before the tile = r + sum_i dd_i q_i
+            if (p1) {
+                column_sums(L::KT, nullptr, zpart);
+            } else {
+                epi_sync256();  // every row's dd is in ddt
+                column_sums(L::QT, ddt, zpart);
+            }
 
             // ---- E2: dd (pass 1: -(dN . AV + q . U) / den; pass 2: parked), this half of
             //      dA -> AD atom hh (over A)
@@ -557,75 +625,21 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             } else {
                 dd = parked.y;
             }
-            if (hh == 0) ddt[t] = dd;  // for the weighted column sums of pass 2 (read after a barrier)
+            if (p1 && hh == 0) ddt[t] = dd;  // for a piece's weighted column sums (read after a barrier)
             // a row past the chunk's end has dN = 0 (so P = 0) and dd = 0: zero unmasked
             stage_masked(std::true_type{}, dd);
+            if (p1 && mode == 1) {  // the piece's sum of dd_i q_i (Q is reloaded once the third round is done)
+                epi_sync256();      // every row's dd is in ddt
+                column_sums(L::QT, ddt, zpart2);
+            }
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_e2);
-            if (!p1) {  // dv -> staging in KT (its last reader, K R, is done) -> TMA store
-#pragma unroll
-                for (int h2 = 0; h2 < HC / 32; ++h2) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::T_DV + hh * HC + 32 * h2, r);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(sm + L::KT + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
-                            pack8(r + 8 * q, 1.f);
-                }
-                fence_async_smem();
-                epi_sync256();
-                if (tid == 0) {
-#pragma unroll
-                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdv, sm + L::KT + a * 16384, 64 * a, row0, (int)g);
-                    tma_store_commit();
-                }
-            }
 
             // ---- E3
-            // per-warp sums over the tile's 128 rows of a bf16 tile's columns, optionally
-            // weighted per row: thread (cc, rg) sums D/16 rows x 8 columns, then the warp's rows
-            auto column_sums = [&](uint32_t tile, const float* wrow, float* part) {
-                constexpr int CH = D / 8, RPG = CH / 2;
-                const int cc = tid % CH, rg = tid / CH;
-                float s[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] = 0.f;
-#pragma unroll
-                for (int rr = 0; rr < RPG; ++rr) {
-                    const int row = rg * RPG + rr;
-                    const float w = wrow ? wrow[row] : 1.f;
-                    const uint4 u = *reinterpret_cast<const uint4*>(sm + tile + chunk_at(row, cc, 16384));
-                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(h2[e]);
-                        s[2 * e] = fmaf(w, f.x, s[2 * e]);
-                        s[2 * e + 1] = fmaf(w, f.y, s[2 * e + 1]);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (CH == 8) s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
-                    s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
-                }
-                if (lane < CH)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) part[warp * D + 8 * cc + e] = s[e];
-            };
-            auto warp_total = [&](const float* part, int c) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) v += part[w * D + c];
-                return v;
-            };
             mbar_wait(bar_m3, par, ERR_TIMEOUT_MMA);
             tc_fence_after();
             if (p1) {
-                if (mode == 1) {  // the piece's sum of dd_i q_i
-                    epi_sync256();  // every row's dd is in ddt
-                    column_sums(L::QT, ddt, zpart2);
-                }
                 // dq = U + dA K + dd z -> staging in AD (dA's last reader, dq += dA K, is done)
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {
@@ -639,7 +653,6 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         *reinterpret_cast<uint4*>(sm + L::AD + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
                             pack8(r + 8 * q, 1.f);
                 }
-                column_sums(L::KT, nullptr, zpart);  // z after the tile = z + sum_j k_j
                 // S after the tile -> bf16 operand for the next tile (the state update is its own group)
                 mbar_wait(bar_m2b, par, ERR_TIMEOUT_MMA);
                 tc_fence_after();
@@ -679,7 +692,16 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         *reinterpret_cast<uint4*>(sm + L::GN + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
                             pack8(r + 8 * q, 1.f);
                 }
-                column_sums(L::QT, ddt, zpart);  // r before the tile = r + sum_i dd_i q_i
+                // dv -> staging in AD (dA's last reader, the third round, is done)
+#pragma unroll
+                for (int h2 = 0; h2 < HC / 32; ++h2) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::T_DV + hh * HC + 32 * h2, r);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(sm + L::AD + chunk_at(t, hh * HCH + 4 * h2 + q, 16384)) =
+                            pack8(r + 8 * q, 1.f);
+                }
                 // R before the tile -> bf16 operand for the next (earlier) tile; after tile 0: dS0
 #pragma unroll
                 for (int h2 = 0; h2 < HC / 32; ++h2) {
@@ -705,10 +727,13 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 fence_async_smem();
                 fence_async_global();  // the parked values were read before the dk store overwrites them
                 tc_fence_before();
-                epi_sync256();  // dk staging and column partials complete; every dk has read r
+                epi_sync256();  // dk, dv staging complete; every dk has read r
                 if (tid == 0) {
 #pragma unroll
-                    for (int a = 0; a < NA; ++a) tma_store_3d(&tdk, sm + L::GN + a * 16384, 64 * a, row0, (int)g);
+                    for (int a = 0; a < NA; ++a) {
+                        tma_store_3d(&tdk, sm + L::GN + a * 16384, 64 * a, row0, (int)g);
+                        tma_store_3d(&tdv, sm + L::AD + a * 16384, 64 * a, row0, (int)g);
+                    }
                     tma_store_commit();
                 }
                 if (tid < D) {
@@ -716,8 +741,8 @@ la_bwd_tcm_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     if (b == 0 && dz0) dz0[g * D + tid] = rz[tid];
                 }
             }
-            epi_sync256();                        // z / r updated before the next tile reads them
-            if (tid == 0) tma_store_wait_read();  // staging read before the tile buffers are reloaded
+            if (tid == 0) tma_store_wait_read();  // staging read before the tile buffers are reused
+            epi_sync256();  // z / r updated and the staging read, before the next tile (its scores may be done)
             mbar_arrive(bar_e3);
         }
         if (mode == 1) {
