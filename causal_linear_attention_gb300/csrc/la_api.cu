@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -785,6 +786,7 @@ extern "C" la_status la_cumsum_bwd(const void* q, const void* k, const void* v, 
 {
     la_status st = check_bwd(q, k, v, S0, z0, dO, dS_out, dz_out, dq, dk, dv, dS0, dz0, G, C, D, 64, dtype, eps);
     if (st != LA_OK) return st;
+    if (G > INT_MAX / 3) return LA_ERR_UNSUPPORTED;  // the second launch has three CTAs per group
     if (G == 0) return LA_OK;
     const size_t need = cumsum_bwd_ws_bytes(G, C, D);
     if (need > 0) {

@@ -222,7 +222,8 @@ la_status la_chunked_bwd_split(const void* q, const void* k, const void* v,
  * la_chunked_bwd, without the block size; workspace is caller-owned DEVICE memory,
  * 16-byte aligned, at least la_cumsum_bwd_workspace_bytes(G, C, D, dtype) bytes and
  * disjoint from every tensor (LA_ERR_INVALID otherwise; NULL is fine when C = 0).  Two
- * kernels are enqueued on `stream`; the library allocates nothing.
+ * kernels are enqueued on `stream`, the second with three CTAs per group (G above
+ * 715,827,882 returns LA_ERR_UNSUPPORTED); the library allocates nothing.
  */
 la_status la_cumsum_fwd(const void* q, const void* k, const void* v,
                         const float* S0, const float* z0,

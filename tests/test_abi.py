@@ -241,6 +241,7 @@ def test_cumsum_forward_checks_arguments_first(L, kw, status):
     (dict(G=-1), INVALID), (dict(dq=None), INVALID), (dict(dk=A + 8), INVALID), (dict(D=48), UNSUPPORTED),
     (dict(dq=A), INVALID), (dict(workspace=None), INVALID), (dict(workspace_bytes=64), INVALID),
     (dict(workspace=0x20000008), INVALID), (dict(workspace=A), INVALID),  # misaligned; overlaps q
+    (dict(G=715827883, C=0), UNSUPPORTED),  # three CTAs per group would overflow the grid
 ])
 def test_cumsum_backward_checks_arguments_first(L, kw, status):
     base = {n: A + i * 0x100000 for i, n in enumerate(("q", "k", "v", "dO", "dq", "dk", "dv"))}
