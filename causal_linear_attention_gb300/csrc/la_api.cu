@@ -712,17 +712,33 @@ size_t cumsum_bwd_ws_bytes(int G, int C, int D)
     return C > 0 ? (cumsum_bwd_copy_offset(G, C) + (size_t)G * D * D) * 4 : 0;
 }
 
+template <class Cf, typename T>
+la_status cumsum_fwd_launch_cfg(const void* q, const void* k, const void* v, const float* S0, const float* z0,
+                                void* o, float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
+{
+    static OptIn flag;
+    auto kern = la::la_cumsum_fwd_kernel<Cf, T>;
+    const la_status st = prepare(kern, flag, Cf::SMEM);
+    if (st != LA_OK) return st;
+    return launch_pdl(kern, Cf::SPLIT * G, Cf::THREADS, Cf::SMEM, stream, static_cast<const T*>(q),
+                      static_cast<const T*>(k), static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out, z_out, C,
+                      eps);
+}
+
+// Two CTAs per group, each owning half the state columns, where that pays (measured): at head
+// size 128 (256-thread CTAs, three to an SM, against one 512-thread CTA), and at 64 when the
+// two still get an SM each (few groups); at 64 a half has one owner column per lane, so its
+// sweep loads twice the shared-memory values per FMA, which costs as much as the second CTA
+// gains once the SMs are full.  One CTA per group also when z_out is z0 itself, since every
+// CTA of a group reads z0.
 template <int D, typename T>
 la_status cumsum_fwd_launch(const void* q, const void* k, const void* v, const float* S0, const float* z0, void* o,
                             float* S_out, float* z_out, int G, int C, float eps, cudaStream_t stream)
 {
-    using Cf = la::CumsumCfg<D>;
-    static OptIn flag;
-    auto kern = la::la_cumsum_fwd_kernel<D, T>;
-    const la_status st = prepare(kern, flag, Cf::SMEM);
-    if (st != LA_OK) return st;
-    return launch_pdl(kern, G, Cf::THREADS, Cf::SMEM, stream, static_cast<const T*>(q), static_cast<const T*>(k),
-                      static_cast<const T*>(v), S0, z0, static_cast<T*>(o), S_out, z_out, C, eps);
+    const bool split = !(z_out && z_out == z0) && G <= INT_MAX / 2 && (D == 128 || 2 * G <= sm_count());
+    if (!split)
+        return cumsum_fwd_launch_cfg<la::CumsumCfg<D>, T>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, stream);
+    return cumsum_fwd_launch_cfg<la::CumsumFwdCfg<D>, T>(q, k, v, S0, z0, o, S_out, z_out, G, C, eps, stream);
 }
 
 template <int D, typename T>

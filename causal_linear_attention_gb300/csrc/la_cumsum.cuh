@@ -13,14 +13,17 @@
 //     R_t = dS_out + sum_{i >= t} q_i dn_i^T,  r_t = dz_out + sum_{i >= t} dd_i q_i
 //     dk_t = R_t v_t + r_t,  dv_t = R_t^T k_t,  dS0 = R_0,  dz0 = r_0
 //
-// One CTA per group.  A D x D state is spread over the CTA as (owners, slice): lane l of
-// warp (ow, cw) owns o = 64 ow + l and o + 32 and holds, for each, the CL = D / NC entries
+// The backward's sweeps run one CTA per group; the forward one or two, each then owning half
+// the state columns (both form the denominators, which need all of q, k and z; 256-thread
+// CTAs, three to an SM).  A D x D state (or a CTA's columns of it) is spread over the CTA as
+// (owners, slice): lane l of warp (ow, cw) owns column o = 32 OW ow + l (and o + 32 when
+// OW = 2: a CTA owning 64 columns or more) and holds, for each, the CL = D / NC entries
 // whose contracted index lies in slice cw.  "Column layout" (owner = value index c,
 // contracted = key index p) serves o = S^T q and dv = R^T k; "row layout" (owner = p,
 // contracted = c) serves dq = S dn and dk = R v.  Per token every lane reads the same CL
 // contracted values (one broadcast per 16 bytes, each serving both owners: the sweep is
 // bound by shared-memory loads, so two owners per lane halve them per FMA), updates its
-// 2 CL entries and sums its slice of both readouts; the NC slice partials meet in shared
+// OW CL entries and sums its slice of its readouts; the NC slice partials meet in shared
 // memory once per block of TB tokens, where the parts
 // that are sequential in the token but not in the state (the denominators, the z and r
 // prefixes, the dO . n dots) are also formed.  Tokens are staged TB at a time as fp32
@@ -38,17 +41,25 @@
 
 namespace la {
 
-template <int D>
+// A CTA's layout: SPLIT CTAs per group, each owning DO = D / SPLIT state columns (the
+// backward's sweeps: SPLIT = 1; the forward: SPLIT = 2, so that three CTAs fit an SM and a
+// launch of G groups fills the SMs evenly).
+template <int D, int SPLIT_ = 1>
 struct CumsumCfg {
-    static constexpr int OW = 2;                      // owners per lane: o and o + 32
-    static constexpr int NOW = D / (32 * OW);         // owner warps
+    static constexpr int DIM = D;
+    static constexpr int SPLIT = SPLIT_;
+    static constexpr int DO = D / SPLIT;              // owners (state columns) per CTA
+    static constexpr int OW = DO >= 64 ? 2 : 1;       // owners per lane: o (and o + 32)
+    static constexpr int NOW = DO / (32 * OW);        // owner warps
     static constexpr int CL = D == 64 ? 8 : 16;       // contracted entries per lane and owner
     static constexpr int NC = D / CL;                 // contracted slices
-    static constexpr int THREADS = 32 * NOW * NC;     // 256 at D = 64, 512 at D = 128
+    static constexpr int THREADS = 32 * NOW * NC;     // 256, or 512 at D = 128 unsplit
     static constexpr int TB = D == 64 ? 32 : 16;      // tokens per staging block
-    // shared memory (floats): A, X, B, O [TB][D] + Y [NC][TB][D] + inv, dd [TB]
-    static constexpr size_t SMEM = ((size_t)(4 + NC) * TB * D + 2 * TB) * 4;
+    // shared memory (floats): A, X, B, O [TB][D] + Y [NC][TB][DO] + inv, dd [TB]
+    static constexpr size_t SMEM = ((size_t)4 * TB * D + (size_t)NC * TB * DO + 2 * TB) * 4;
+    static_assert(DO % (32 * OW) == 0 && D <= THREADS && 8 * TB <= THREADS, "layout");
 };
+template <int D> using CumsumFwdCfg = CumsumCfg<D, 2>;
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
@@ -89,20 +100,22 @@ template <> struct Elem<__nv_bfloat16> {
 // One thread's share of a staged block: elements [E tid, E tid + E) of the TB x D values
 // of rows t0 .. t0 + TB - 1 (contiguous in the group's [C][D] tensor), held as loaded, so
 // that a load issued for the next block passes under the current block's work.
-template <int D, typename T>
+template <class Cf, typename T>
 struct CsShare {
-    static constexpr int E = CumsumCfg<D>::TB * D / CumsumCfg<D>::THREADS;  // 8 at D = 64, 4 at D = 128
+    static constexpr int D = Cf::DIM;
+    static constexpr int E = Cf::TB * D / Cf::THREADS;  // 8, or 4 at D = 128 with 512 threads
     static constexpr int WORDS = E * (int)sizeof(T) / 4;
-    static_assert(E * CumsumCfg<D>::THREADS == CumsumCfg<D>::TB * D && D % E == 0, "whole rows per block");
+    static_assert(E * Cf::THREADS == Cf::TB * D && D % E == 0, "whole rows per block");
     uint32_t w[WORDS];
 };
 
 // Issue the loads of this thread's share of rows t0 .. t0 + nt - 1; elements of rows >= nt
 // are zero.  The row of this thread's elements is E tid / D.
-template <int D, typename T>
-__device__ __forceinline__ void cs_fetch(CsShare<D, T>& r, const T* src, int t0, int nt)
+template <class Cf, typename T>
+__device__ __forceinline__ void cs_fetch(CsShare<Cf, T>& r, const T* src, int t0, int nt)
 {
-    using Sh = CsShare<D, T>;
+    using Sh = CsShare<Cf, T>;
+    constexpr int D = Cf::DIM;
     const int i = Sh::E * (int)threadIdx.x;
     const bool in = i < nt * D;
     const T* p = src + (size_t)t0 * D + i;
@@ -127,10 +140,10 @@ __device__ __forceinline__ void cs_fetch(CsShare<D, T>& r, const T* src, int t0,
 
 // This thread's share -> dst[TB][D] fp32, times `scale` (bf16 is the upper half of an fp32
 // word, so widening is a shift).
-template <int D, typename T>
-__device__ __forceinline__ void cs_put(float* dst, const CsShare<D, T>& r, float scale)
+template <class Cf, typename T>
+__device__ __forceinline__ void cs_put(float* dst, const CsShare<Cf, T>& r, float scale)
 {
-    using Sh = CsShare<D, T>;
+    using Sh = CsShare<Cf, T>;
     float f[Sh::E];
 #pragma unroll
     for (int n = 0; n < Sh::WORDS; ++n) {
@@ -154,8 +167,8 @@ __device__ __forceinline__ void cs_put(float* dst, const CsShare<D, T>& r, float
 }
 
 // The row of a block this thread's share lies in.
-template <int D, typename T>
-__device__ __forceinline__ int cs_row() { return CsShare<D, T>::E * (int)threadIdx.x / D; }
+template <class Cf, typename T>
+__device__ __forceinline__ int cs_row() { return CsShare<Cf, T>::E * (int)threadIdx.x / Cf::DIM; }
 
 // Start rows r0 .. of a group's tensor (up to 128 of them, not past C) towards L2 (before
 // the wait for the previous kernel: a prefetch hands nothing to this kernel, and the loads
@@ -167,18 +180,19 @@ __device__ __forceinline__ void cs_prefetch(const T* src, int r0, int C)
     if (r0 >= 0 && C - r0 > 0) tc::prefetch_l2(src + (size_t)r0 * D, rows * D * (uint32_t)sizeof(T));
 }
 
-// src[TB][D] fp32 rows 0 .. nt - 1 -> rows t0 .. of one group's [C][D] output tensor.
-template <int D, typename T>
-__device__ __forceinline__ void cs_write(T* dst, const float* src, int t0, int nt)
+// src[TB][DO] fp32 rows 0 .. nt - 1 -> columns c0 .. c0 + DO - 1 of rows t0 .. of one
+// group's [C][D] output tensor.
+template <class Cf, typename T>
+__device__ __forceinline__ void cs_write(T* dst, const float* src, int t0, int nt, int c0 = 0)
 {
-    constexpr int PER_ROW = D / 8;
-    for (int i = threadIdx.x; i < nt * PER_ROW; i += CumsumCfg<D>::THREADS) {
+    constexpr int D = Cf::DIM, DO = Cf::DO, PER_ROW = DO / 8;
+    for (int i = threadIdx.x; i < nt * PER_ROW; i += Cf::THREADS) {
         const int row = i / PER_ROW, c8 = i % PER_ROW;
         float f[8];
-        const float4* s4 = reinterpret_cast<const float4*>(src + row * D + 8 * c8);
+        const float4* s4 = reinterpret_cast<const float4*>(src + row * DO + 8 * c8);
         const float4 a = s4[0], b = s4[1];
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-        Elem<T>::store8(dst + (size_t)(t0 + row) * D + 8 * c8, f);
+        Elem<T>::store8(dst + (size_t)(t0 + row) * D + c0 + 8 * c8, f);
     }
 }
 
@@ -211,24 +225,24 @@ __device__ __forceinline__ void cs_token(float (&s)[OW][CL], const float* a, con
 }
 
 // The block's tokens through this lane's state, in order (REV: from the last); owner u is
-// own + 32 u, its readout part -> sY[cw][tt][own + 32 u].
-template <int D, bool REV>
-__device__ __forceinline__ void cs_sweep(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* sA,
-                                         const float* sX, const float* sB, float* sY, int nt, int own, int cw)
+// own + 32 u of the CTA's columns (c0 + own + 32 u of the state), its readout part ->
+// sY[cw][tt][own + 32 u].
+template <class Cf, bool REV>
+__device__ __forceinline__ void cs_sweep(float (&s)[Cf::OW][Cf::CL], const float* sA, const float* sX,
+                                         const float* sB, float* sY, int nt, int own, int cw, int c0 = 0)
 {
-    using Cf = CumsumCfg<D>;
-    constexpr int CL = Cf::CL, TB = Cf::TB, OW = Cf::OW;
-    float* y = sY + cw * TB * D + own;
+    constexpr int D = Cf::DIM, DO = Cf::DO, CL = Cf::CL, TB = Cf::TB, OW = Cf::OW;
+    float* y = sY + cw * TB * DO + own;
     const float* a = sA + cw * CL;
     const float* x = sX + cw * CL;
-    const float* b = sB + own;
+    const float* b = sB + c0 + own;
     auto token = [&](int tt) {
         float bv[OW], yv[OW];
 #pragma unroll
         for (int u = 0; u < OW; ++u) bv[u] = b[tt * D + 32 * u];
         cs_token<CL, OW>(s, a + tt * D, x + tt * D, bv, yv);
 #pragma unroll
-        for (int u = 0; u < OW; ++u) y[tt * D + 32 * u] = yv[u];
+        for (int u = 0; u < OW; ++u) y[tt * DO + 32 * u] = yv[u];
     };
     if (!REV) {
 #pragma unroll 2
@@ -239,34 +253,31 @@ __device__ __forceinline__ void cs_sweep(float (&s)[CumsumCfg<D>::OW][CumsumCfg<
     }
 }
 
-// A D x D matrix <-> this lane's state.  Column layout: s[u][i] = M[p = cw CL + i][own + 32 u]
-// (lanes read consecutive columns); row layout: s[u][i] = M[own + 32 u][c = cw CL + i]
-// (16-byte pieces of a row).  A NULL source is zero.
-template <int D>
-__device__ __forceinline__ void cs_load_col(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* M, int own,
-                                            int cw)
+// A D x D matrix <-> this lane's state.  Column layout: s[u][i] = M[p = cw CL + i][c0 + own +
+// 32 u] (lanes read consecutive columns; c0 the CTA's first column); row layout: s[u][i] =
+// M[own + 32 u][c = cw CL + i] (16-byte pieces of a row).  A NULL source is zero.
+template <class Cf>
+__device__ __forceinline__ void cs_load_col(float (&s)[Cf::OW][Cf::CL], const float* M, int own, int cw, int c0 = 0)
 {
-    using Cf = CumsumCfg<D>;
+    constexpr int D = Cf::DIM;
 #pragma unroll
     for (int u = 0; u < Cf::OW; ++u)
 #pragma unroll
-        for (int i = 0; i < Cf::CL; ++i) s[u][i] = M ? M[(size_t)(cw * Cf::CL + i) * D + own + 32 * u] : 0.f;
+        for (int i = 0; i < Cf::CL; ++i) s[u][i] = M ? M[(size_t)(cw * Cf::CL + i) * D + c0 + own + 32 * u] : 0.f;
 }
-template <int D>
-__device__ __forceinline__ void cs_store_col(const float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], float* M, int own,
-                                             int cw)
+template <class Cf>
+__device__ __forceinline__ void cs_store_col(const float (&s)[Cf::OW][Cf::CL], float* M, int own, int cw, int c0 = 0)
 {
-    using Cf = CumsumCfg<D>;
+    constexpr int D = Cf::DIM;
 #pragma unroll
     for (int u = 0; u < Cf::OW; ++u)
 #pragma unroll
-        for (int i = 0; i < Cf::CL; ++i) M[(size_t)(cw * Cf::CL + i) * D + own + 32 * u] = s[u][i];
+        for (int i = 0; i < Cf::CL; ++i) M[(size_t)(cw * Cf::CL + i) * D + c0 + own + 32 * u] = s[u][i];
 }
-template <int D>
-__device__ __forceinline__ void cs_load_row(float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], const float* M, int own,
-                                            int cw)
+template <class Cf>
+__device__ __forceinline__ void cs_load_row(float (&s)[Cf::OW][Cf::CL], const float* M, int own, int cw)
 {
-    using Cf = CumsumCfg<D>;
+    constexpr int D = Cf::DIM;
 #pragma unroll
     for (int u = 0; u < Cf::OW; ++u)
 #pragma unroll
@@ -276,11 +287,10 @@ __device__ __forceinline__ void cs_load_row(float (&s)[CumsumCfg<D>::OW][CumsumC
             s[u][i] = f.x; s[u][i + 1] = f.y; s[u][i + 2] = f.z; s[u][i + 3] = f.w;
         }
 }
-template <int D>
-__device__ __forceinline__ void cs_store_row(const float (&s)[CumsumCfg<D>::OW][CumsumCfg<D>::CL], float* M, int own,
-                                             int cw)
+template <class Cf>
+__device__ __forceinline__ void cs_store_row(const float (&s)[Cf::OW][Cf::CL], float* M, int own, int cw)
 {
-    using Cf = CumsumCfg<D>;
+    constexpr int D = Cf::DIM;
 #pragma unroll
     for (int u = 0; u < Cf::OW; ++u)
 #pragma unroll
@@ -289,128 +299,15 @@ __device__ __forceinline__ void cs_store_row(const float (&s)[CumsumCfg<D>::OW][
                 make_float4(s[u][i], s[u][i + 1], s[u][i + 2], s[u][i + 3]);
 }
 
-// sum of the NC slice parts of token tt, owner o
-template <int D>
+// sum of the NC slice parts of token tt, owner o (of the CTA's DO)
+template <class Cf>
 __device__ __forceinline__ float cs_parts(const float* sY, int tt, int o)
 {
-    using Cf = CumsumCfg<D>;
     float v = 0.f;
 #pragma unroll
-    for (int c = 0; c < Cf::NC; ++c) v += sY[(c * Cf::TB + tt) * D + o];
+    for (int c = 0; c < Cf::NC; ++c) v += sY[(c * Cf::TB + tt) * Cf::DO + o];
     return v;
 }
-
-// 1/den of the block's tokens -> sInv[0 .. nt): threads p < D carry z[p] (zl) across blocks
-// and write q_t[p] z_t[p] into scratch[TB][D]; eight threads per token then sum its row.
-// Ends with the CTA synchronised.
-template <int D>
-__device__ __forceinline__ void cs_denominators(const float* sK, const float* sQ, float* scratch, float* sInv, int nt,
-                                                float& zl, float eps)
-{
-    const int tid = threadIdx.x;
-    if (tid < D) {
-        float kv[CumsumCfg<D>::TB];
-#pragma unroll
-        for (int tt = 0; tt < CumsumCfg<D>::TB; ++tt) kv[tt] = tt < nt ? sK[tt * D + tid] : 0.f;
-#pragma unroll
-        for (int tt = 0; tt < CumsumCfg<D>::TB; ++tt) {
-            zl += kv[tt];  // inclusive of token t (padding adds zero)
-            if (tt < nt) scratch[tt * D + tid] = sQ[tt * D + tid] * zl;
-        }
-    }
-    __syncthreads();
-    // row sums, eight threads per token: thread j of token t adds the float4s at 4 j + 32 m
-    // (a quarter warp reads 128 contiguous bytes), then the eight meet by shuffles
-    constexpr int TB = CumsumCfg<D>::TB;
-    static_assert(8 * TB % 32 == 0 && 8 * TB <= CumsumCfg<D>::THREADS, "whole warps of eight threads per token");
-    if (tid < 8 * TB) {
-        const int t = tid >> 3, j = tid & 7;
-        const float* r = scratch + t * D + 4 * j;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < D / 32; ++m) {
-            const float4 f = *reinterpret_cast<const float4*>(r + 32 * m);
-            acc += (f.x + f.y) + (f.z + f.w);
-        }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        if (j == 0 && t < nt) sInv[t] = 1.f / (acc + eps);
-    }
-    __syncthreads();
-}
-
-// ---------------------------------------------------------------- forward
-// Column layout: s[u][i] = S[p = cw CL + i][c = own + 32 u].  S_out may be S0 and z_out z0: every entry
-// is read and written back by the same thread, after a barrier.
-template <int D, typename T>
-__global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
-la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, T* o, float* S_out,
-                     float* z_out, int C, float eps)
-{
-    using Cf = CumsumCfg<D>;
-    constexpr int TB = Cf::TB, CL = Cf::CL;
-    extern __shared__ __align__(16) float smf[];
-    float* sK = smf;
-    float* sQ = sK + TB * D;
-    float* sV = sQ + TB * D;
-    float* sO = sV + TB * D;       // q z products, then the outputs
-    float* sY = sO + TB * D;       // [NC][TB][D]
-    float* sInv = sY + Cf::NC * TB * D;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
-    const size_t g = blockIdx.x;
-    const T* qg = q + g * (size_t)C * D;
-    const T* kg = k + g * (size_t)C * D;
-    const T* vg = v + g * (size_t)C * D;
-    if (tid == 0) {
-        cs_prefetch<D>(kg, 0, C);
-        cs_prefetch<D>(qg, 0, C);
-        cs_prefetch<D>(vg, 0, C);
-    }
-    pdl_wait();
-    float s[Cf::OW][CL];
-    cs_load_col<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
-    float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
-    CsShare<D, T> rk, rq, rv;  // the block about to be staged
-    cs_fetch<D>(rk, kg, 0, min(TB, C));
-    cs_fetch<D>(rq, qg, 0, min(TB, C));
-    cs_fetch<D>(rv, vg, 0, min(TB, C));
-    for (int t0 = 0; t0 < C; t0 += TB) {
-        const int nt = min(TB, C - t0);
-        cs_put<D>(sK, rk, 1.f);
-        cs_put<D>(sQ, rq, 1.f);
-        cs_put<D>(sV, rv, 1.f);
-        __syncthreads();
-        if (t0 + TB < C) {  // the next block's loads pass under this block's work
-            const int nn = min(TB, C - t0 - TB);
-            cs_fetch<D>(rk, kg, t0 + TB, nn);
-            cs_fetch<D>(rq, qg, t0 + TB, nn);
-            cs_fetch<D>(rv, vg, t0 + TB, nn);
-        }
-        cs_denominators<D>(sK, sQ, sO, sInv, nt, zl, eps);
-        cs_sweep<D, false>(s, sK, sQ, sV, sY, nt, own, cw);
-        __syncthreads();
-        for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = cs_parts<D>(sY, i / D, i % D) * sInv[i / D];
-        __syncthreads();
-        cs_write<D>(o + g * (size_t)C * D, sO, t0, nt);
-    }
-    __syncthreads();  // every thread has read its S0 / z0 entries before any is overwritten
-    if (S_out) cs_store_col<D>(s, S_out + g * D * D, own, cw);
-    if (z_out && tid < D) z_out[g * D + tid] = zl;
-}
-
-// ---------------------------------------------------------------- backward
-// la_cumsum_bwd_scan_kernel (one CTA per group, column layout) runs the forward sweep:
-// n_t = S_t^T q_t and den_t -> 1/den_t and dd_t = -(dO_t . n_t) / den_t^2 of every token into
-// ws_inv / ws_dd ([G][C] fp32).  The three sweeps left need only those and nothing from one
-// another, so la_cumsum_bwd_sweeps_kernel runs them side by side, three CTAs per group:
-//   part 0, column layout, reverse: R from dS_out, dv_t = R_t^T k_t;
-//   part 1, row layout, forward: dq_t = S_t dn_t + dd_t z_t (z from z0);
-//   part 2, row layout, reverse: dk_t = R_t v_t + r_t, dS0 = R_0, dz0 = r_0 (r from dz_out).
-// dS0 may be dS_out itself: part 2 writes dS0 when it ends, and part 0 of the same group
-// need not have read dS_out by then, so the scan kernel first copies dS_out into the
-// workspace (R0copy) and part 0 reads the copy.
 
 // Sum of row t = tid / 8 of rows[TB][D] (shared memory) by threads 8 t .. 8 t + 7 (whole
 // warps, threads < 8 TB): thread j adds the float4s at 4 j + 32 m (a quarter warp reads 128
@@ -430,6 +327,112 @@ __device__ __forceinline__ float cs_row_sum8(const float* rows)
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     return acc;
 }
+
+// 1/den of the block's tokens -> sInv[0 .. nt): threads p < D carry z[p] (zl) across blocks
+// and write q_t[p] z_t[p] into scratch[TB][D]; eight threads per token then sum its row.
+// Ends with the CTA synchronised.
+template <class Cf>
+__device__ __forceinline__ void cs_denominators(const float* sK, const float* sQ, float* scratch, float* sInv, int nt,
+                                                float& zl, float eps)
+{
+    constexpr int D = Cf::DIM;
+    const int tid = threadIdx.x;
+    if (tid < D) {
+        float kv[Cf::TB];
+#pragma unroll
+        for (int tt = 0; tt < Cf::TB; ++tt) kv[tt] = tt < nt ? sK[tt * D + tid] : 0.f;
+#pragma unroll
+        for (int tt = 0; tt < Cf::TB; ++tt) {
+            zl += kv[tt];  // inclusive of token t (padding adds zero)
+            if (tt < nt) scratch[tt * D + tid] = sQ[tt * D + tid] * zl;
+        }
+    }
+    __syncthreads();
+    // row sums, eight threads per token
+    constexpr int TB = Cf::TB;
+    static_assert(8 * TB % 32 == 0 && 8 * TB <= Cf::THREADS, "whole warps of eight threads per token");
+    if (tid < 8 * TB) {
+        const float acc = cs_row_sum8<D>(scratch);
+        const int t = tid >> 3;
+        if ((tid & 7) == 0 && t < nt) sInv[t] = 1.f / (acc + eps);
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- forward
+// Cf::SPLIT CTAs per group; CTA h owns the state columns c0 = h DO .. c0 + DO - 1 and writes
+// those columns of o and S_out; every CTA forms the denominators itself (they need all of q,
+// k, z), and CTA 0 writes z_out.  Column layout: s[u][i] = S[p = cw CL + i][c = c0 + own +
+// 32 u].  S_out may be S0: every entry is read and written back by the same thread, after a
+// barrier.  z_out may be z0 only with one CTA per group (the other CTAs read z0).
+template <class Cf, typename T>
+__global__ void __launch_bounds__(Cf::THREADS, Cf::SPLIT == 1 ? 1 : (Cf::DIM == 128 && sizeof(T) == 4 ? 2 : 3))
+la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const float* z0, T* o, float* S_out,
+                     float* z_out, int C, float eps)
+{
+    constexpr int D = Cf::DIM, DO = Cf::DO, TB = Cf::TB, CL = Cf::CL;
+    extern __shared__ __align__(16) float smf[];
+    float* sK = smf;
+    float* sQ = sK + TB * D;
+    float* sV = sQ + TB * D;
+    float* sO = sV + TB * D;       // q z products [TB][D], then the outputs [TB][DO]
+    float* sY = sO + TB * D;       // [NC][TB][DO]
+    float* sInv = sY + Cf::NC * TB * DO;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
+    const size_t g = blockIdx.x / Cf::SPLIT;
+    const int c0 = (int)(blockIdx.x % Cf::SPLIT) * DO;
+    const T* qg = q + g * (size_t)C * D;
+    const T* kg = k + g * (size_t)C * D;
+    const T* vg = v + g * (size_t)C * D;
+    if (tid == 0) {
+        cs_prefetch<D>(kg, 0, C);
+        cs_prefetch<D>(qg, 0, C);
+        cs_prefetch<D>(vg, 0, C);
+    }
+    pdl_wait();
+    float s[Cf::OW][CL];
+    cs_load_col<Cf>(s, S0 ? S0 + g * D * D : nullptr, own, cw, c0);
+    float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
+    CsShare<Cf, T> rk, rq, rv;  // the block about to be staged
+    cs_fetch<Cf>(rk, kg, 0, min(TB, C));
+    cs_fetch<Cf>(rq, qg, 0, min(TB, C));
+    cs_fetch<Cf>(rv, vg, 0, min(TB, C));
+    for (int t0 = 0; t0 < C; t0 += TB) {
+        const int nt = min(TB, C - t0);
+        cs_put<Cf>(sK, rk, 1.f);
+        cs_put<Cf>(sQ, rq, 1.f);
+        cs_put<Cf>(sV, rv, 1.f);
+        __syncthreads();
+        if (t0 + TB < C) {  // the next block's loads pass under this block's work
+            const int nn = min(TB, C - t0 - TB);
+            cs_fetch<Cf>(rk, kg, t0 + TB, nn);
+            cs_fetch<Cf>(rq, qg, t0 + TB, nn);
+            cs_fetch<Cf>(rv, vg, t0 + TB, nn);
+        }
+        cs_denominators<Cf>(sK, sQ, sO, sInv, nt, zl, eps);
+        cs_sweep<Cf, false>(s, sK, sQ, sV, sY, nt, own, cw, c0);
+        __syncthreads();
+        for (int i = tid; i < nt * DO; i += Cf::THREADS) sO[i] = cs_parts<Cf>(sY, i / DO, i % DO) * sInv[i / DO];
+        __syncthreads();
+        cs_write<Cf>(o + g * (size_t)C * D, sO, t0, nt, c0);
+    }
+    __syncthreads();  // every thread has read its S0 / z0 entries before any is overwritten
+    if (S_out) cs_store_col<Cf>(s, S_out + g * D * D, own, cw, c0);
+    if (z_out && c0 == 0 && tid < D) z_out[g * D + tid] = zl;
+}
+
+// ---------------------------------------------------------------- backward
+// la_cumsum_bwd_scan_kernel (one CTA per group, column layout) runs the forward sweep:
+// n_t = S_t^T q_t and den_t -> 1/den_t and dd_t = -(dO_t . n_t) / den_t^2 of every token into
+// ws_inv / ws_dd ([G][C] fp32).  The three sweeps left need only those and nothing from one
+// another, so la_cumsum_bwd_sweeps_kernel runs them side by side, three CTAs per group:
+//   part 0, column layout, reverse: R from dS_out, dv_t = R_t^T k_t;
+//   part 1, row layout, forward: dq_t = S_t dn_t + dd_t z_t (z from z0);
+//   part 2, row layout, reverse: dk_t = R_t v_t + r_t, dS0 = R_0, dz0 = r_0 (r from dz_out).
+// dS0 may be dS_out itself: part 2 writes dS0 when it ends, and part 0 of the same group
+// need not have read dS_out by then, so the scan kernel first copies dS_out into the
+// workspace (R0copy) and part 0 reads the copy.
 
 template <int D, typename T>
 __global__ void __launch_bounds__(CumsumCfg<D>::THREADS)
@@ -467,31 +470,31 @@ la_cumsum_bwd_scan_kernel(const T* q, const T* k, const T* v, const float* S0, c
         for (int i = tid; i < D * D / 4; i += Cf::THREADS) dst[i] = src[i];
     }
     float s[Cf::OW][CL];
-    cs_load_col<D>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
+    cs_load_col<Cf>(s, S0 ? S0 + g * D * D : nullptr, own, cw);
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
-    CsShare<D, T> ra, rx, rb, rg;  // k, q, v of the block about to be staged; dO of the current one
-    cs_fetch<D>(ra, kg, 0, min(TB, C));
-    cs_fetch<D>(rx, qg, 0, min(TB, C));
-    cs_fetch<D>(rb, vg, 0, min(TB, C));
+    CsShare<Cf, T> ra, rx, rb, rg;  // k, q, v of the block about to be staged; dO of the current one
+    cs_fetch<Cf>(ra, kg, 0, min(TB, C));
+    cs_fetch<Cf>(rx, qg, 0, min(TB, C));
+    cs_fetch<Cf>(rb, vg, 0, min(TB, C));
     for (int t0 = 0; t0 < C; t0 += TB) {
         const int nt = min(TB, C - t0);
-        cs_put<D>(sA, ra, 1.f);
-        cs_put<D>(sX, rx, 1.f);
-        cs_put<D>(sB, rb, 1.f);
+        cs_put<Cf>(sA, ra, 1.f);
+        cs_put<Cf>(sX, rx, 1.f);
+        cs_put<Cf>(sB, rb, 1.f);
         __syncthreads();
-        cs_fetch<D>(rg, gg, t0, nt);
+        cs_fetch<Cf>(rg, gg, t0, nt);
         if (t0 + TB < C) {  // the next block's loads pass under this block's work
             const int nn = min(TB, C - t0 - TB);
-            cs_fetch<D>(ra, kg, t0 + TB, nn);
-            cs_fetch<D>(rx, qg, t0 + TB, nn);
-            cs_fetch<D>(rb, vg, t0 + TB, nn);
+            cs_fetch<Cf>(ra, kg, t0 + TB, nn);
+            cs_fetch<Cf>(rx, qg, t0 + TB, nn);
+            cs_fetch<Cf>(rb, vg, t0 + TB, nn);
         }
-        cs_denominators<D>(sA, sX, sO, sInv, nt, zl, eps);
-        cs_sweep<D, false>(s, sA, sX, sB, sY, nt, own, cw);
+        cs_denominators<Cf>(sA, sX, sO, sInv, nt, zl, eps);
+        cs_sweep<Cf, false>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();  // every slice of every owner has read v
-        cs_put<D>(sB, rg, 1.f);  // dO
+        cs_put<Cf>(sB, rg, 1.f);  // dO
         __syncthreads();
-        for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = sB[i] * cs_parts<D>(sY, i / D, i % D);
+        for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = sB[i] * cs_parts<Cf>(sY, i / D, i % D);
         __syncthreads();
         if (tid < 8 * TB) {
             const float dot = cs_row_sum8<D>(sO);
@@ -522,29 +525,29 @@ __device__ __forceinline__ void cs_bwd_dv(float* smf, const T* qg, const T* kg, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     float s[Cf::OW][CL];
-    cs_load_col<D>(s, R0, own, cw);
-    const int row = cs_row<D, T>(), nblk = (C + TB - 1) / TB;
-    CsShare<D, T> ra, rx, rg;  // q, k, dO of the block about to be staged, and its row's 1/den
+    cs_load_col<Cf>(s, R0, own, cw);
+    const int row = cs_row<Cf, T>(), nblk = (C + TB - 1) / TB;
+    CsShare<Cf, T> ra, rx, rg;  // q, k, dO of the block about to be staged, and its row's 1/den
     float inv = 0.f;
     auto fetch = [&](int t0, int nt) {
-        cs_fetch<D>(ra, qg, t0, nt);
-        cs_fetch<D>(rx, kg, t0, nt);
-        cs_fetch<D>(rg, gg, t0, nt);
+        cs_fetch<Cf>(ra, qg, t0, nt);
+        cs_fetch<Cf>(rx, kg, t0, nt);
+        cs_fetch<Cf>(rg, gg, t0, nt);
         inv = row < nt ? winv[t0 + row] : 0.f;
     };
     if (nblk > 0) fetch((nblk - 1) * TB, C - (nblk - 1) * TB);
     for (int bi = nblk - 1; bi >= 0; --bi) {
         const int t0 = bi * TB, nt = min(TB, C - t0);
-        cs_put<D>(sA, ra, 1.f);
-        cs_put<D>(sX, rx, 1.f);
-        cs_put<D>(sB, rg, inv);  // dn = dO / den
+        cs_put<Cf>(sA, ra, 1.f);
+        cs_put<Cf>(sX, rx, 1.f);
+        cs_put<Cf>(sB, rg, inv);  // dn = dO / den
         __syncthreads();
         if (bi > 0) fetch(t0 - TB, TB);  // the previous (whole) block passes under this one's work
-        cs_sweep<D, true>(s, sA, sX, sB, sY, nt, own, cw);
+        cs_sweep<Cf, true>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
-        for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = cs_parts<D>(sY, i / D, i % D);
+        for (int i = tid; i < nt * D; i += Cf::THREADS) sO[i] = cs_parts<Cf>(sY, i / D, i % D);
         __syncthreads();
-        cs_write<D>(dvg, sO, t0, nt);  // (the next block's staging leaves sO alone)
+        cs_write<Cf>(dvg, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
 }
 
@@ -569,15 +572,15 @@ __device__ __forceinline__ void cs_bwd_row(float* smf, const T* qg, const T* kg,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int own = 32 * Cf::OW * (warp % Cf::NOW) + lane, cw = warp / Cf::NOW;
     float s[Cf::OW][CL];
-    cs_load_row<D>(s, M0, own, cw);
+    cs_load_row<Cf>(s, M0, own, cw);
     float zr = (tid < D && m0) ? m0[tid] : 0.f;
-    const int row = cs_row<D, T>(), nblk = (C + TB - 1) / TB;
-    CsShare<D, T> ra, rx, rb;  // the block about to be staged, its row's 1/den, dd of token tid
+    const int row = cs_row<Cf, T>(), nblk = (C + TB - 1) / TB;
+    CsShare<Cf, T> ra, rx, rb;  // the block about to be staged, its row's 1/den, dd of token tid
     float inv = 0.f, dd = 0.f;
     auto fetch = [&](int t0, int nt) {
-        cs_fetch<D>(ra, REV ? gg : vg, t0, nt);
-        cs_fetch<D>(rx, REV ? vg : gg, t0, nt);
-        cs_fetch<D>(rb, REV ? qg : kg, t0, nt);
+        cs_fetch<Cf>(ra, REV ? gg : vg, t0, nt);
+        cs_fetch<Cf>(rx, REV ? vg : gg, t0, nt);
+        cs_fetch<Cf>(rb, REV ? qg : kg, t0, nt);
         inv = row < nt ? winv[t0 + row] : 0.f;
         dd = tid < nt ? wdd[t0 + tid] : 0.f;
     };
@@ -585,35 +588,35 @@ __device__ __forceinline__ void cs_bwd_row(float* smf, const T* qg, const T* kg,
     for (int n = 0; n < nblk; ++n) {
         const int bi = REV ? nblk - 1 - n : n;
         const int t0 = bi * TB, nt = min(TB, C - t0);
-        cs_put<D>(sA, ra, REV ? inv : 1.f);  // dn = dO / den
-        cs_put<D>(sX, rx, REV ? 1.f : inv);
-        cs_put<D>(sB, rb, 1.f);
+        cs_put<Cf>(sA, ra, REV ? inv : 1.f);  // dn = dO / den
+        cs_put<Cf>(sX, rx, REV ? 1.f : inv);
+        cs_put<Cf>(sB, rb, 1.f);
         if (tid < TB) sDD[tid] = dd;
         __syncthreads();
         if (n + 1 < nblk) {  // the next block in sweep order passes under this one's work
             const int tn = REV ? t0 - TB : t0 + TB;
             fetch(tn, min(TB, C - tn));
         }
-        cs_sweep<D, REV>(s, sA, sX, sB, sY, nt, own, cw);
+        cs_sweep<Cf, REV>(s, sA, sX, sB, sY, nt, own, cw);
         __syncthreads();
         if (tid < D) {
             if (!REV) {
                 for (int tt = 0; tt < nt; ++tt) {
                     zr += sB[tt * D + tid];
-                    sO[tt * D + tid] = fmaf(sDD[tt], zr, cs_parts<D>(sY, tt, tid));
+                    sO[tt * D + tid] = fmaf(sDD[tt], zr, cs_parts<Cf>(sY, tt, tid));
                 }
             } else {
                 for (int tt = nt - 1; tt >= 0; --tt) {
                     zr = fmaf(sDD[tt], sB[tt * D + tid], zr);
-                    sO[tt * D + tid] = cs_parts<D>(sY, tt, tid) + zr;
+                    sO[tt * D + tid] = cs_parts<Cf>(sY, tt, tid) + zr;
                 }
             }
         }
         __syncthreads();
-        cs_write<D>(outg, sO, t0, nt);  // (the next block's staging leaves sO alone)
+        cs_write<Cf>(outg, sO, t0, nt);  // (the next block's staging leaves sO alone)
     }
     if (REV) {
-        if (Mend) cs_store_row<D>(s, Mend, own, cw);
+        if (Mend) cs_store_row<Cf>(s, Mend, own, cw);
         if (mend && tid < D) mend[tid] = zr;
     }
 }
