@@ -391,6 +391,7 @@ la_cumsum_fwd_kernel(const T* q, const T* k, const T* v, const float* S0, const 
         cs_prefetch<D>(vg, 0, C);
     }
     pdl_wait();
+    pdl_launch_dependents();  // the next kernel's CTAs may start, prefetch and wait
     float s[Cf::OW][CL];
     cs_load_col<Cf>(s, S0 ? S0 + g * D * D : nullptr, own, cw, c0);
     float zl = (tid < D && z0) ? z0[g * D + tid] : 0.f;
@@ -464,6 +465,7 @@ la_cumsum_bwd_scan_kernel(const T* q, const T* k, const T* v, const float* S0, c
         cs_prefetch<D>(gg, 0, C);
     }
     pdl_wait();
+    pdl_launch_dependents();  // the next kernel's CTAs may start, prefetch and wait
     if (R0copy) {  // dS0 is dS_out: the reverse column sweep reads this copy
         const float4* src = reinterpret_cast<const float4*>(dS_out + g * D * D);
         float4* dst = reinterpret_cast<float4*>(R0copy + g * D * D);
@@ -642,6 +644,7 @@ la_cumsum_bwd_sweeps_kernel(const T* q, const T* k, const T* v, const float* S0,
         cs_prefetch<D>(part == 1 ? kg : qg, r0, C);
     }
     pdl_wait();
+    pdl_launch_dependents();  // the next kernel's CTAs may start, prefetch and wait
     const float* winv = ws_inv + g * (size_t)C;
     const float* wdd = ws_dd + g * (size_t)C;
     if (part == 0)
