@@ -56,6 +56,7 @@ la_ce_lse_merge_kernel(const float* pm, const float* ps, const float* tl, int ns
                        const int* y, float* lse, float* row_loss)
 {
     pdl_wait();
+    pdl_launch_dependents();  // the next kernel's CTAs may start and wait
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (i >= nc) return;
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(1024) la_ce_mean_kernel(const float* row_loss,
 {
     __shared__ float part[1024];
     pdl_wait();
+    pdl_launch_dependents();
     float s = 0.f;
     for (int i = threadIdx.x; i < N; i += 1024) s += row_loss[i];
     part[threadIdx.x] = s;
@@ -194,6 +196,9 @@ la_ce_persist_kernel(const __grid_constant__ CUtensorMap th, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tslot;
     pdl_wait();
+    // forward: the merge kernel may start and wait (measured: a gain); backward: not (the
+    // GEMM after it, and the next chunk's launches, were slower started early)
+    if constexpr (MODE == 0) pdl_launch_dependents();
 
     if (warp == 4) {
         if (lane == 0) {  // TMA producer: every (tile, k-slice) of this CTA, in order

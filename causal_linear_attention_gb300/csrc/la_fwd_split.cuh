@@ -499,6 +499,7 @@ la_state_scan_kernel(const float* init_S, const float* init_z, float* delta, flo
     constexpr int NB = scan_blocks(D);
     __shared__ float tot[SCAN_MAXW][32];
     pdl_wait();
+    pdl_launch_dependents();  // the pieces' kernel may start, prefetch and wait
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int e = ((int)blockIdx.x % NB) * 32 + lane;
     const size_t g = blockIdx.x / NB;
