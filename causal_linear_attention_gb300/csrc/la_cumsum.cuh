@@ -63,12 +63,7 @@ template <int D> using CumsumFwdCfg = CumsumCfg<D, 2>;
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
-    // 8 consecutive elements -> fp32
-    __device__ static void load8(const float* p, float (&f)[8])
-    {
-        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-    }
+    // 8 fp32 values -> 8 consecutive elements
     __device__ static void store8(float* p, const float (&f)[8])
     {
         reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
@@ -76,17 +71,6 @@ template <> struct Elem<float> {
     }
 };
 template <> struct Elem<__nv_bfloat16> {
-    __device__ static void load8(const __nv_bfloat16* p, float (&f)[8])
-    {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 x = __bfloat1622float2(h[e]);
-            f[2 * e] = x.x;
-            f[2 * e + 1] = x.y;
-        }
-    }
     __device__ static void store8(__nv_bfloat16* p, const float (&f)[8])
     {
         uint4 u;
