@@ -48,6 +48,7 @@ def fwd_bwd(G, C, D, dtype, seed, carry=True, upstream=True):
     (5, 33, 64, "bf16"),      # one token past a staging block
     (2, 1, 64, "f32"),        # one token
     (2, 1000, 64, "bf16"),    # several staging blocks, ragged
+    (160, 128, 128, "bf16"),  # wide heads over many groups: two forward CTAs per group, three per SM
 ])
 def test_cumsum_matches_oracle(G, C, D, dtype):
     fwd_bwd(G, C, D, dtype, seed=G * 1000 + C)
