@@ -287,7 +287,7 @@ def test_bounded_wait_gives_up_and_the_device_stays_usable():
 
 @pytest.mark.parametrize("G,C,D", [(2, 4096, 64), (8, 1000, 64), (1, 300, 64), (3, 2048, 64),
                                    (2, 4096, 128), (8, 1000, 128), (1, 300, 128), (1, 8192, 128), (3, 2000, 128),
-                                   (1, 5000, 64), (1, 12800, 128)])
+                                   (1, 5000, 64), (1, 12800, 128), (8, 8192, 128)])
 def test_chunk_parallel_forward(G, C, D):
     """la_chunked_fwd_split (pieces on separate CTAs, carries from a prefix over the
     pieces' sums) matches the oracle, and the sequential kernel within the bf16 bounds."""
@@ -346,7 +346,7 @@ def test_chunk_parallel_forward_falls_back_and_threads_carry_in_place():
 
 @pytest.mark.parametrize("G,C,D", [(2, 4096, 64), (8, 1000, 64), (1, 300, 64), (3, 2048, 64), (1, 16384, 64),
                                    (2, 4096, 128), (8, 1000, 128), (1, 300, 128), (3, 2000, 128), (1, 8192, 128),
-                                   (1, 5000, 64), (1, 12800, 128)])
+                                   (1, 5000, 64), (1, 12800, 128), (8, 8192, 128)])
 def test_chunk_parallel_backward(G, C, D):
     """la_chunked_bwd_split (forward carries from a prefix over the pieces, carry gradients
     from a reverse prefix) matches the oracle, and the sequential kernel within the bf16
